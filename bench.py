@@ -1,0 +1,430 @@
+"""Benchmark: selective diagonal scan, forward + backward, on one GB300 per rank.
+
+A step is one pass of the whole path over one batch of the largest workload:
+B=16 T=2048 D=5120 DS=16, bf16 I/O, float32 state and gradients, checkpoints
+every 256 steps: the forward (y, hT, checkpoints) then the backward (gx,
+gdelta, gA, gb, gc, gh0). Inputs are seeded synthetic tensors of that shape
+(gen.make_inputs); every input tensor is larger than L2, so no flush is
+needed between steps. ``value`` is B*T*D*DS elements per second of
+forward+backward over all ranks (weak scaling: every rank runs its own copy).
+
+Also reported: the device time of each kernel group (CUDA events on the launch
+stream), the roofline of the dominant kernel, an end-to-end number through the
+public API with host buffers (H2D of the inputs and D2H of all outputs inside
+the timed region), SM clocks sampled during the timed region, the float64 CPU
+oracle timed on a bounded sample (cpu_baseline), and one-line timings of the
+other two large workloads (bf16 forward B=8 T=4096 D=1536; float32 forward
+B=1 T=65536 D=2048 as 16 chained calls of 4096 steps).
+
+--impl reference times the float64 oracle (the only other implementation of
+the method here) on a bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import gen  # noqa: E402
+
+WORKLOAD = 5
+METRIC = "scan elements/s (B*T*D*DS) fwd+bwd"
+UNIT = "elem/s"
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------- algorithmic work per element
+
+def compulsory_bytes(w, direction):
+    """Bytes the step must move at least once (inputs read, outputs written)."""
+    s = gen.io_bytes(w.io)
+    btd, bts, ds = w.B * w.T * w.D, w.B * w.T * w.DS, w.D * w.DS
+    state = w.B * w.D * w.DS * 4
+    nck = gen.ceil_div(w.T, w.ckpt_interval) if w.ckpt_interval else 0
+    if direction == "fwd":   # x, delta in; y out; b, c in; A in; h0 (if any) in; hT out; checkpoints out
+        return btd * 3 * s + bts * 2 * s + ds * 4 + (state if w.h0_std > 0 else 0) + state + nck * state
+    # bwd: x, delta, dy in; gx, gdelta out (f32); b, c in; gb, gc out (f32); A in, gA out; ckpt in; gh0 out
+    return btd * (3 * s + 8) + bts * (2 * s + 8) + 2 * ds * 4 + nck * state + state
+
+
+# FP32-pipe operations per element the backward needs with one recompute of the
+# state from checkpoints: recompute delta*A, a*h, +delta*x*b (3); adjoint
+# dy*c, g update, a*g, p = (a g) h_{t-1}, gA, gdelta, <g,b>, gb term, gc term (9).
+BWD_OPS_PER_ELEM = 12
+FWD_EX2_PER_ELEM = 1    # one exp per element (MUFU)
+EX2_PER_SM_CLK = 32     # GB300 MUFU ex2 throughput, measured on the box
+FP32_PER_SM_CLK = 128   # FP32 FMA lanes per SM
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi SM clock / throttle-reason sampling during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+
+def oracle_sample(w, budget_s=12.0, seed=0):
+    """Time the float64 oracle (forward + backward) on the first batch and a
+    slice of channels of workload w, growing the slice until it takes about
+    budget_s seconds. Returns (elements/s, cores, description)."""
+    import oracle
+    inp = gen.make_inputs(gen.workload(WORKLOAD, B=1, D=min(w.D, 1024)), seed=seed)
+    ncols = 16
+    while True:
+        sl = slice(0, ncols)
+        args = [inp["x"][:, :, sl], inp["delta"][:, :, sl], inp["A"][sl], inp["b"], inp["c"], None]
+        t0 = time.perf_counter()
+        oracle.fwd(*args, ckpt_interval=w.ckpt_interval)
+        oracle.bwd(*args, inp["dy"][:, :, sl])
+        dt = time.perf_counter() - t0
+        if dt >= budget_s / 4 or ncols >= inp["x"].shape[2]:
+            break
+        ncols = min(inp["x"].shape[2], ncols * max(2, int(budget_s / 4 / max(dt, 1e-3))))
+    el = 1 * w.T * ncols * w.DS
+    return el / dt, oracle.threads(), f"B=1 T={w.T} D={ncols} DS={w.DS} (fwd+bwd, {dt:.1f} s)"
+
+
+# ---------------------------------------------------------------- our implementation
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import selective_state_space_03_gb300 as ssm
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = gen.workload(WORKLOAD)
+    inp = gen.make_inputs(w, seed=0)
+    el = gen.elements(w)
+    K = w.ckpt_interval
+
+    def to_dev(a):
+        if a is None:
+            return None
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(a).to(dev)
+
+    t = {k: to_dev(inp.get(k)) for k in ("x", "delta", "A", "b", "c", "h0", "dy")}
+    y, hT, ckpt = ssm.ssm_scan_fwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], ckpt_interval=K)
+    grads = ssm.ssm_scan_bwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], ckpt, t["dy"],
+                             ckpt_interval=K)
+    desc = ssm.make_desc(w.B, w.T, w.D, w.DS, ssm.SSM_IO_BF16, K, 0)
+    import ctypes
+    fwd_kernels = 2 if ssm.lib().ssm_scan_fwd_workspace_bytes(ctypes.byref(desc)) else 1
+    kernels_per_step = fwd_kernels + 1
+
+    def fwd():
+        ssm.ssm_scan_fwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], ckpt_interval=K, y=y, hT=hT,
+                         ckpt=ckpt)
+
+    def bwd():
+        ssm.ssm_scan_bwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], ckpt, t["dy"], ckpt_interval=K,
+                         grads=grads)
+
+    for _ in range(args.warmup):
+        fwd()
+        bwd()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        fwd()
+        ev[i][1].record(stream)
+        bwd()
+        ev[i][2].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    total_ms = start.elapsed_time(end)
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    if dist:
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_per_step = total_ms / args.steps
+    value = world * el * args.steps / (total_ms / 1e3)
+
+    # ---- end to end through the public API with host buffers
+    pin = {k: (torch.from_numpy(np.ascontiguousarray(inp[k]).view(np.int16)).view(torch.bfloat16)
+               if inp[k].dtype == np.uint16 else torch.from_numpy(np.ascontiguousarray(inp[k]))).pin_memory()
+           for k in ("x", "delta", "A", "b", "c", "dy")}
+    outs_h = {"y": torch.empty(y.shape, dtype=y.dtype).pin_memory(),
+              "hT": torch.empty(hT.shape, dtype=hT.dtype).pin_memory()}
+    for k, v in grads.items():
+        outs_h[k] = torch.empty(v.shape, dtype=v.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in pin.values())
+    d2h = sum(v.numel() * v.element_size() for v in outs_h.values())
+    dev_out = {"y": y, "hT": hT, **grads}
+    e2e_steps = max(2, min(args.steps, 5))
+
+    def e2e_step():
+        for k, v in pin.items():
+            t[k].copy_(v, non_blocking=True)
+        fwd()
+        bwd()
+        for k, v in outs_h.items():
+            v.copy_(dev_out[k], non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if dist:
+        tt = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+
+    # ---- other large workloads (forward only), one line each
+    extra = {}
+    if not args.no_extra:
+        extra = other_workloads(torch, ssm, dev)
+
+    if rank != 0:
+        return
+    hbm_peak, peak_kind = load_peaks()
+    sm_mhz = clk.get("sm_mhz") or 2070.0
+    fp32_peak = FP32_PER_SM_CLK * torch.cuda.get_device_properties(dev).multi_processor_count * sm_mhz * 1e6
+    ex2_peak = EX2_PER_SM_CLK * torch.cuda.get_device_properties(dev).multi_processor_count * sm_mhz * 1e6
+    bwd_ops = el * BWD_OPS_PER_ELEM / (bwd_ms / 1e3)
+    fwd_ex2 = el * FWD_EX2_PER_ELEM / (fwd_ms / 1e3)
+    fwd_bytes, bwd_bytes = compulsory_bytes(w, "fwd"), compulsory_bytes(w, "bwd")
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded Philox normals, gen.make_inputs)",
+        "config": {"workload": w.name, "B": w.B, "T": w.T, "D": w.D, "DS": w.DS, "io": w.io,
+                   "state_and_grads": "f32", "ckpt_interval": K, "l2": "inputs larger than L2 (no flush)",
+                   "parallelism": f"replicas x{world}"},
+        "kernels": {"fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+                    "fwd_elem_per_s": el / (fwd_ms / 1e3), "bwd_elem_per_s": el / (bwd_ms / 1e3),
+                    "fwd_hbm_gbs": fwd_bytes / (fwd_ms / 1e3) / 1e9, "bwd_hbm_gbs": bwd_bytes / (bwd_ms / 1e3) / 1e9,
+                    "fwd_hbm_frac": fwd_bytes / (fwd_ms / 1e3) / 1e9 / hbm_peak,
+                    "bwd_hbm_frac": bwd_bytes / (bwd_ms / 1e3) / 1e9 / hbm_peak,
+                    "fwd_ex2_frac": fwd_ex2 / ex2_peak},
+        "roofline": {"kernel": "bwd_kernel (reverse sweep with recompute)", "bound": "alu",
+                     "achieved": bwd_ops / 1e12, "peak": fp32_peak / 1e12, "unit": "TFLOP/s",
+                     "frac": bwd_ops / fp32_peak, "traffic": None,
+                     "basis": f"{BWD_OPS_PER_ELEM} FP32-pipe ops/element x {el} elements per launch; peak = "
+                              f"{FP32_PER_SM_CLK} lanes x SMs x median SM clock {sm_mhz:.0f} MHz",
+                     "hbm": {"achieved": bwd_bytes / (bwd_ms / 1e3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
+                             "frac": bwd_bytes / (bwd_ms / 1e3) / 1e9 / hbm_peak, "peak_kind": peak_kind}},
+        "e2e": {"value": el / (e2e_ms / 1e3) * world, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": kernels_per_step * args.steps,
+        "clocks": clk,
+        "other_workloads": extra,
+    }
+    if not args.no_cpu:
+        v, cores, sample = oracle_sample(w)
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
+    print(json.dumps(line), flush=True)
+
+
+def other_workloads(torch, ssm, dev):
+    out = {}
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def timed(fn, reps=5):
+        fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    def dev_t(a):
+        if a is None:
+            return None
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(a).to(dev)
+
+    w3 = gen.workload(3)
+    i3 = gen.make_inputs(w3)
+    t3 = {k: dev_t(i3.get(k)) for k in ("x", "delta", "A", "b", "c", "h0")}
+    y3, h3, _ = ssm.ssm_scan_fwd(t3["x"], t3["delta"], t3["A"], t3["b"], t3["c"], t3["h0"])
+    ms = timed(lambda: ssm.ssm_scan_fwd(t3["x"], t3["delta"], t3["A"], t3["b"], t3["c"], t3["h0"], y=y3, hT=h3))
+    out[w3.name] = {"fwd_ms": ms, "elem_per_s": gen.elements(w3) / (ms / 1e3), "l2": "flushed"}
+    del t3, y3, h3, i3
+    w4 = gen.workload(4)
+    i4 = gen.make_inputs(w4)
+    L = w4.chunk_T
+    parts = []
+    for k in range(w4.T // L):
+        sl = slice(L * k, L * (k + 1))
+        parts.append(tuple(dev_t(i4[n][:, sl]) for n in ("x", "delta", "b", "c")))
+    A4, h04 = dev_t(i4["A"]), dev_t(i4["h0"])
+    ys = [torch.empty_like(p[0]) for p in parts]
+
+    def f4():
+        h = h04
+        for (x, d, b, c), yk in zip(parts, ys):
+            _, h, _ = ssm.ssm_scan_fwd(x, d, A4, b, c, h, y=yk)
+
+    ms = timed(f4, reps=3)
+    out[w4.name] = {"fwd_ms": ms, "elem_per_s": gen.elements(w4) / (ms / 1e3), "calls": w4.T // L,
+                    "l2": "flushed before the 16 calls"}
+    return out
+
+
+# ---------------------------------------------------------------- reference arm (the oracle)
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    w = gen.workload(WORKLOAD)
+    import oracle
+    oracle.build()
+    v0, cores, sample = oracle_sample(w, budget_s=max(2.0, 40.0 / max(1, args.steps + args.warmup)))
+    # each step re-times the same bounded sample
+    inp = gen.make_inputs(gen.workload(WORKLOAD, B=1, D=min(w.D, 1024)), seed=0)
+    ncols = int(sample.split("D=")[1].split()[0])
+    sl = slice(0, ncols)
+    a = [inp["x"][:, :, sl], inp["delta"][:, :, sl], inp["A"][sl], inp["b"], inp["c"], None]
+    for _ in range(args.warmup):
+        pass  # the sizing run above already warmed the oracle
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.fwd(*a, ckpt_interval=w.ckpt_interval)
+        oracle.bwd(*a, inp["dy"][:, :, sl])
+    dt = (time.perf_counter() - t0) / args.steps
+    el = w.T * ncols * w.DS
+    v = el / dt
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded Philox normals, gen.make_inputs)",
+            "config": {"workload": w.name, "sample": f"B=1 T={w.T} D={ncols} DS={w.DS}"},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"B=1 T={w.T} D={ncols} DS={w.DS} per step (fwd+bwd)"},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extra", action="store_true", help="skip the other two workloads")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle timing")
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local_rank = int(os.environ.get("LOCAL_RANK", 0))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,132 @@
+/*
+ * ssm_scan.h: C ABI of libssm_scan.so, the selective diagonal state-space scan
+ * on one GB300 GPU (sm_103a).
+ *
+ * The operation (page "pssa_kernels.py", NSC64/pssa-100m, module docstring and
+ * `scan_reference`): for every batch b, channel d, state s and t = 0..T-1,
+ *     a_t[s]    = exp(delta[b,t,d] * A[d,s])
+ *     h_t[s]    = a_t[s] * h_{t-1}[s] + delta[b,t,d] * b[b,t,s] * x[b,t,d]
+ *     y[b,t,d]  = sum_s h_t[s] * c[b,t,s]          (reads the updated state)
+ *     hT[b,d,s] = h_{T-1}[s],   h_{-1} = h0[b,d,:]
+ * The backward (same page, `scan_bwd`) is the reverse sweep for the loss
+ * L = sum dy*y + sum ghT*hT; with g_t = dL/dh_t,
+ *     g_{T-1} = dy_{T-1} c_{T-1} + ghT,   g_t = dy_t c_t + a_{t+1} g_{t+1},
+ *     gx = delta * sum_s g b,   gdelta = sum_s (g a h_{t-1} A + g b x),
+ *     gb[b,t,s] = sum_d g delta x,   gc[b,t,s] = sum_d dy h_t,
+ *     gA[d,s] = sum_{b,t} g a h_{t-1} delta,   gh0 = a_0 g_0.
+ * Checkpoints follow the chunk-boundary retention of the ruDNN page
+ * ("src/kda/chunk.rs", `chunk_kda`): slot j holds the state entering step j*K.
+ *
+ * Layouts: every buffer is contiguous and row-major.
+ *   x, delta, y, dy              (B, T, D)   io dtype
+ *   gx, gdelta                   (B, T, D)   float32
+ *   b, c                         (B, T, DS)  io dtype
+ *   gb, gc                       (B, T, DS)  float32
+ *   A, gA                        (D, DS)     float32
+ *   h0, hT, ghT, gh0             (B, D, DS)  float32
+ *   ckpt                         (ceil(T/K), B, D, DS) float32, slot j = h entering step j*K
+ * io dtype is float32 or bf16 (selected by ssm_scan_desc.io). The state and
+ * all gradients are float32 in both cases.
+ *
+ * Ownership: the caller owns every buffer. All data pointers are DEVICE
+ * pointers on the current CUDA device and must be 16-byte aligned. The library
+ * never allocates, frees or synchronises; it only enqueues work on `stream`
+ * (a cudaStream_t passed as void*, NULL = the legacy default stream) and
+ * returns without waiting. Inputs are never written. Outputs are fully
+ * overwritten; the backward clears its own accumulation targets (gA, gb, gc).
+ *
+ * Errors: every argument is checked on the host before anything is enqueued;
+ * a failing check returns a status and enqueues nothing. Not checked (the
+ * caller's preconditions): A < 0, delta > 0, finite inputs, buffer sizes, and
+ * that buffers do not overlap. Numbers outside these preconditions give
+ * unspecified (but memory-safe) results.
+ *
+ * Supported: DS == 16; B, T, D >= 0; B <= 65535. T == 0 or B == 0 or D == 0
+ * launches no kernel: hT <- h0 (zeros if h0 is NULL), gh0 <- ghT (zeros if
+ * NULL), gA <- 0, as the ruDNN page's `chunk_kda` returns the initial state for
+ * an empty sequence.
+ */
+#ifndef SSM_SCAN_H
+#define SSM_SCAN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* dtype of x, delta, b, c, y and dy */
+typedef enum { SSM_IO_F32 = 0, SSM_IO_BF16 = 1 } ssm_io_dtype;
+
+typedef enum {
+    SSM_OK = 0,
+    SSM_ERR_INVALID_ARG = 1,  /* NULL required pointer, negative size, bad enum, B > 65535 */
+    SSM_ERR_UNSUPPORTED = 2,  /* DS != 16 */
+    SSM_ERR_MISALIGNED = 3,   /* a data pointer is not 16-byte aligned */
+    SSM_ERR_WORKSPACE = 4,    /* workspace NULL or smaller than the query returned */
+    SSM_ERR_CUDA = 5          /* a CUDA runtime call or a launch failed */
+} ssm_status;
+
+typedef struct {
+    int64_t B, T, D, DS;
+    int32_t io;             /* ssm_io_dtype */
+    int32_t ckpt_interval;  /* K >= 0: the forward writes ceil(T/K) checkpoint slots when
+                               K > 0; the backward reads them (see ssm_scan_bwd) */
+    int32_t chunk_len;      /* forward schedule: 0 = chosen by the library; > 0 = chunked
+                               two-pass scan with chunks of this many steps; < 0 = one
+                               pass over T. Every schedule computes the same function. */
+    int32_t reserved;       /* must be 0 */
+} ssm_scan_desc;
+
+/* Bytes of the checkpoint buffer: ceil(T/K)*B*D*DS*4, 0 when K == 0. */
+size_t ssm_scan_ckpt_bytes(const ssm_scan_desc* desc);
+
+/* Bytes of device scratch memory ssm_scan_fwd needs for this desc (0 when the
+ * schedule needs none). The workspace holds the chunked scan's per-chunk
+ * decay sums and partial states. */
+size_t ssm_scan_fwd_workspace_bytes(const ssm_scan_desc* desc);
+
+/* Bytes of device scratch memory ssm_scan_bwd needs for this desc when it is
+ * called with ckpt == NULL (it then rebuilds checkpoints there); the backward
+ * with checkpoints from the forward needs none. */
+size_t ssm_scan_bwd_workspace_bytes(const ssm_scan_desc* desc);
+
+/* Forward scan: y, hT and (if K > 0 and ckpt != NULL) the checkpoints.
+ *   h0    may be NULL (zero initial state)
+ *   hT    may be NULL (not written)
+ *   ckpt  may be NULL (not written); ignored when K == 0
+ *   workspace/workspace_bytes: at least ssm_scan_fwd_workspace_bytes(desc)
+ *         (may be NULL when that is 0)
+ * Chained calls with hT of one call passed as h0 of the next compute the same
+ * function as one call over the concatenated sequence (up to rounding). */
+ssm_status ssm_scan_fwd(const ssm_scan_desc* desc,
+                        const void* x, const void* delta, const float* A,
+                        const void* b, const void* c, const float* h0,
+                        void* y, float* hT, float* ckpt,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/* Backward scan: gx, gdelta, gA, gb, gc, gh0 (all float32) for
+ * L = sum dy*y + sum ghT*hT.
+ *   ckpt  the checkpoints the forward wrote with the same desc (K > 0), or
+ *         NULL: the backward then rebuilds them from h0 in the workspace
+ *   h0    may be NULL (zero initial state); used only when ckpt is NULL
+ *   ghT   may be NULL (hT not differentiated, as on the pssa page)
+ * gA, gb and gc are sums over many (b, d) chains accumulated with atomic adds,
+ * so their last bits can differ from run to run. */
+ssm_status ssm_scan_bwd(const ssm_scan_desc* desc,
+                        const void* x, const void* delta, const float* A,
+                        const void* b, const void* c, const float* h0,
+                        const float* ckpt, const void* dy, const float* ghT,
+                        float* gx, float* gdelta, float* gA, float* gb, float* gc,
+                        float* gh0,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/* Static description of a status code. */
+const char* ssm_status_str(ssm_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSM_SCAN_H */

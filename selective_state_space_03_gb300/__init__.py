@@ -1,0 +1,236 @@
+"""Selective diagonal state-space scan on GB300: Python binding of libssm_scan.so.
+
+The functions here only marshal arguments: they check shapes and dtypes of
+torch CUDA tensors, allocate outputs with torch, and call the C ABI declared
+in ``include/ssm_scan.h`` (``ssm_scan_fwd`` / ``ssm_scan_bwd``) on the current
+torch stream. Every step of the scan runs in the library's CUDA kernels; there
+is no fallback. If the library has not been built, the first call raises.
+
+    y, hT, ckpt = ssm_scan_fwd(x, delta, A, b, c, h0, ckpt_interval=256)
+    grads = ssm_scan_bwd(x, delta, A, b, c, h0, ckpt, dy, ckpt_interval=256)
+    y, hT = selective_scan(x, delta, A, b, c, h0)        # autograd wrapper
+
+Shapes: x, delta (B, T, D); A (D, 16); b, c (B, T, 16); h0 (B, D, 16).
+x, delta, b, c (and dy) are float32 or bfloat16 (all the same); A, h0 and the
+state, hT, checkpoints and gradients are float32.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libssm_scan.so")
+
+SSM_IO_F32, SSM_IO_BF16 = 0, 1
+MAX_BWD_CKPT_INTERVAL = 256   # longest checkpoint interval ssm_scan_bwd reads without a rebuild
+STATUS = {0: "SSM_OK", 1: "SSM_ERR_INVALID_ARG", 2: "SSM_ERR_UNSUPPORTED", 3: "SSM_ERR_MISALIGNED",
+          4: "SSM_ERR_WORKSPACE", 5: "SSM_ERR_CUDA"}
+EXPORTS = ("ssm_scan_ckpt_bytes", "ssm_scan_fwd_workspace_bytes", "ssm_scan_bwd_workspace_bytes",
+           "ssm_scan_fwd", "ssm_scan_bwd", "ssm_status_str")
+
+
+class ssm_scan_desc(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int64), ("T", ctypes.c_int64), ("D", ctypes.c_int64), ("DS", ctypes.c_int64),
+                ("io", ctypes.c_int32), ("ckpt_interval", ctypes.c_int32), ("chunk_len", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
+class SSMError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)} ({lib().ssm_status_str(status).decode()})")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build it with `python -c \"import __graft_entry__ as g; "
+                                   f"g.build()\"` (needs nvcc); there is no CPU fallback")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, sz, dp = ctypes.c_void_p, ctypes.c_size_t, ctypes.POINTER(ssm_scan_desc)
+            for name in ("ssm_scan_ckpt_bytes", "ssm_scan_fwd_workspace_bytes", "ssm_scan_bwd_workspace_bytes"):
+                getattr(L, name).argtypes = [dp]
+                getattr(L, name).restype = sz
+            L.ssm_scan_fwd.argtypes = [dp] + [vp] * 9 + [vp, sz, vp]
+            L.ssm_scan_fwd.restype = ctypes.c_int
+            L.ssm_scan_bwd.argtypes = [dp] + [vp] * 15 + [vp, sz, vp]
+            L.ssm_scan_bwd.restype = ctypes.c_int
+            L.ssm_status_str.argtypes = [ctypes.c_int]
+            L.ssm_status_str.restype = ctypes.c_char_p
+            _lib = L
+    return _lib
+
+
+def make_desc(B, T, D, DS=16, io=SSM_IO_F32, ckpt_interval=0, chunk_len=0) -> ssm_scan_desc:
+    return ssm_scan_desc(int(B), int(T), int(D), int(DS), int(io), int(ckpt_interval), int(chunk_len), 0)
+
+
+# ---------------------------------------------------------------- torch marshalling
+
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _io_of(x):
+    torch = _torch()
+    if x.dtype == torch.float32:
+        return SSM_IO_F32
+    if x.dtype == torch.bfloat16:
+        return SSM_IO_BF16
+    raise TypeError(f"x must be float32 or bfloat16, got {x.dtype}")
+
+
+def _check(t, shape, dtype, name, device):
+    if t is None:
+        return
+    if tuple(t.shape) != tuple(shape) or t.dtype != dtype or not t.is_contiguous() or t.device != device:
+        raise ValueError(f"{name}: expected contiguous {dtype} {tuple(shape)} on {device}, "
+                         f"got {t.dtype} {tuple(t.shape)} on {t.device} (contiguous={t.is_contiguous()})")
+
+
+def _stream(stream):
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _workspace(nbytes, device):
+    torch = _torch()
+    if nbytes == 0:
+        return None, 0
+    return torch.empty(nbytes, dtype=torch.uint8, device=device), nbytes
+
+
+def ssm_scan_fwd(x, delta, A, b, c, h0=None, *, ckpt_interval=0, chunk_len=0, y=None, hT=None, ckpt=None,
+                 workspace=None, stream=None):
+    """Forward scan. Returns (y, hT, ckpt); ckpt is None when ckpt_interval == 0."""
+    torch = _torch()
+    B, T, D = x.shape
+    DS = A.shape[1] if A.dim() == 2 else 16
+    io = _io_of(x)
+    dev = x.device
+    _check(delta, (B, T, D), x.dtype, "delta", dev)
+    _check(A, (D, DS), torch.float32, "A", dev)
+    _check(b, (B, T, DS), x.dtype, "b", dev)
+    _check(c, (B, T, DS), x.dtype, "c", dev)
+    _check(h0, (B, D, DS), torch.float32, "h0", dev)
+    desc = make_desc(B, T, D, DS, io, ckpt_interval, chunk_len)
+    L = lib()
+    if y is None:
+        y = torch.empty((B, T, D), dtype=x.dtype, device=dev)
+    if hT is None:
+        hT = torch.empty((B, D, DS), dtype=torch.float32, device=dev)
+    if ckpt is None and ckpt_interval > 0:
+        nslots = -(-T // ckpt_interval)
+        ckpt = torch.empty((nslots, B, D, DS), dtype=torch.float32, device=dev)
+    _check(y, (B, T, D), x.dtype, "y", dev)
+    _check(hT, (B, D, DS), torch.float32, "hT", dev)
+    need = L.ssm_scan_fwd_workspace_bytes(ctypes.byref(desc))
+    if workspace is None:
+        workspace, wsb = _workspace(need, dev)
+    else:
+        wsb = workspace.numel() * workspace.element_size()
+    st = L.ssm_scan_fwd(ctypes.byref(desc), _ptr(x), _ptr(delta), _ptr(A), _ptr(b), _ptr(c), _ptr(h0),
+                        _ptr(y), _ptr(hT), _ptr(ckpt), _ptr(workspace), wsb, _stream(stream))
+    if st != 0:
+        raise SSMError(st, "ssm_scan_fwd")
+    return y, hT, ckpt
+
+
+def ssm_scan_bwd(x, delta, A, b, c, h0, ckpt, dy, ghT=None, *, ckpt_interval=0, grads=None, workspace=None,
+                 stream=None):
+    """Backward scan. Returns dict(gx, gdelta, gA, gb, gc, gh0), all float32."""
+    torch = _torch()
+    B, T, D = x.shape
+    DS = A.shape[1]
+    io = _io_of(x)
+    dev = x.device
+    _check(dy, (B, T, D), x.dtype, "dy", dev)
+    _check(ghT, (B, D, DS), torch.float32, "ghT", dev)
+    _check(h0, (B, D, DS), torch.float32, "h0", dev)
+    desc = make_desc(B, T, D, DS, io, ckpt_interval, 0)
+    L = lib()
+    f32 = dict(dtype=torch.float32, device=dev)
+    g = grads or {}
+    out = {
+        "gx": g.get("gx", torch.empty((B, T, D), **f32)),
+        "gdelta": g.get("gdelta", torch.empty((B, T, D), **f32)),
+        "gA": g.get("gA", torch.empty((D, DS), **f32)),
+        "gb": g.get("gb", torch.empty((B, T, DS), **f32)),
+        "gc": g.get("gc", torch.empty((B, T, DS), **f32)),
+        "gh0": g.get("gh0", torch.empty((B, D, DS), **f32)),
+    }
+    # the library rebuilds checkpoints in the workspace when none are given or
+    # when they are further apart than the backward reads directly
+    rebuild = ckpt is None or not (0 < ckpt_interval <= MAX_BWD_CKPT_INTERVAL)
+    need = L.ssm_scan_bwd_workspace_bytes(ctypes.byref(desc)) if rebuild else 0
+    if workspace is None:
+        workspace, wsb = _workspace(need, dev)
+    else:
+        wsb = workspace.numel() * workspace.element_size()
+    st = L.ssm_scan_bwd(ctypes.byref(desc), _ptr(x), _ptr(delta), _ptr(A), _ptr(b), _ptr(c), _ptr(h0),
+                        _ptr(ckpt), _ptr(dy), _ptr(ghT), _ptr(out["gx"]), _ptr(out["gdelta"]), _ptr(out["gA"]),
+                        _ptr(out["gb"]), _ptr(out["gc"]), _ptr(out["gh0"]), _ptr(workspace), wsb,
+                        _stream(stream))
+    if st != 0:
+        raise SSMError(st, "ssm_scan_bwd")
+    return out
+
+
+def selective_scan(x, delta, A, b, c, h0=None, ckpt_interval=256):
+    """Differentiable scan: returns (y, hT). Gradients flow to x, delta, A, b, c and h0;
+    hT is differentiated too (its gradient enters the backward as ghT)."""
+    return _ScanFn.apply(x, delta, A, b, c, h0, ckpt_interval)
+
+
+def _make_autograd():
+    torch = _torch()
+
+    class ScanFn(torch.autograd.Function):
+        @staticmethod
+        def forward(ctx, x, delta, A, b, c, h0, K):
+            y, hT, ckpt = ssm_scan_fwd(x, delta, A, b, c, h0, ckpt_interval=K)
+            ctx.save_for_backward(x, delta, A, b, c, h0, ckpt)
+            ctx.K = K
+            ctx.has_h0 = h0 is not None
+            return y, hT
+
+        @staticmethod
+        def backward(ctx, dy, dhT):
+            x, delta, A, b, c, h0, ckpt = ctx.saved_tensors
+            dy = torch.zeros_like(x) if dy is None else dy.to(x.dtype).contiguous()
+            ghT = None if dhT is None else dhT.float().contiguous()
+            g = ssm_scan_bwd(x, delta, A, b, c, h0, ckpt, dy, ghT, ckpt_interval=ctx.K)
+            return (g["gx"].to(x.dtype), g["gdelta"].to(delta.dtype), g["gA"], g["gb"].to(b.dtype),
+                    g["gc"].to(c.dtype), g["gh0"] if ctx.has_h0 else None, None)
+
+    return ScanFn
+
+
+class _Lazy:
+    _fn = None
+
+    def apply(self, *args):
+        if _Lazy._fn is None:
+            _Lazy._fn = _make_autograd()
+        return _Lazy._fn.apply(*args)
+
+
+_ScanFn = _Lazy()
+
+__all__ = ["lib", "ssm_scan_desc", "make_desc", "ssm_scan_fwd", "ssm_scan_bwd", "selective_scan", "SSMError",
+           "EXPORTS", "LIB_PATH", "SSM_IO_F32", "SSM_IO_BF16"]

@@ -1,0 +1,259 @@
+// C ABI of libssm_scan.so: argument checks, schedule choice and launches.
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+
+#include "ssm_internal.h"
+#include "ssm_scan.h"
+
+namespace ssm {
+
+cudaError_t launch_fwd_f32(const FwdLaunch& L, int mode, cudaStream_t stream);
+cudaError_t launch_fwd_bf16(const FwdLaunch& L, int mode, cudaStream_t stream);
+cudaError_t launch_bwd_f32(const BwdLaunch& L, cudaStream_t stream);
+cudaError_t launch_bwd_bf16(const BwdLaunch& L, cudaStream_t stream);
+
+int device_sm_count() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 152;
+    }
+    if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        n = 152;
+    }
+    if (dev >= 0 && dev < 64) cache[dev] = n;
+    return n;
+}
+
+namespace {
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+ssm_status check_desc(const ssm_scan_desc* d) {
+    if (d == nullptr) return SSM_ERR_INVALID_ARG;
+    if (d->B < 0 || d->T < 0 || d->D < 0 || d->DS < 0) return SSM_ERR_INVALID_ARG;
+    if (d->io != SSM_IO_F32 && d->io != SSM_IO_BF16) return SSM_ERR_INVALID_ARG;
+    if (d->ckpt_interval < 0 || d->reserved != 0) return SSM_ERR_INVALID_ARG;
+    if (d->B > 65535) return SSM_ERR_INVALID_ARG;
+    if (d->DS != kDS) return SSM_ERR_UNSUPPORTED;
+    return SSM_OK;
+}
+
+int64_t io_size(const ssm_scan_desc& d) { return d.io == SSM_IO_BF16 ? 2 : 4; }
+
+// 16-byte staging needs rows of x-like tensors to be whole 16-byte chunks.
+bool vec_ok(const ssm_scan_desc& d) { return (d.D * io_size(d)) % 16 == 0; }
+
+struct FwdPlan {
+    int mode;        // kSingle (0) or chunked (2, meaning pass 1 + pass 2)
+    int G;
+    int64_t Lc;
+    int64_t nchunk;
+    size_t ws_S, ws_Sd;   // byte sizes of the two workspace arrays
+};
+
+FwdPlan plan_fwd(const ssm_scan_desc& d) {
+    FwdPlan P{0, 4, d.T, 1, 0, 0};
+    const int64_t chains = d.B * d.D;
+    const int64_t want = int64_t(device_sm_count()) * 512;   // ~16 resident warps per SM
+    bool chunked = false;
+    int64_t Lc = 0;
+    if (d.chunk_len > 0) {
+        chunked = true;
+        Lc = d.chunk_len;
+    } else if (d.chunk_len == 0 && chains * 4 * 2 < want && d.T >= 256) {
+        chunked = true;
+        const int64_t nch = cdiv(want, chains * 4);
+        Lc = cdiv(cdiv(d.T, nch), 32) * 32;
+        if (Lc < 64) Lc = 64;
+    }
+    if (chunked && cdiv(d.T, Lc) < 2) chunked = false;
+    if (chunked) {
+        P.mode = 2;
+        P.G = 4;
+        P.Lc = Lc;
+        P.nchunk = cdiv(d.T, Lc);
+        P.ws_S = align_up(size_t(d.B) * size_t(P.nchunk - 1) * size_t(d.D) * kDS * 4);
+        P.ws_Sd = align_up(size_t(d.B) * size_t(P.nchunk - 1) * size_t(d.D) * 4);
+    } else {
+        P.G = chains >= want ? 1 : (chains * 2 >= want ? 2 : 4);
+        // testing aid: force the lanes per chain of the one-pass schedule
+        if (const char* env = std::getenv("SSM_SCAN_FORCE_LANES")) {
+            const int g = std::atoi(env);
+            if (g == 1 || g == 2 || g == 4) P.G = g;
+        }
+    }
+    return P;
+}
+
+cudaError_t run_fwd(const ssm_scan_desc& d, FwdLaunch L, int mode, cudaStream_t st) {
+    return d.io == SSM_IO_BF16 ? launch_fwd_bf16(L, mode, st) : launch_fwd_f32(L, mode, st);
+}
+
+int64_t bwd_internal_K(const ssm_scan_desc& d) {
+    return (d.ckpt_interval > 0 && d.ckpt_interval <= kMaxBwdK) ? d.ckpt_interval : kMaxBwdK;
+}
+
+}  // namespace
+}  // namespace ssm
+
+using namespace ssm;
+
+extern "C" {
+
+const char* ssm_status_str(ssm_status s) {
+    switch (s) {
+        case SSM_OK: return "ok";
+        case SSM_ERR_INVALID_ARG: return "invalid argument";
+        case SSM_ERR_UNSUPPORTED: return "unsupported shape (DS must be 16)";
+        case SSM_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+        case SSM_ERR_WORKSPACE: return "workspace missing or too small";
+        case SSM_ERR_CUDA: return "CUDA error";
+    }
+    return "unknown status";
+}
+
+size_t ssm_scan_ckpt_bytes(const ssm_scan_desc* d) {
+    if (check_desc(d) != SSM_OK || d->ckpt_interval <= 0) return 0;
+    return size_t(cdiv(d->T, d->ckpt_interval)) * size_t(d->B) * size_t(d->D) * size_t(d->DS) * 4;
+}
+
+size_t ssm_scan_fwd_workspace_bytes(const ssm_scan_desc* d) {
+    if (check_desc(d) != SSM_OK || d->B == 0 || d->T == 0 || d->D == 0) return 0;
+    const FwdPlan P = plan_fwd(*d);
+    return P.mode == 2 ? P.ws_S + P.ws_Sd : 0;
+}
+
+size_t ssm_scan_bwd_workspace_bytes(const ssm_scan_desc* d) {
+    if (check_desc(d) != SSM_OK || d->B == 0 || d->T == 0 || d->D == 0) return 0;
+    return align_up(size_t(cdiv(d->T, bwd_internal_K(*d))) * size_t(d->B) * size_t(d->D) * kDS * 4);
+}
+
+ssm_status ssm_scan_fwd(const ssm_scan_desc* desc, const void* x, const void* delta, const float* A,
+                        const void* b, const void* c, const float* h0, void* y, float* hT, float* ckpt,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+    ssm_status st = check_desc(desc);
+    if (st != SSM_OK) return st;
+    const ssm_scan_desc& d = *desc;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool work = d.B > 0 && d.T > 0 && d.D > 0;
+    if (work && (!x || !delta || !A || !b || !c || !y)) return SSM_ERR_INVALID_ARG;
+    const void* ptrs[] = {x, delta, A, b, c, h0, y, hT, ckpt};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return SSM_ERR_MISALIGNED;
+    if (!work) {
+        // empty sequence (or no chains): hT = h0, nothing else to write
+        if (hT && d.B > 0 && d.D > 0) {
+            const size_t bytes = size_t(d.B) * size_t(d.D) * kDS * 4;
+            const cudaError_t e = h0 ? cudaMemcpyAsync(hT, h0, bytes, cudaMemcpyDeviceToDevice, s)
+                                     : cudaMemsetAsync(hT, 0, bytes, s);
+            if (e != cudaSuccess) return SSM_ERR_CUDA;
+        }
+        return SSM_OK;
+    }
+    const FwdPlan P = plan_fwd(d);
+    if (P.mode == 2 && (workspace == nullptr || workspace_bytes < P.ws_S + P.ws_Sd)) return SSM_ERR_WORKSPACE;
+    if (workspace && !aligned16(workspace)) return SSM_ERR_MISALIGNED;
+
+    FwdLaunch L{};
+    L.x = x; L.delta = delta; L.A = A; L.b = b; L.c = c; L.h0 = h0;
+    L.y = y; L.hT = hT; L.ckpt = d.ckpt_interval > 0 ? ckpt : nullptr;
+    L.B = d.B; L.T = d.T; L.D = d.D; L.K = d.ckpt_interval;
+    L.io = d.io == SSM_IO_BF16 ? IO::BF16 : IO::F32;
+    L.vec = vec_ok(d);
+    L.ckpt_only = false;
+    L.G = P.G;
+    cudaError_t e;
+    if (P.mode == 2) {
+        L.Lc = P.Lc;
+        L.nchunk = P.nchunk;
+        L.ws_S = static_cast<float*>(workspace);
+        L.ws_Sd = reinterpret_cast<float*>(static_cast<char*>(workspace) + P.ws_S);
+        e = run_fwd(d, L, 1, s);
+        if (e == cudaSuccess) e = run_fwd(d, L, 2, s);
+    } else {
+        L.Lc = d.T;
+        L.nchunk = 1;
+        e = run_fwd(d, L, 0, s);
+    }
+    return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+ssm_status ssm_scan_bwd(const ssm_scan_desc* desc, const void* x, const void* delta, const float* A,
+                        const void* b, const void* c, const float* h0, const float* ckpt, const void* dy,
+                        const float* ghT, float* gx, float* gdelta, float* gA, float* gb, float* gc,
+                        float* gh0, void* workspace, size_t workspace_bytes, void* stream) {
+    ssm_status st = check_desc(desc);
+    if (st != SSM_OK) return st;
+    const ssm_scan_desc& d = *desc;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool work = d.B > 0 && d.T > 0 && d.D > 0;
+    if (work && (!x || !delta || !A || !b || !c || !dy || !gx || !gdelta || !gb || !gc)) return SSM_ERR_INVALID_ARG;
+    if (d.D > 0 && !gA) return SSM_ERR_INVALID_ARG;
+    if (d.B > 0 && d.D > 0 && !gh0) return SSM_ERR_INVALID_ARG;
+    const void* ptrs[] = {x, delta, A, b, c, h0, ckpt, dy, ghT, gx, gdelta, gA, gb, gc, gh0};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return SSM_ERR_MISALIGNED;
+    if (!work) {
+        // no steps: gA = 0, gh0 = ghT (zeros without ghT); gb, gc have no rows unless D == 0
+        cudaError_t e = cudaSuccess;
+        if (d.D > 0) e = cudaMemsetAsync(gA, 0, size_t(d.D) * kDS * 4, s);
+        if (e == cudaSuccess && d.B > 0 && d.D > 0) {
+            const size_t bytes = size_t(d.B) * size_t(d.D) * kDS * 4;
+            e = ghT ? cudaMemcpyAsync(gh0, ghT, bytes, cudaMemcpyDeviceToDevice, s) : cudaMemsetAsync(gh0, 0, bytes, s);
+        }
+        if (e == cudaSuccess && d.D == 0 && d.B > 0 && d.T > 0) {
+            // no channels: the sums over d are empty
+            const size_t bytes = size_t(d.B) * size_t(d.T) * kDS * 4;
+            if (gb) e = cudaMemsetAsync(gb, 0, bytes, s);
+            if (e == cudaSuccess && gc) e = cudaMemsetAsync(gc, 0, bytes, s);
+        }
+        return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+    }
+
+    // checkpoints: the forward's, or rebuilt in the workspace
+    const float* ck = ckpt;
+    int64_t K = d.ckpt_interval;
+    const bool rebuild = (ckpt == nullptr) || K <= 0 || K > kMaxBwdK;
+    if (rebuild) {
+        K = bwd_internal_K(d);
+        const size_t need = ssm_scan_bwd_workspace_bytes(desc);
+        if (workspace == nullptr || workspace_bytes < need) return SSM_ERR_WORKSPACE;
+        if (!aligned16(workspace)) return SSM_ERR_MISALIGNED;
+        FwdLaunch L{};
+        L.x = x; L.delta = delta; L.A = A; L.b = b; L.c = c; L.h0 = h0;
+        L.y = nullptr; L.hT = nullptr; L.ckpt = static_cast<float*>(workspace);
+        L.B = d.B; L.T = d.T; L.D = d.D; L.K = K; L.Lc = d.T; L.nchunk = 1;
+        L.io = d.io == SSM_IO_BF16 ? IO::BF16 : IO::F32;
+        L.vec = vec_ok(d);
+        L.G = 4;
+        L.ckpt_only = true;
+        if (run_fwd(d, L, 3, s) != cudaSuccess) return SSM_ERR_CUDA;
+        ck = static_cast<const float*>(workspace);
+    }
+
+    if (cudaMemsetAsync(gA, 0, size_t(d.D) * kDS * 4, s) != cudaSuccess) return SSM_ERR_CUDA;
+    const size_t bts = size_t(d.B) * size_t(d.T) * kDS * 4;
+    if (cudaMemsetAsync(gb, 0, bts, s) != cudaSuccess) return SSM_ERR_CUDA;
+    if (cudaMemsetAsync(gc, 0, bts, s) != cudaSuccess) return SSM_ERR_CUDA;
+
+    BwdLaunch L{};
+    L.x = x; L.delta = delta; L.A = A; L.b = b; L.c = c; L.ckpt = ck; L.dy = dy; L.ghT = ghT;
+    L.gx = gx; L.gdelta = gdelta; L.gA = gA; L.gb = gb; L.gc = gc; L.gh0 = gh0;
+    L.B = d.B; L.T = d.T; L.D = d.D; L.K = K;
+    L.io = d.io == SSM_IO_BF16 ? IO::BF16 : IO::F32;
+    L.vec = vec_ok(d);
+    const cudaError_t e = d.io == SSM_IO_BF16 ? launch_bwd_bf16(L, s) : launch_bwd_f32(L, s);
+    return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,6 @@
+// Backward kernel with float32 I/O.
+#include "ssm_bwd_impl.cuh"
+
+namespace ssm {
+cudaError_t launch_bwd_f32(const BwdLaunch& L, cudaStream_t stream) { return launch_bwd_io<float>(L, stream); }
+}  // namespace ssm

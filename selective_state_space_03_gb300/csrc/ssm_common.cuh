@@ -1,0 +1,124 @@
+// Device helpers shared by the scan kernels (sm_103a).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include "ssm_internal.h"
+
+namespace ssm {
+
+constexpr float kLog2e = 1.4426950408889634f;   // exp(v) = 2^(v * log2(e))
+
+// 2^v on the special-function unit (MUFU), denormal results flushed to zero.
+// Its relative error is a few units in the last place of float32, far inside
+// the scan's tolerance; decays are in (0, 1] so flushing only affects values
+// below 2^-126.
+__device__ __forceinline__ float ex2(float v) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+    return r;
+}
+
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
+    return __float2bfloat16_rn(v);   // round to nearest even
+}
+
+// ---------------------------------------------------------------- cp.async
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// 16-byte global->shared copy; src_bytes == 0 writes zeros and reads nothing.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, int src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n"
+                 :: "r"(smem_u32(dst)), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" :: "n"(N) : "memory"); }
+
+// ---------------------------------------------------------------- tile staging
+//
+// Rows [t0, t0 + TT) x columns [d0, d0 + W) of one batch of a (B, T, W_total)
+// tensor into dst[TT][W] (same element type). Rows at or past t_end and
+// columns at or past ncols are zero-filled. VEC uses 16-byte cp.async and
+// needs ncols * sizeof(E) % 16 == 0 and a 16-byte aligned base; otherwise the
+// copy is element by element with plain loads.
+template <typename E, int TT, int W, int NT, bool VEC>
+__device__ __forceinline__ void stage_tile(E* dst, const E* src_b, int64_t ncols, int64_t t0,
+                                           int64_t t_end, int64_t d0) {
+    if constexpr (VEC) {
+        constexpr int EPC = 16 / sizeof(E);
+        static_assert(W % EPC == 0, "tile width must be a whole number of 16-byte chunks");
+        constexpr int CPR = W / EPC;
+        constexpr int NCH = TT * CPR;
+        for (int i = threadIdx.x; i < NCH; i += NT) {
+            const int r = i / CPR, cc = i % CPR;
+            const int64_t t = t0 + r, col = d0 + int64_t(cc) * EPC;
+            const bool ok = (t < t_end) && (col < ncols);
+            const E* g = ok ? src_b + t * ncols + col : src_b;
+            cp_async16(dst + r * W + cc * EPC, g, ok ? 16 : 0);
+        }
+    } else {
+        for (int i = threadIdx.x; i < TT * W; i += NT) {
+            const int r = i / W, cc = i % W;
+            const int64_t t = t0 + r, col = d0 + cc;
+            dst[i] = (t < t_end && col < ncols) ? src_b[t * ncols + col] : E(0.0f);
+        }
+    }
+}
+
+// Widen a bf16 tile in shared memory to float32 (n elements, n % 8 == 0).
+template <int NT>
+__device__ __forceinline__ void widen_bf16(float* dst, const __nv_bfloat16* src, int n) {
+    for (int i = threadIdx.x * 8; i < n; i += NT * 8) {
+        const uint4 raw = *reinterpret_cast<const uint4*>(src + i);
+        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+        float4 lo, hi;
+        lo.x = __uint_as_float(w[0] << 16); lo.y = __uint_as_float(w[0] & 0xffff0000u);
+        lo.z = __uint_as_float(w[1] << 16); lo.w = __uint_as_float(w[1] & 0xffff0000u);
+        hi.x = __uint_as_float(w[2] << 16); hi.y = __uint_as_float(w[2] & 0xffff0000u);
+        hi.z = __uint_as_float(w[3] << 16); hi.w = __uint_as_float(w[3] & 0xffff0000u);
+        *reinterpret_cast<float4*>(dst + i) = lo;
+        *reinterpret_cast<float4*>(dst + i + 4) = hi;
+    }
+}
+
+// ---------------------------------------------------------------- lane reductions
+//
+// A chain's DS states are split over G neighbouring lanes. Each lane holds its
+// partial sums for G consecutive steps (v[0..G-1]). After the call, lane gl of
+// the group returns the full sum for step gl: a reduce-scatter that needs G-1
+// shuffles per lane for G steps instead of log2(G) per step.
+template <int G>
+__device__ __forceinline__ float reduce_scatter_steps(const float (&v)[G], int gl) {
+    if constexpr (G == 1) {
+        return v[0];
+    } else if constexpr (G == 2) {
+        const bool hi = gl & 1;
+        const float send = hi ? v[0] : v[1];
+        const float keep = hi ? v[1] : v[0];
+        return keep + __shfl_xor_sync(0xffffffffu, send, 1);
+    } else {
+        static_assert(G == 4, "G must be 1, 2 or 4");
+        const bool hi2 = gl & 2;
+        const float s0 = hi2 ? v[0] : v[2], s1 = hi2 ? v[1] : v[3];
+        const float k0 = hi2 ? v[2] : v[0], k1 = hi2 ? v[3] : v[1];
+        const float q0 = k0 + __shfl_xor_sync(0xffffffffu, s0, 2);
+        const float q1 = k1 + __shfl_xor_sync(0xffffffffu, s1, 2);
+        const bool hi1 = gl & 1;
+        const float send = hi1 ? q0 : q1;
+        const float keep = hi1 ? q1 : q0;
+        return keep + __shfl_xor_sync(0xffffffffu, send, 1);
+    }
+}
+
+}  // namespace ssm

@@ -1,0 +1,71 @@
+// Host-side interface between the C ABI (ssm_api.cu) and the kernel launchers.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace ssm {
+
+constexpr int kDS = 16;   // state size the kernels are built for
+
+enum class IO { F32 = 0, BF16 = 1 };
+
+// Forward launch description. `mode` selects the schedule:
+//   0: one pass over T per (b, d) chain;
+//   1: chunked pass 1, per chunk the local end state (zero start) and the
+//      delta sum, written to the workspace (all chunks but the last);
+//   2: chunked pass 2, per chunk the start state from the carries of all
+//      earlier chunks, then the scan of the chunk with readout.
+struct FwdLaunch {
+    const void* x;
+    const void* delta;
+    const float* A;
+    const void* b;
+    const void* c;
+    const float* h0;
+    void* y;        // may be null only in mode 1, or when ckpt_only
+    float* hT;      // may be null
+    float* ckpt;    // may be null
+    float* ws_S;    // [B][nchunk-1][D][16]   (chunked modes)
+    float* ws_Sd;   // [B][nchunk-1][D]       (chunked modes)
+    int64_t B, T, D;
+    int64_t K;      // checkpoint interval, 0 = none
+    int64_t Lc;     // chunk length (chunked modes; T in mode 0)
+    int64_t nchunk; // number of chunks (1 in mode 0)
+    IO io;
+    int G;          // lanes per chain: 1, 2 or 4
+    bool vec;       // 16-byte staging allowed
+    bool ckpt_only; // mode 0 without readout (checkpoint rebuild for the backward)
+};
+
+cudaError_t launch_fwd(const FwdLaunch& L, int mode, cudaStream_t stream);
+
+struct BwdLaunch {
+    const void* x;
+    const void* delta;
+    const float* A;
+    const void* b;
+    const void* c;
+    const float* ckpt;   // (ceil(T/K), B, D, 16), slot 0 = h0
+    const void* dy;
+    const float* ghT;    // may be null
+    float* gx;
+    float* gdelta;
+    float* gA;           // zeroed by the launcher
+    float* gb;           // zeroed by the launcher
+    float* gc;           // zeroed by the launcher
+    float* gh0;
+    int64_t B, T, D;
+    int64_t K;           // checkpoint interval of ckpt, 1 <= K <= kMaxBwdK
+    IO io;
+    bool vec;
+};
+
+constexpr int64_t kMaxBwdK = 256;   // largest checkpoint interval the backward reads directly
+
+cudaError_t launch_bwd(const BwdLaunch& L, cudaStream_t stream);
+
+int device_sm_count();
+
+}  // namespace ssm

@@ -1,0 +1,130 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function the
+header declares, and rejects bad arguments on the host before any launch.
+
+The pointers passed here are fake (never dereferenced): every call below fails
+validation, which happens before anything is enqueued.
+"""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from selective_state_space_03_gb300 import build
+    build.build()
+    import selective_state_space_03_gb300 as ssm
+    return ssm.lib()
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"\b(ssm_\w+)\s*\(", text):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_header_declares_the_api():
+    names = declared_functions()
+    for n in ("ssm_scan_fwd", "ssm_scan_bwd", "ssm_scan_ckpt_bytes", "ssm_scan_fwd_workspace_bytes",
+              "ssm_scan_bwd_workspace_bytes", "ssm_status_str"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), f"{name} declared in include/ but not exported"
+
+
+def desc(**kw):
+    import selective_state_space_03_gb300 as ssm
+    base = dict(B=2, T=64, D=32, DS=16, io=0, ckpt_interval=0, chunk_len=0)
+    base.update(kw)
+    return ssm.make_desc(**base)
+
+
+FAKE = 0x7f0000000000      # 16-byte aligned, never dereferenced
+
+
+def fwd(L, d, x=FAKE, delta=FAKE, A=FAKE, b=FAKE, c=FAKE, h0=None, y=FAKE, hT=None, ckpt=None, ws=None,
+        wsb=0):
+    P = ctypes.c_void_p
+    return L.ssm_scan_fwd(ctypes.byref(d) if d is not None else None, P(x), P(delta), P(A), P(b), P(c), P(h0),
+                          P(y), P(hT), P(ckpt), P(ws), wsb, None)
+
+
+def bwd(L, d, ckpt=FAKE, ws=None, wsb=0, **kw):
+    P = ctypes.c_void_p
+    a = dict(x=FAKE, delta=FAKE, A=FAKE, b=FAKE, c=FAKE, h0=None, dy=FAKE, ghT=None, gx=FAKE, gdelta=FAKE,
+             gA=FAKE, gb=FAKE, gc=FAKE, gh0=FAKE)
+    a.update(kw)
+    return L.ssm_scan_bwd(ctypes.byref(d), P(a["x"]), P(a["delta"]), P(a["A"]), P(a["b"]), P(a["c"]), P(a["h0"]),
+                          P(ckpt), P(a["dy"]), P(a["ghT"]), P(a["gx"]), P(a["gdelta"]), P(a["gA"]), P(a["gb"]),
+                          P(a["gc"]), P(a["gh0"]), P(ws), wsb, None)
+
+
+def test_status_strings(L):
+    for s in range(6):
+        assert L.ssm_status_str(s)
+    assert b"DS" in L.ssm_status_str(2)
+
+
+def test_invalid_descriptors(L):
+    assert fwd(L, None) == 1
+    assert fwd(L, desc(B=-1)) == 1
+    assert fwd(L, desc(T=-5)) == 1
+    assert fwd(L, desc(io=7)) == 1
+    assert fwd(L, desc(ckpt_interval=-1)) == 1
+    assert fwd(L, desc(B=70000)) == 1
+    d = desc()
+    d.reserved = 3
+    assert fwd(L, d) == 1
+    assert fwd(L, desc(DS=8)) == 2
+    assert fwd(L, desc(DS=32)) == 2
+    assert bwd(L, desc(DS=8)) == 2
+
+
+def test_null_and_misaligned_pointers(L):
+    assert fwd(L, desc(), x=None) == 1
+    assert fwd(L, desc(), y=None) == 1
+    assert fwd(L, desc(), A=None) == 1
+    assert fwd(L, desc(), delta=FAKE + 4) == 3
+    assert fwd(L, desc(), hT=FAKE + 8) == 3
+    assert bwd(L, desc(), gx=None) == 1
+    assert bwd(L, desc(), gA=None) == 1
+    assert bwd(L, desc(), gb=FAKE + 2) == 3
+
+
+def test_workspace_checks(L):
+    d = desc(T=1024, chunk_len=64)                       # forced chunked schedule needs scratch
+    need = L.ssm_scan_fwd_workspace_bytes(ctypes.byref(d))
+    nch = 1024 // 64
+    assert need >= 2 * (nch - 1) * 32 * 16 * 4
+    assert fwd(L, d) == 4
+    assert fwd(L, d, ws=FAKE, wsb=need - 1) == 4
+    assert L.ssm_scan_fwd_workspace_bytes(ctypes.byref(desc(chunk_len=-1))) == 0
+    # backward without checkpoints rebuilds them in the workspace
+    db = desc(T=1000, ckpt_interval=100)
+    needb = L.ssm_scan_bwd_workspace_bytes(ctypes.byref(db))
+    assert needb >= 10 * 2 * 32 * 16 * 4
+    assert bwd(L, db, ckpt=None) == 4
+    # checkpoints further apart than the backward reads directly are rebuilt too
+    dk = desc(T=2048, ckpt_interval=1024)
+    assert bwd(L, dk, ckpt=FAKE) == 4
+
+
+def test_size_queries(L):
+    d = desc(B=3, T=1000, D=40, ckpt_interval=256)
+    assert L.ssm_scan_ckpt_bytes(ctypes.byref(d)) == 4 * 3 * 40 * 16 * 4
+    assert L.ssm_scan_ckpt_bytes(ctypes.byref(desc(ckpt_interval=0))) == 0
+    assert L.ssm_scan_fwd_workspace_bytes(ctypes.byref(desc(T=0))) == 0
+    assert L.ssm_scan_bwd_workspace_bytes(ctypes.byref(desc(B=0))) == 0
+    assert L.ssm_scan_ckpt_bytes(None) == 0

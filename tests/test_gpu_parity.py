@@ -1,0 +1,299 @@
+"""GPU parity: the CUDA path through the C ABI against the float64 oracle.
+
+Small and medium cases compare every output element; the full benchmark
+workloads compare sampled (b, d) chains (y, hT, gx, gdelta, gh0), sampled
+channels over all batches (gA), one whole batch over all channels (gb, gc),
+and check the Euler identities of the loss on the full outputs.
+Tolerances: float32 I/O 1e-4 (y, hT) and 1e-3 (gradients); bf16 I/O 1e-2;
+all as max |got - ref| / (1 + |ref|).
+"""
+import os
+
+import numpy as np
+import pytest
+
+import gen
+import oracle
+from gpu_util import GRADS, assert_close, dev_inputs, sample_indices, sub_inputs, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _setup():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from selective_state_space_03_gb300 import build
+    build.build()
+    torch.cuda.set_device(0)
+
+
+def ssm():
+    import selective_state_space_03_gb300 as m
+    return m
+
+
+def run_case(w, K, chunk_len=0, seed=0, ghT=False, bwd=True, lanes=None, ckpt_to_bwd=True):
+    import torch
+    inp = gen.make_inputs(w, seed=seed, with_grad_inputs=bwd, with_ghT=ghT)
+    t = dev_inputs(inp)
+    env_old = os.environ.get("SSM_SCAN_FORCE_LANES")
+    if lanes is not None:
+        os.environ["SSM_SCAN_FORCE_LANES"] = str(lanes)
+    try:
+        y, hT, ckpt = ssm().ssm_scan_fwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], ckpt_interval=K,
+                                         chunk_len=chunk_len)
+    finally:
+        if lanes is not None:
+            if env_old is None:
+                del os.environ["SSM_SCAN_FORCE_LANES"]
+            else:
+                os.environ["SSM_SCAN_FORCE_LANES"] = env_old
+    torch.cuda.synchronize()
+    ref = oracle.fwd(inp["x"], inp["delta"], inp["A"], inp["b"], inp["c"], inp["h0"], ckpt_interval=K)
+    assert_close(to_host(y), ref["y"], w.io, "fwd", "y")
+    assert_close(to_host(hT), ref["hT"], w.io, "fwd", "hT")
+    if K > 0:
+        assert_close(to_host(ckpt), ref["ckpt"], w.io, "fwd", "ckpt")
+    if not bwd:
+        return
+    g = ssm().ssm_scan_bwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], ckpt if ckpt_to_bwd else None,
+                           t["dy"], t["ghT"], ckpt_interval=K)
+    torch.cuda.synchronize()
+    gref = oracle.bwd(inp["x"], inp["delta"], inp["A"], inp["b"], inp["c"], inp["h0"], inp["dy"], inp.get("ghT"))
+    for k in GRADS:
+        assert_close(to_host(g[k]), gref[k], w.io, "grad", k)
+
+
+# ---------------------------------------------------------------- whole-output cases
+
+def test_workload1_fwd_bwd():
+    run_case(gen.workload(1), K=16, ghT=True)
+
+
+def test_workload1_chunked_schedule():
+    run_case(gen.workload(1), K=16, chunk_len=16, bwd=False)
+
+
+def test_workload2_full_fwd_bwd():
+    run_case(gen.workload(2), K=256)
+
+
+def test_workload2_one_pass_schedule():
+    run_case(gen.workload(2), K=256, chunk_len=-1, bwd=False)
+
+
+def test_workload3_shape_reduced_bf16():
+    run_case(gen.workload(3, B=2, T=300, D=200), K=64)
+
+
+def test_workload5_shape_reduced_bf16():
+    run_case(gen.workload(5, B=2, T=600, D=264), K=256, ghT=True)
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("lanes", [1, 2, 4])
+def test_lanes_per_chain_variants(io, lanes):
+    run_case(gen.workload(1, B=3, T=100, D=72, io=io), K=32, chunk_len=-1, lanes=lanes, bwd=False)
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_unaligned_channel_count(io):
+    # D * sizeof(io) not a multiple of 16 bytes: element-wise staging path
+    D = 37 if io == "f32" else 20
+    run_case(gen.workload(2, B=2, T=77, D=D, io=io, h0_std=0.1), K=24, ghT=True)
+    run_case(gen.workload(2, B=2, T=77, D=D, io=io, h0_std=0.1), K=24, chunk_len=20, bwd=False)
+
+
+@pytest.mark.parametrize("T,K", [(1, 1), (33, 16), (20, 64), (230, 50), (257, 256)])
+def test_ragged_lengths_and_intervals(T, K):
+    run_case(gen.workload(2, B=2, T=T, D=40, h0_std=0.1), K=K, ghT=True)
+
+
+@pytest.mark.parametrize("chunk_len", [32, 50, 129])
+def test_chunked_ragged_chunks(chunk_len):
+    run_case(gen.workload(2, B=2, T=230, D=48, h0_std=0.1), K=64, chunk_len=chunk_len, bwd=False)
+
+
+def test_backward_rebuilds_checkpoints():
+    # no checkpoints passed: the backward rebuilds them in its workspace
+    run_case(gen.workload(2, B=2, T=300, D=40, h0_std=0.1), K=64, ghT=True, ckpt_to_bwd=False)
+    # interval longer than the backward reads directly
+    run_case(gen.workload(2, B=2, T=700, D=40, h0_std=0.1), K=512, ghT=True)
+
+
+def test_chained_calls_match_one_long_scan():
+    import torch
+    w = gen.workload(4, T=4 * 200, D=96)
+    inp = gen.make_inputs(w)
+    t = dev_inputs(inp)
+    h = t["h0"]
+    ys = []
+    for k in range(4):
+        sl = slice(200 * k, 200 * (k + 1))
+        y, h, _ = ssm().ssm_scan_fwd(t["x"][:, sl].contiguous(), t["delta"][:, sl].contiguous(), t["A"],
+                                     t["b"][:, sl].contiguous(), t["c"][:, sl].contiguous(), h)
+        ys.append(y)
+    torch.cuda.synchronize()
+    ref = oracle.fwd(inp["x"], inp["delta"], inp["A"], inp["b"], inp["c"], inp["h0"])
+    assert_close(to_host(torch.cat(ys, 1)), ref["y"], "f32", "fwd", "y")
+    assert_close(to_host(h), ref["hT"], "f32", "fwd", "hT")
+
+
+def test_empty_sizes():
+    import torch
+    m = ssm()
+    dev = "cuda:0"
+    for B, T, D in ((2, 0, 8), (0, 5, 8), (2, 5, 0)):
+        x = torch.zeros(B, T, D, device=dev)
+        A = -torch.ones(D, 16, device=dev)
+        bc = torch.zeros(B, T, 16, device=dev)
+        h0 = torch.randn(B, D, 16, device=dev)
+        y, hT, _ = m.ssm_scan_fwd(x, x, A, bc, bc, h0)
+        ghT = torch.randn(B, D, 16, device=dev)
+        g = m.ssm_scan_bwd(x, x, A, bc, bc, h0, None, x, ghT)
+        torch.cuda.synchronize()
+        assert torch.equal(hT, h0)
+        assert torch.equal(g["gh0"], ghT)
+        assert torch.all(g["gA"] == 0)
+        assert torch.all(g["gb"] == 0) and torch.all(g["gc"] == 0)
+
+
+def test_outputs_stay_in_bounds_and_forward_is_deterministic():
+    import torch
+    m = ssm()
+    w = gen.workload(2, B=2, T=70, D=36, h0_std=0.1)
+    inp = gen.make_inputs(w, with_grad_inputs=True, with_ghT=True)
+    t = dev_inputs(inp)
+    B, T, D = 2, 70, 36
+    pad = 64
+    canary = 12345.0
+
+    def guarded(n):
+        buf = torch.full((n + 2 * pad,), canary, device="cuda:0")
+        return buf, buf[pad:pad + n]
+
+    yb, y = guarded(B * T * D)
+    hb, hT = guarded(B * D * 16)
+    cb, ck = guarded(3 * B * D * 16)
+    m.ssm_scan_fwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], ckpt_interval=32,
+                   y=y.view(B, T, D), hT=hT.view(B, D, 16), ckpt=ck.view(3, B, D, 16))
+    grads = {}
+    bufs = []
+    for k, n in (("gx", B * T * D), ("gdelta", B * T * D), ("gA", D * 16), ("gb", B * T * 16),
+                 ("gc", B * T * 16), ("gh0", B * D * 16)):
+        full, inner = guarded(n)
+        bufs.append(full)
+        grads[k] = inner
+    shapes = {"gx": (B, T, D), "gdelta": (B, T, D), "gA": (D, 16), "gb": (B, T, 16), "gc": (B, T, 16),
+              "gh0": (B, D, 16)}
+    m.ssm_scan_bwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], ck.view(3, B, D, 16), t["dy"], t["ghT"],
+                   ckpt_interval=32, grads={k: v.view(shapes[k]) for k, v in grads.items()})
+    torch.cuda.synchronize()
+    for full in [yb, hb, cb] + bufs:
+        assert torch.all(full[:pad] == canary) and torch.all(full[-pad:] == canary)
+    y2, _, _ = m.ssm_scan_fwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], ckpt_interval=32)
+    torch.cuda.synchronize()
+    assert torch.equal(y2, y.view(B, T, D))
+
+
+def test_autograd_wrapper():
+    import torch
+    w = gen.workload(2, B=2, T=64, D=16, h0_std=0.1)
+    inp = gen.make_inputs(w, with_grad_inputs=True, with_ghT=True)
+    t = dev_inputs(inp)
+    leaves = {k: t[k].clone().requires_grad_(True) for k in ("x", "delta", "A", "b", "c", "h0")}
+    y, hT = ssm().selective_scan(leaves["x"], leaves["delta"], leaves["A"], leaves["b"], leaves["c"],
+                                 leaves["h0"], ckpt_interval=16)
+    ((y * t["dy"]).sum() + (hT * t["ghT"]).sum()).backward()
+    gref = oracle.bwd(inp["x"], inp["delta"], inp["A"], inp["b"], inp["c"], inp["h0"], inp["dy"], inp["ghT"])
+    for k, gk in zip(("x", "delta", "A", "b", "c", "h0"), GRADS):
+        assert_close(to_host(leaves[k].grad), gref[gk], "f32", "grad", gk)
+
+
+# ---------------------------------------------------------------- full benchmark workloads, sampled
+
+def test_workload3_full_size_sampled():
+    import torch
+    w = gen.workload(3)
+    inp = gen.make_inputs(w)
+    t = dev_inputs(inp)
+    y, hT, _ = ssm().ssm_scan_fwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"])
+    torch.cuda.synchronize()
+    bsel = sample_indices(w.B, 2, 1)
+    dsel = sample_indices(w.D, 24, 2)
+    sub = sub_inputs(inp, bsel, dsel)
+    ref = oracle.fwd(sub["x"], sub["delta"], sub["A"], sub["b"], sub["c"], sub["h0"])
+    ys = to_host(y[torch.as_tensor(bsel)][:, :, torch.as_tensor(dsel)])
+    assert_close(ys, ref["y"], "bf16", "fwd", "y")
+    assert_close(to_host(hT[torch.as_tensor(bsel)][:, torch.as_tensor(dsel)]), ref["hT"], "bf16", "fwd", "hT")
+
+
+def test_workload4_full_size_chained_sampled():
+    import torch
+    w = gen.workload(4)
+    inp = gen.make_inputs(w)
+    t = dev_inputs(inp)
+    L = w.chunk_T
+    h = t["h0"]
+    y = torch.empty_like(t["x"])
+    for k in range(w.T // L):
+        sl = slice(L * k, L * (k + 1))
+        yk, h, _ = ssm().ssm_scan_fwd(t["x"][:, sl].contiguous(), t["delta"][:, sl].contiguous(), t["A"],
+                                      t["b"][:, sl].contiguous(), t["c"][:, sl].contiguous(), h)
+        y[:, sl] = yk
+    torch.cuda.synchronize()
+    dsel = sample_indices(w.D, 12, 3)
+    sub = sub_inputs(inp, np.array([0]), dsel)
+    ref = oracle.fwd(sub["x"], sub["delta"], sub["A"], sub["b"], sub["c"], sub["h0"])
+    assert_close(to_host(y[:, :, torch.as_tensor(dsel)]), ref["y"], "f32", "fwd", "y")
+    assert_close(to_host(h[:, torch.as_tensor(dsel)]), ref["hT"], "f32", "fwd", "hT")
+
+
+def test_workload5_full_size_sampled_and_identities():
+    import torch
+    w = gen.workload(5)
+    inp = gen.make_inputs(w)
+    t = dev_inputs(inp)
+    K = w.ckpt_interval
+    y, hT, ckpt = ssm().ssm_scan_fwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], ckpt_interval=K)
+    g = ssm().ssm_scan_bwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], ckpt, t["dy"], None,
+                           ckpt_interval=K)
+    torch.cuda.synchronize()
+    # chains: y, hT, gx, gdelta, gh0
+    bsel = sample_indices(w.B, 3, 4)
+    dsel = sample_indices(w.D, 10, 5)
+    sub = sub_inputs(inp, bsel, dsel)
+    ref = oracle.fwd(sub["x"], sub["delta"], sub["A"], sub["b"], sub["c"], sub["h0"])
+    gref = oracle.bwd(sub["x"], sub["delta"], sub["A"], sub["b"], sub["c"], sub["h0"], sub["dy"])
+    bi, di = torch.as_tensor(bsel), torch.as_tensor(dsel)
+    assert_close(to_host(y[bi][:, :, di]), ref["y"], "bf16", "fwd", "y")
+    assert_close(to_host(hT[bi][:, di]), ref["hT"], "bf16", "fwd", "hT")
+    for k in ("gx", "gdelta"):
+        assert_close(to_host(g[k][bi][:, :, di]), gref[k], "bf16", "grad", k)
+    assert_close(to_host(g["gh0"][bi][:, di]), gref["gh0"], "bf16", "grad", "gh0")
+    # gA: all batches, sampled channels
+    sub = sub_inputs(inp, np.arange(w.B), dsel[:4])
+    gref = oracle.bwd(sub["x"], sub["delta"], sub["A"], sub["b"], sub["c"], sub["h0"], sub["dy"])
+    assert_close(to_host(g["gA"][torch.as_tensor(dsel[:4])]), gref["gA"], "bf16", "grad", "gA")
+    # gb, gc: one batch, all channels
+    sub = sub_inputs(inp, np.array([bsel[1]]), np.arange(w.D))
+    gref = oracle.bwd(sub["x"], sub["delta"], sub["A"], sub["b"], sub["c"], sub["h0"], sub["dy"])
+    for k in ("gb", "gc"):
+        assert_close(to_host(g[k][int(bsel[1])][None]), gref[k], "bf16", "grad", k)
+    # Euler identities on the full GPU outputs (float64 sums on the host):
+    # I1 sum_s c gc = sum_d dy y per (b, t); I4 sum delta gdelta = sum_s A gA + sum x gx per d
+    c64, dy64 = oracle.to_f64(inp["c"]), oracle.to_f64(inp["dy"])
+    y64 = to_host(y)
+    i1l = np.einsum("bts,bts->bt", c64, to_host(g["gc"]))
+    i1r = np.einsum("btd,btd->bt", dy64, y64)
+    scale = np.einsum("btd,btd->bt", np.abs(dy64), np.abs(y64)) + 1.0
+    assert np.max(np.abs(i1l - i1r) / scale) < 1e-2
+    del y64
+    x64, d64 = oracle.to_f64(inp["x"]), oracle.to_f64(inp["delta"])
+    gx, gd = to_host(g["gx"]), to_host(g["gdelta"])
+    i4l = np.einsum("btd,btd->d", d64, gd)
+    i4r = np.einsum("ds,ds->d", inp["A"].astype(np.float64), to_host(g["gA"])) + np.einsum("btd,btd->d", x64, gx)
+    scale4 = np.einsum("btd,btd->d", np.abs(d64), np.abs(gd)) + 1.0
+    assert np.max(np.abs(i4l - i4r) / scale4) < 1e-3
