@@ -130,25 +130,26 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- CPU oracle timing
 
-def oracle_sample(w, budget_s=12.0, seed=0):
-    """Time the float64 oracle (forward + backward) on the first batch and a
-    slice of channels of workload w, growing the slice until it takes about
-    budget_s seconds. Returns (elements/s, cores, description)."""
+def oracle_sample(w, budget_s=12.0, seed=0, max_batches=8):
+    """Time the float64 oracle (forward with checkpoints + backward) on the first
+    B' batches of workload w (all channels), B' grown until one run takes about
+    budget_s seconds (at most max_batches). Returns (elements/s, cores, sample)."""
     import oracle
-    inp = gen.make_inputs(gen.workload(WORKLOAD, B=1, D=min(w.D, 1024)), seed=seed)
-    ncols = 16
+    B1 = 1
     while True:
-        sl = slice(0, ncols)
-        args = [inp["x"][:, :, sl], inp["delta"][:, :, sl], inp["A"][sl], inp["b"], inp["c"], None]
+        inp = gen.make_inputs(gen.workload(WORKLOAD, B=B1), seed=seed)
+        args = [inp["x"], inp["delta"], inp["A"], inp["b"], inp["c"], inp["h0"]]
         t0 = time.perf_counter()
         oracle.fwd(*args, ckpt_interval=w.ckpt_interval)
-        oracle.bwd(*args, inp["dy"][:, :, sl])
+        oracle.bwd(*args, inp["dy"])
         dt = time.perf_counter() - t0
-        if dt >= budget_s / 4 or ncols >= inp["x"].shape[2]:
+        if dt >= budget_s / 2 or B1 >= max_batches:
             break
-        ncols = min(inp["x"].shape[2], ncols * max(2, int(budget_s / 4 / max(dt, 1e-3))))
-    el = 1 * w.T * ncols * w.DS
-    return el / dt, oracle.threads(), f"B=1 T={w.T} D={ncols} DS={w.DS} (fwd+bwd, {dt:.1f} s)"
+        B1 = min(max_batches, max(2 * B1, int(B1 * budget_s / max(dt, 1e-3))))
+        del inp, args
+    el = B1 * w.T * w.D * w.DS
+    return el / dt, oracle.threads(), f"B={B1} T={w.T} D={w.D} DS={w.DS} (first {B1} of {w.B} batches, " \
+                                      f"fwd+bwd, {dt:.1f} s)"
 
 
 # ---------------------------------------------------------------- our implementation
@@ -370,30 +371,34 @@ def other_workloads(torch, ssm, dev):
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    w = gen.workload(WORKLOAD)
     import oracle
     oracle.build()
-    v0, cores, sample = oracle_sample(w, budget_s=max(2.0, 40.0 / max(1, args.steps + args.warmup)))
-    # each step re-times the same bounded sample
-    inp = gen.make_inputs(gen.workload(WORKLOAD, B=1, D=min(w.D, 1024)), seed=0)
-    ncols = int(sample.split("D=")[1].split()[0])
-    sl = slice(0, ncols)
-    a = [inp["x"][:, :, sl], inp["delta"][:, :, sl], inp["A"][sl], inp["b"], inp["c"], None]
+    w = gen.workload(WORKLOAD)
+    # size the per-step sample so that warm-up + timed steps take a few minutes at most
+    budget = max(2.0, 120.0 / max(1, args.steps + args.warmup))
+    _, cores, sample = oracle_sample(w, budget_s=budget)
+    B1 = int(sample.split("B=")[1].split()[0])
+    inp = gen.make_inputs(gen.workload(WORKLOAD, B=B1), seed=0)
+    a = [inp["x"], inp["delta"], inp["A"], inp["b"], inp["c"], inp["h0"]]
+
+    def step():
+        oracle.fwd(*a, ckpt_interval=w.ckpt_interval)
+        oracle.bwd(*a, inp["dy"])
+
     for _ in range(args.warmup):
-        pass  # the sizing run above already warmed the oracle
+        step()
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.fwd(*a, ckpt_interval=w.ckpt_interval)
-        oracle.bwd(*a, inp["dy"][:, :, sl])
+        step()
     dt = (time.perf_counter() - t0) / args.steps
-    el = w.T * ncols * w.DS
+    el = B1 * w.T * w.D * w.DS
     v = el / dt
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded Philox normals, gen.make_inputs)",
-            "config": {"workload": w.name, "sample": f"B=1 T={w.T} D={ncols} DS={w.DS}"},
+            "config": {"workload": w.name, "sample": f"B={B1} T={w.T} D={w.D} DS={w.DS} per step (fwd+bwd)"},
             "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": f"B=1 T={w.T} D={ncols} DS={w.DS} per step (fwd+bwd)"},
+                             "sample": f"B={B1} T={w.T} D={w.D} DS={w.DS} per step (fwd+bwd)"},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
