@@ -122,6 +122,33 @@ ssm_status ssm_scan_bwd(const ssm_scan_desc* desc,
                         float* gh0,
                         void* workspace, size_t workspace_bytes, void* stream);
 
+/* Forward scan that allocates nothing and takes no workspace. The pages have
+ * no counterpart of this call; it exists for callers that cannot allocate
+ * device memory while they run: code hosted inside another runtime that owns
+ * all device memory (an engine plugin, a replayed graph step), or services that
+ * must not call cudaMalloc on the hot path because it synchronises the device
+ * and can fail under memory pressure.
+ *
+ * It always uses the chunked two-pass schedule (chunk length desc->chunk_len
+ * when > 0, else chosen by the library; one chunk falls back to the one-pass
+ * scan, which needs no scratch) and keeps the chunk carries in a fixed device
+ * array inside the library of SSM_SCAN_NOALLOC_SCRATCH_BYTES bytes, which
+ * every GPU that loads the library holds until the process exits. Carries take
+ * B*(nchunk-1)*D*68 bytes (each part rounded up to 256); larger problems are
+ * rejected with SSM_ERR_WORKSPACE before anything is enqueued.
+ *
+ * The first call on each device looks up the array's device address with that
+ * device current (later calls reuse it), so make the first call before any
+ * stream capture. All calls on a device share the array: calls that overlap on
+ * the GPU race on it, so the caller must order them (one stream, or events).
+ * Nothing in the array needs clearing: each call writes every entry it reads.
+ * Arguments, layouts, results and other errors are those of ssm_scan_fwd. */
+#define SSM_SCAN_NOALLOC_SCRATCH_BYTES (8u << 20)
+ssm_status ssm_scan_fwd_noalloc(const ssm_scan_desc* desc,
+                                const void* x, const void* delta, const float* A,
+                                const void* b, const void* c, const float* h0,
+                                void* y, float* hT, float* ckpt, void* stream);
+
 /* Static description of a status code. */
 const char* ssm_status_str(ssm_status status);
 

@@ -191,6 +191,38 @@ def ssm_scan_bwd(x, delta, A, b, c, h0, ckpt, dy, ghT=None, *, ckpt_interval=0, 
     return out
 
 
+def ssm_scan_fwd_noalloc(x, delta, A, b, c, h0=None, *, ckpt_interval=0, chunk_len=0, y=None, hT=None, ckpt=None,
+                         stream=None):
+    """Forward scan through ssm_scan_fwd_noalloc: the chunked schedule with its
+    scratch in the library's fixed device array, for callers that cannot
+    allocate scratch memory (outputs can be passed in so nothing is allocated
+    here either). Returns (y, hT, ckpt)."""
+    torch = _torch()
+    L = lib()
+    fn = L.ssm_scan_fwd_noalloc
+    fn.argtypes = [ctypes.POINTER(ssm_scan_desc)] + [ctypes.c_void_p] * 10
+    fn.restype = ctypes.c_int
+    B, T, D = x.shape
+    DS = A.shape[1]
+    dev = x.device
+    for t_, shape, dt, name in ((delta, (B, T, D), x.dtype, "delta"), (A, (D, DS), torch.float32, "A"),
+                                (b, (B, T, DS), x.dtype, "b"), (c, (B, T, DS), x.dtype, "c"),
+                                (h0, (B, D, DS), torch.float32, "h0")):
+        _check(t_, shape, dt, name, dev)
+    desc = make_desc(B, T, D, DS, _io_of(x), ckpt_interval, chunk_len)
+    if y is None:
+        y = torch.empty((B, T, D), dtype=x.dtype, device=dev)
+    if hT is None:
+        hT = torch.empty((B, D, DS), dtype=torch.float32, device=dev)
+    if ckpt is None and ckpt_interval > 0:
+        ckpt = torch.empty((-(-T // ckpt_interval), B, D, DS), dtype=torch.float32, device=dev)
+    st = fn(ctypes.byref(desc), _ptr(x), _ptr(delta), _ptr(A), _ptr(b), _ptr(c), _ptr(h0), _ptr(y), _ptr(hT),
+            _ptr(ckpt), _stream(stream))
+    if st != 0:
+        raise SSMError(st, "ssm_scan_fwd_noalloc")
+    return y, hT, ckpt
+
+
 def selective_scan(x, delta, A, b, c, h0=None, ckpt_interval=256):
     """Differentiable scan: returns (y, hT). Gradients flow to x, delta, A, b, c and h0;
     hT is differentiated too (its gradient enters the backward as ghT)."""

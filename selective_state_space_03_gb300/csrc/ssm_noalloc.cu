@@ -1,0 +1,135 @@
+// ssm_scan_fwd_noalloc: the chunked forward scan with its scratch memory in a
+// fixed device array owned by this library, for callers that cannot allocate.
+//
+// The chunked forward needs scratch for the per-chunk carries (partial end
+// states and delta sums). ssm_scan_fwd takes that scratch from the caller.
+// Some callers cannot provide it: code running inside another runtime that
+// owns all device memory and forbids allocation while it executes (a plugin
+// in an inference engine, a step replayed from a captured graph), or services
+// that must never call cudaMalloc on the hot path because it synchronises the
+// device and can fail under memory pressure. This entry point takes the
+// scratch from `g_scratch` below instead, so it allocates nothing.
+//
+// Costs and rules of that choice:
+//  - every GPU that loads the library holds kNoallocScratchBytes of device
+//    memory for this array until the process exits;
+//  - host code cannot use the array's name as a device address, so the first
+//    call on each device looks the address up (cudaGetSymbolAddress, with
+//    that device current) and caches it; that first call should therefore
+//    happen before any stream capture;
+//  - every call on a device shares the one array: calls that overlap on the
+//    GPU (other streams, other host threads) race on it and must be ordered by
+//    the caller. Pass 1 overwrites every entry pass 2 reads, so nothing in the
+//    array needs clearing between calls.
+#include <mutex>
+
+#include "ssm_internal.h"
+#include "ssm_scan.h"
+
+namespace ssm {
+
+cudaError_t launch_fwd_f32(const FwdLaunch& L, int mode, cudaStream_t stream);
+cudaError_t launch_fwd_bf16(const FwdLaunch& L, int mode, cudaStream_t stream);
+
+namespace {
+
+constexpr size_t kNoallocScratchBytes = SSM_SCAN_NOALLOC_SCRATCH_BYTES;
+static_assert(kNoallocScratchBytes % 256 == 0, "scratch size must keep 256-byte alignment");
+
+static __device__ __align__(256) unsigned char g_scratch[kNoallocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_setup_mutex;
+void* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of g_scratch on the current device (looked up once per device).
+cudaError_t scratch_address(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_setup_mutex);
+    if (g_scratch_addr[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_scratch);
+        if (e != cudaSuccess) return e;
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return cudaSuccess;
+}
+
+size_t up256(size_t v) { return (v + 255) / 256 * 256; }
+int64_t cdiv64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+bool is_aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+}  // namespace ssm
+
+using namespace ssm;
+
+extern "C" ssm_status ssm_scan_fwd_noalloc(const ssm_scan_desc* desc, const void* x, const void* delta,
+                                           const float* A, const void* b, const void* c, const float* h0,
+                                           void* y, float* hT, float* ckpt, void* stream) {
+    if (desc == nullptr) return SSM_ERR_INVALID_ARG;
+    const ssm_scan_desc& d = *desc;
+    if (d.B < 0 || d.T < 0 || d.D < 0 || d.DS < 0) return SSM_ERR_INVALID_ARG;
+    if (d.io != SSM_IO_F32 && d.io != SSM_IO_BF16) return SSM_ERR_INVALID_ARG;
+    if (d.ckpt_interval < 0 || d.reserved != 0 || d.B > 65535) return SSM_ERR_INVALID_ARG;
+    if (d.DS != kDS) return SSM_ERR_UNSUPPORTED;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool work = d.B > 0 && d.T > 0 && d.D > 0;
+    if (work && (!x || !delta || !A || !b || !c || !y)) return SSM_ERR_INVALID_ARG;
+    const void* ptrs[] = {x, delta, A, b, c, h0, y, hT, ckpt};
+    for (const void* p : ptrs)
+        if (p && !is_aligned16(p)) return SSM_ERR_MISALIGNED;
+    if (!work) {
+        if (hT && d.B > 0 && d.D > 0) {
+            const size_t bytes = size_t(d.B) * size_t(d.D) * kDS * 4;
+            const cudaError_t e = h0 ? cudaMemcpyAsync(hT, h0, bytes, cudaMemcpyDeviceToDevice, s)
+                                     : cudaMemsetAsync(hT, 0, bytes, s);
+            if (e != cudaSuccess) return SSM_ERR_CUDA;
+        }
+        return SSM_OK;
+    }
+
+    // chunk length: the caller's, else enough chunks for ~16 resident warps per SM
+    int64_t Lc = d.chunk_len;
+    if (Lc <= 0) {
+        const int64_t want = int64_t(device_sm_count()) * 512;
+        const int64_t nch = cdiv64(want, d.B * d.D * 4);
+        Lc = cdiv64(cdiv64(d.T, nch), 32) * 32;
+        if (Lc < 64) Lc = 64;
+    }
+    const int64_t nchunk = cdiv64(d.T, Lc);
+
+    FwdLaunch L{};
+    L.x = x; L.delta = delta; L.A = A; L.b = b; L.c = c; L.h0 = h0;
+    L.y = y; L.hT = hT; L.ckpt = d.ckpt_interval > 0 ? ckpt : nullptr;
+    L.B = d.B; L.T = d.T; L.D = d.D; L.K = d.ckpt_interval;
+    L.io = d.io == SSM_IO_BF16 ? IO::BF16 : IO::F32;
+    L.vec = (d.D * (d.io == SSM_IO_BF16 ? 2 : 4)) % 16 == 0;
+    L.ckpt_only = false;
+    L.G = 4;
+    auto run = [&](int mode) {
+        return d.io == SSM_IO_BF16 ? launch_fwd_bf16(L, mode, s) : launch_fwd_f32(L, mode, s);
+    };
+    if (nchunk < 2) {            // one chunk: the one-pass scan, which needs no scratch
+        L.Lc = d.T;
+        L.nchunk = 1;
+        return run(0) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+    }
+    const size_t bytes_S = up256(size_t(d.B) * size_t(nchunk - 1) * size_t(d.D) * kDS * 4);
+    const size_t bytes_Sd = up256(size_t(d.B) * size_t(nchunk - 1) * size_t(d.D) * 4);
+    if (bytes_S + bytes_Sd > kNoallocScratchBytes) return SSM_ERR_WORKSPACE;
+
+    void* base = nullptr;
+    if (scratch_address(&base) != cudaSuccess) return SSM_ERR_CUDA;
+    L.Lc = Lc;
+    L.nchunk = nchunk;
+    L.ws_S = static_cast<float*>(base);
+    L.ws_Sd = reinterpret_cast<float*>(static_cast<unsigned char*>(base) + bytes_S);
+    cudaError_t e = run(1);
+    if (e == cudaSuccess) e = run(2);
+    return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}

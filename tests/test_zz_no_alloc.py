@@ -1,0 +1,77 @@
+"""ssm_scan_fwd_noalloc: the forward that allocates nothing.
+
+Some callers cannot allocate device memory while they run (code hosted in
+another runtime that owns all device memory, or services that keep cudaMalloc
+off the hot path because it synchronises the device and can fail under memory
+pressure). For them the library keeps the chunked forward's scratch in a fixed
+device array. These tests call that entry point through the C ABI (ctypes)
+and compare it with ssm_scan_fwd on the same inputs and chunk length, on two
+calls in a row (the second reuses the array the first one wrote). The file is
+named so that pytest collects it last.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+import gen
+from gpu_util import assert_close, dev_inputs, to_host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def L():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from selective_state_space_03_gb300 import build
+    build.build()
+    torch.cuda.set_device(0)
+    import selective_state_space_03_gb300 as ssm
+    lib = ssm.lib()
+    lib.ssm_scan_fwd_noalloc.argtypes = [ctypes.POINTER(ssm.ssm_scan_desc)] + [ctypes.c_void_p] * 10
+    lib.ssm_scan_fwd_noalloc.restype = ctypes.c_int
+    return lib
+
+
+def call_noalloc(L, t, w, K, chunk_len):
+    import torch
+    import selective_state_space_03_gb300 as ssm
+    B, T, D = w.B, w.T, w.D
+    io = ssm.SSM_IO_BF16 if w.io == "bf16" else ssm.SSM_IO_F32
+    desc = ssm.make_desc(B, T, D, 16, io, K, chunk_len)
+    y = torch.empty_like(t["x"])
+    hT = torch.empty((B, D, 16), dtype=torch.float32, device="cuda:0")
+    ck = torch.empty((-(-T // K), B, D, 16), dtype=torch.float32, device="cuda:0")
+    p = lambda v: None if v is None else ctypes.c_void_p(v.data_ptr())  # noqa: E731
+    st = L.ssm_scan_fwd_noalloc(ctypes.byref(desc), p(t["x"]), p(t["delta"]), p(t["A"]), p(t["b"]), p(t["c"]),
+                                p(t["h0"]), p(y), p(hT), p(ck), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0, st
+    return y, hT, ck
+
+
+def test_noalloc_matches_workspace_forward_two_calls(L):
+    import torch
+    import selective_state_space_03_gb300 as ssm
+    cases = [(gen.workload(2, B=2, T=700, D=96, h0_std=0.1), 128, 100, 0),
+             (gen.workload(5, B=3, T=513, D=64), 64, 96, 1)]
+    for w, K, chunk_len, seed in cases:
+        t = dev_inputs(gen.make_inputs(w, seed=seed, with_grad_inputs=False))
+        y0, h0, c0 = ssm.ssm_scan_fwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], ckpt_interval=K,
+                                      chunk_len=chunk_len)
+        y1, h1, c1 = call_noalloc(L, t, w, K, chunk_len)
+        torch.cuda.synchronize()
+        assert_close(to_host(y1), to_host(y0), w.io, "fwd", "y")
+        assert_close(to_host(h1), to_host(h0), w.io, "fwd", "hT")
+        assert_close(to_host(c1), to_host(c0), w.io, "fwd", "ckpt")
+
+
+def test_noalloc_rejects_problems_beyond_its_scratch(L):
+    import selective_state_space_03_gb300 as ssm
+    fake = ctypes.c_void_p(0x7F0000000000)      # aligned, never dereferenced: the call fails its size check
+    # 2 * 99 carries of 8192 channels: 2*99*8192*68 bytes > the fixed scratch
+    desc = ssm.make_desc(2, 100 * 64, 8192, 16, ssm.SSM_IO_F32, 0, 64)
+    st = L.ssm_scan_fwd_noalloc(ctypes.byref(desc), fake, fake, fake, fake, fake, None, fake, None, None, None)
+    assert st == 4
+    assert np.int64(2 * 99 * 8192 * 68) > (8 << 20)
