@@ -45,6 +45,7 @@ ssm_status check_desc(const ssm_scan_desc* d) {
     if (d->ckpt_interval < 0 || d->reserved != 0) return SSM_ERR_INVALID_ARG;
     if (d->B > 65535) return SSM_ERR_INVALID_ARG;
     if (d->DS != kDS) return SSM_ERR_UNSUPPORTED;
+    if (d->D > kMaxD) return SSM_ERR_UNSUPPORTED;     // kernels use 32-bit in-tile offsets
     return SSM_OK;
 }
 
@@ -85,11 +86,13 @@ FwdPlan plan_fwd(const ssm_scan_desc& d) {
         P.ws_S = align_up(size_t(d.B) * size_t(P.nchunk - 1) * size_t(d.D) * kDS * 4);
         P.ws_Sd = align_up(size_t(d.B) * size_t(P.nchunk - 1) * size_t(d.D) * 4);
     } else {
-        P.G = chains >= want ? 1 : (chains * 2 >= want ? 2 : 4);
-        // testing aid: force the lanes per chain of the one-pass schedule
+        // 2 lanes x 4 channels per lane (64 channels per warp) when that still gives
+        // ~6 warps per SM; otherwise 4 lanes x 1 channel (8 channels per warp)
+        P.G = chains >= int64_t(device_sm_count()) * 6 * 64 ? 2 : 4;
+        // testing aid: force the lane layout of the one-pass schedule (2 or 4)
         if (const char* env = std::getenv("SSM_SCAN_FORCE_LANES")) {
             const int g = std::atoi(env);
-            if (g == 1 || g == 2 || g == 4) P.G = g;
+            if (g == 2 || g == 4) P.G = g;
         }
     }
     return P;

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <type_traits>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
@@ -89,6 +90,57 @@ __device__ __forceinline__ void widen_bf16(float* dst, const __nv_bfloat16* src,
         hi.z = __uint_as_float(w[3] << 16); hi.w = __uint_as_float(w[3] & 0xffff0000u);
         *reinterpret_cast<float4*>(dst + i) = lo;
         *reinterpret_cast<float4*>(dst + i + 4) = hi;
+    }
+}
+
+// ---------------------------------------------------------------- small vector loads / stores
+//
+// N consecutive I/O elements (N * sizeof(T) bytes, naturally aligned) in one
+// shared- or global-memory access, widened to / narrowed from float32.
+template <typename T, int N>
+__device__ __forceinline__ void load_vals(const T* p, float (&v)[N]) {
+    if constexpr (std::is_same<T, float>::value) {
+        if constexpr (N == 4) {
+            const float4 q = *reinterpret_cast<const float4*>(p);
+            v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+        } else if constexpr (N == 2) {
+            const float2 q = *reinterpret_cast<const float2*>(p);
+            v[0] = q.x; v[1] = q.y;
+        } else {
+#pragma unroll
+            for (int i = 0; i < N; ++i) v[i] = p[i];
+        }
+    } else {
+        if constexpr (N == 4) {
+            const uint2 q = *reinterpret_cast<const uint2*>(p);
+            v[0] = __uint_as_float(q.x << 16); v[1] = __uint_as_float(q.x & 0xffff0000u);
+            v[2] = __uint_as_float(q.y << 16); v[3] = __uint_as_float(q.y & 0xffff0000u);
+        } else if constexpr (N == 2) {
+            const uint32_t q = *reinterpret_cast<const uint32_t*>(p);
+            v[0] = __uint_as_float(q << 16); v[1] = __uint_as_float(q & 0xffff0000u);
+        } else {
+#pragma unroll
+            for (int i = 0; i < N; ++i) v[i] = to_f32(p[i]);
+        }
+    }
+}
+
+template <typename T, int N>
+__device__ __forceinline__ void store_vals(T* p, const float (&v)[N]) {
+    if constexpr (std::is_same<T, float>::value) {
+        if constexpr (N == 2) {
+            *reinterpret_cast<float2*>(p) = make_float2(v[0], v[1]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < N; ++i) p[i] = v[i];
+        }
+    } else {
+        if constexpr (N == 2) {
+            *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(v[0], v[1]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < N; ++i) p[i] = __float2bfloat16_rn(v[i]);
+        }
     }
 }
 

@@ -9,14 +9,29 @@
 // sums of every chunk but the last; pass 2 folds the carries of chunks 0..k-1
 // into the start state of chunk k and rescans the chunk with readout.
 //
-// Thread layout: a CTA of NT threads covers DT = NT / G channels d of one
-// batch b; each channel's DS = 16 states are split over G neighbouring lanes
-// (KS = 16 / G states per lane, kept in registers for the whole sweep). Time
-// is walked in tiles of TT steps; x, delta, b, c tiles are double-buffered in
-// shared memory with cp.async (zero-filled past the end, which leaves the
-// state unchanged: delta = 0 gives decay 1 and no input). With G > 1 the
-// readout <h_t, c_t> is finished by a reduce-scatter over G steps, and y is
-// written back a tile at a time with 16-byte stores.
+// Work per element is one ex2 on the MUFU (32/clk/SM on GB300) and four FP32
+// operations (delta*A, delta*x*b, a*h + u, h*c), i.e. the MUFU and the FP32
+// pipe (128 lanes/clk/SM) are both busy 1/32 clk per element: the kernel is
+// built to spend as few issue slots as possible on anything else.
+//  - One-warp CTAs, so the grid spreads evenly over the SMs and late CTAs run
+//    alone at full speed instead of leaving a quantised last wave.
+//  - A lane owns KD neighbouring channels x 16/G states (kept in registers for
+//    the whole sweep); each channel's 16 states are split over G lanes. b and c
+//    are the same for every channel, so each b/c value a lane reads from
+//    shared memory feeds KD channels: broadcast shared loads deliver only 4
+//    bytes per wavefront, which would cap the kernel at 16*KD elements per
+//    clock per SM. KD = 2, G = 2 is used when there are enough (b, d) chains;
+//    KD = 1, G = 4 otherwise. State pairs use packed FP32x2 multiply/FMA.
+//  - x, delta, b, c tiles of TT steps are double-buffered in shared memory with
+//    16-byte cp.async, zero-filled past the end (delta = 0 gives decay 1 and no
+//    input, so padded steps leave the state unchanged). bf16 b and c are
+//    widened to float32 once per tile.
+//  - The readout <h_t, c_t> is finished across the G lanes of a channel: with
+//    KD > 1 by a reduce-scatter over the lane's channels, with KD = 1 by a
+//    reduce-scatter over G steps. y goes to a shared-memory tile and leaves in
+//    16-byte stores once per tile; checkpoints are written at tile starts when
+//    every checkpoint step is one; staging offsets are per-lane constants, so a
+//    full tile costs a few instructions per 16-byte chunk.
 #pragma once
 
 #include <type_traits>
@@ -28,24 +43,38 @@ namespace ssm {
 
 enum FwdMode { kSingle = 0, kPass1 = 1, kPass2 = 2, kCkptOnly = 3 };
 
-template <typename TIO, int G>
+template <typename TIO, int G, int KD>
 struct FwdCfg {
-    static constexpr int NT = 128;
-    static constexpr int KS = kDS / G;
-    static constexpr int DT = NT / G;
-    static constexpr int TT = 32;
+    static constexpr int NT = 32;                                // one warp per CTA
+    static constexpr int KS = kDS / G;                           // states per lane
+    static constexpr int KP = KS / 2;                            // state pairs per lane
+    static constexpr int DT = NT / G * KD;                       // channels per CTA
+    static constexpr int TT = 16;                                // steps per tile
     static constexpr bool BF = std::is_same<TIO, __nv_bfloat16>::value;
+    static constexpr int EPC = 16 / int(sizeof(TIO));           // I/O elements per 16-byte chunk
+    static constexpr int X_CPR = DT / EPC;                       // x/delta chunks per tile row
+    static constexpr int X_CH = TT * X_CPR;                      // x/delta chunks per tile
+    static constexpr int X_PL = (X_CH + NT - 1) / NT;            // ... per lane
+    static constexpr int BC_CPR = kDS / EPC;
+    static constexpr int BC_CH = TT * BC_CPR;
+    static constexpr int BC_PL = (BC_CH + NT - 1) / NT;
+    static constexpr int Y_CH = TT * X_CPR;                      // y chunks per tile
+    static constexpr int Y_PL = (Y_CH + NT - 1) / NT;
     static constexpr size_t X_BYTES = size_t(2) * TT * DT * sizeof(TIO);     // one tensor, 2 buffers
     static constexpr size_t BC_RAW = size_t(2) * TT * kDS * sizeof(TIO);    // one tensor, 2 buffers
     static constexpr size_t BC_F32 = BF ? size_t(TT) * kDS * 4 : 0;          // widened copy (bf16)
-    static constexpr size_t Y_BYTES = size_t(TT) * DT * 4;
+    static constexpr size_t Y_BYTES = size_t(TT) * DT * sizeof(TIO);
     static constexpr size_t SMEM = 2 * X_BYTES + 2 * BC_RAW + 2 * BC_F32 + Y_BYTES;
+    // registers: keep enough warps resident for the whole grid of the largest shapes
+    static constexpr int MINB = (KD == 2) ? 20 : 1;
+    static_assert(KD == 1 || G == 2, "multi-channel lanes are built with 2 lanes per channel");
+    static_assert(X_CPR >= 1 && DT % EPC == 0, "tile rows must be whole 16-byte chunks");
 };
 
-template <typename TIO, int G, bool VEC, int MODE>
-__global__ void __launch_bounds__(128) fwd_kernel(const FwdLaunch p) {
-    using C = FwdCfg<TIO, G>;
-    constexpr int NT = C::NT, KS = C::KS, DT = C::DT, TT = C::TT;
+template <typename TIO, int G, int KD, bool VEC, int MODE, bool CKT>
+__global__ void __launch_bounds__(32, FwdCfg<TIO, G, KD>::MINB) fwd_kernel(const FwdLaunch p) {
+    using C = FwdCfg<TIO, G, KD>;
+    constexpr int NT = C::NT, KS = C::KS, KP = C::KP, DT = C::DT, TT = C::TT, EPC = C::EPC;
     constexpr bool READ = (MODE == kSingle || MODE == kPass2);
 
     extern __shared__ __align__(16) unsigned char smem[];
@@ -55,58 +84,114 @@ __global__ void __launch_bounds__(128) fwd_kernel(const FwdLaunch p) {
     TIO* csr = reinterpret_cast<TIO*>(smem + 2 * C::X_BYTES + C::BC_RAW);
     float* bsf = reinterpret_cast<float*>(smem + 2 * C::X_BYTES + 2 * C::BC_RAW);
     float* csf = bsf + (C::BF ? TT * kDS : 0);
-    float* ys = reinterpret_cast<float*>(smem + 2 * C::X_BYTES + 2 * C::BC_RAW + 2 * C::BC_F32);
+    TIO* ys = reinterpret_cast<TIO*>(smem + 2 * C::X_BYTES + 2 * C::BC_RAW + 2 * C::BC_F32);
 
-    const int tid = threadIdx.x;
-    const int cg = tid / G;          // channel within the CTA
-    const int gl = tid % G;          // lane within the channel's group
+    const int lane = threadIdx.x;
+    const int gl = lane % G;                 // lane within the channel group
+    const int c0 = (lane / G) * KD;          // first channel of this lane within the CTA
     const int s0 = gl * KS;
     const int64_t T = p.T, D = p.D;
     const int64_t b = blockIdx.z;
     const int64_t d0 = int64_t(blockIdx.x) * DT;
-    const int64_t d = d0 + cg;
-    const bool valid = d < D;
+    const int64_t nprev = p.nchunk - 1;      // chunks with a stored carry
     const int64_t chunk = (MODE == kPass1 || MODE == kPass2) ? int64_t(blockIdx.y) : 0;
     const int64_t t_begin = chunk * p.Lc;
     const int64_t t_end = (MODE == kPass1 || MODE == kPass2) ? min(T, t_begin + p.Lc) : T;
-    const int64_t nprev = p.nchunk - 1;   // chunks with a stored carry
+    const bool full_d = d0 + DT <= D;
 
     const TIO* xg = static_cast<const TIO*>(p.x) + b * T * D;
     const TIO* dg = static_cast<const TIO*>(p.delta) + b * T * D;
     const TIO* bg = static_cast<const TIO*>(p.b) + b * T * kDS;
     const TIO* cgl = static_cast<const TIO*>(p.c) + b * T * kDS;
+    TIO* yg = static_cast<TIO*>(p.y) + b * T * D;
 
-    float A2[KS], h[KS];
+    bool valid[KD];
+    float2 A2[KD][KP], h[KD][KP];
 #pragma unroll
-    for (int s = 0; s < KS; ++s) {
-        A2[s] = valid ? p.A[d * kDS + s0 + s] * kLog2e : 0.f;
-        h[s] = 0.f;
-    }
-    if (MODE != kPass1 && valid && p.h0 != nullptr) {
+    for (int k = 0; k < KD; ++k) {
+        const int64_t d = d0 + c0 + k;
+        valid[k] = d < D;
 #pragma unroll
-        for (int s = 0; s < KS; ++s) h[s] = p.h0[(b * D + d) * kDS + s0 + s];
-    }
-    if (MODE == kPass2 && valid) {
-        // start state of this chunk: fold the carries of the chunks before it
-        for (int64_t j = 0; j < chunk; ++j) {
-            const int64_t row = (b * nprev + j) * D + d;
-            const float sd = p.ws_Sd[row];
+        for (int q = 0; q < KP; ++q) {
+            A2[k][q] = valid[k] ? make_float2(p.A[d * kDS + s0 + 2 * q] * kLog2e, p.A[d * kDS + s0 + 2 * q + 1] * kLog2e)
+                                : make_float2(0.f, 0.f);
+            h[k][q] = make_float2(0.f, 0.f);
+        }
+        if (MODE != kPass1 && valid[k] && p.h0 != nullptr) {
+            const float* src = p.h0 + (b * D + d) * kDS + s0;
 #pragma unroll
-            for (int s = 0; s < KS; ++s) h[s] = fmaf(ex2(A2[s] * sd), h[s], p.ws_S[row * kDS + s0 + s]);
+            for (int q = 0; q < KP; ++q) h[k][q] = make_float2(src[2 * q], src[2 * q + 1]);
+        }
+        if (MODE == kPass2 && valid[k]) {
+            // start state of this chunk: fold the carries of the chunks before it
+            for (int64_t j = 0; j < chunk; ++j) {
+                const int64_t row = (b * nprev + j) * D + d;
+                const float sd = p.ws_Sd[row];
+                const float* S = p.ws_S + row * kDS + s0;
+#pragma unroll
+                for (int q = 0; q < KP; ++q) {
+                    const float2 P = make_float2(ex2(A2[k][q].x * sd), ex2(A2[k][q].y * sd));
+                    h[k][q] = __ffma2_rn(P, h[k][q], make_float2(S[2 * q], S[2 * q + 1]));
+                }
+            }
         }
     }
-    float dsum = 0.f;
+    float dsum[KD];
+#pragma unroll
+    for (int k = 0; k < KD; ++k) dsum[k] = 0.f;
     const int64_t K = p.K;
     const bool want_ckpt = (MODE != kPass1) && p.ckpt != nullptr && K > 0;
     int64_t next_ck = want_ckpt ? ((t_begin + K - 1) / K) * K : INT64_MAX;
 
+    // This lane's share of the 16-byte chunks of a full tile, as element offsets from
+    // the tile's first row (x, delta and y tiles share one geometry; b and c another).
+    int x_goff[C::X_PL], x_soff[C::X_PL], bc_off[C::BC_PL];
+#pragma unroll
+    for (int k = 0; k < C::X_PL; ++k) {
+        const int i = lane + NT * k;
+        const int r = i / C::X_CPR, cc = i % C::X_CPR;
+        x_goff[k] = r * int(D) + cc * EPC;
+        x_soff[k] = r * DT + cc * EPC;
+    }
+#pragma unroll
+    for (int k = 0; k < C::BC_PL; ++k) bc_off[k] = (lane + NT * k) * EPC;   // rows of 16 are contiguous
+
     const int64_t ntiles = (t_end - t_begin + TT - 1) / TT;
     auto stage = [&](int64_t tile, int buf) {
         const int64_t t0 = t_begin + tile * TT;
-        stage_tile<TIO, TT, DT, NT, VEC>(xs + buf * TT * DT, xg, D, t0, t_end, d0);
-        stage_tile<TIO, TT, DT, NT, VEC>(ds + buf * TT * DT, dg, D, t0, t_end, d0);
-        stage_tile<TIO, TT, kDS, NT, true>(bsr + buf * TT * kDS, bg, kDS, t0, t_end, 0);
-        if (READ) stage_tile<TIO, TT, kDS, NT, true>(csr + buf * TT * kDS, cgl, kDS, t0, t_end, 0);
+        if (VEC && full_d && t0 + TT <= t_end) {
+            const TIO* xsrc = xg + t0 * D + d0;
+            const TIO* dsrc = dg + t0 * D + d0;
+#pragma unroll
+            for (int k = 0; k < C::X_PL; ++k) {
+                if (C::X_CH % NT == 0 || lane + NT * k < C::X_CH) {
+                    cp_async16(xs + buf * TT * DT + x_soff[k], xsrc + x_goff[k], 16);
+                    cp_async16(ds + buf * TT * DT + x_soff[k], dsrc + x_goff[k], 16);
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < C::BC_PL; ++k) {
+                if (C::BC_CH % NT == 0 || lane + NT * k < C::BC_CH) {
+                    cp_async16(bsr + buf * TT * kDS + bc_off[k], bg + t0 * kDS + bc_off[k], 16);
+                    if (READ) cp_async16(csr + buf * TT * kDS + bc_off[k], cgl + t0 * kDS + bc_off[k], 16);
+                }
+            }
+        } else {
+            stage_tile<TIO, TT, DT, NT, VEC>(xs + buf * TT * DT, xg, D, t0, t_end, d0);
+            stage_tile<TIO, TT, DT, NT, VEC>(ds + buf * TT * DT, dg, D, t0, t_end, d0);
+            stage_tile<TIO, TT, kDS, NT, true>(bsr + buf * TT * kDS, bg, kDS, t0, t_end, 0);
+            if (READ) stage_tile<TIO, TT, kDS, NT, true>(csr + buf * TT * kDS, cgl, kDS, t0, t_end, 0);
+        }
+    };
+    auto store_state = [&](float* base) {     // the lane's KD x KS states into a (.., D, 16) array
+#pragma unroll
+        for (int k = 0; k < KD; ++k) {
+            if (!valid[k]) continue;
+            float4* dst = reinterpret_cast<float4*>(base + (b * D + d0 + c0 + k) * kDS + s0);
+#pragma unroll
+            for (int q = 0; q < KP; q += 2)
+                dst[q / 2] = make_float4(h[k][q].x, h[k][q].y, h[k][q + 1].x, h[k][q + 1].y);
+        }
     };
 
     if (ntiles > 0) {
@@ -122,13 +207,13 @@ __global__ void __launch_bounds__(128) fwd_kernel(const FwdLaunch p) {
         } else {
             cp_async_wait<0>();
         }
-        __syncthreads();
+        __syncwarp();
         const float* bt;
         const float* ct;
         if constexpr (C::BF) {
             widen_bf16<NT>(bsf, reinterpret_cast<const __nv_bfloat16*>(bsr + buf * TT * kDS), TT * kDS);
             if (READ) widen_bf16<NT>(csf, reinterpret_cast<const __nv_bfloat16*>(csr + buf * TT * kDS), TT * kDS);
-            __syncthreads();
+            __syncwarp();
             bt = bsf;
             ct = csf;
         } else {
@@ -138,91 +223,121 @@ __global__ void __launch_bounds__(128) fwd_kernel(const FwdLaunch p) {
         const TIO* xt = xs + buf * TT * DT;
         const TIO* dt = ds + buf * TT * DT;
         const int64_t t0 = t_begin + tile * TT;
+        if (CKT && t0 == next_ck) {               // checkpoints fall on tile starts
+            if (next_ck < t_end) store_state(p.ckpt + (next_ck / K) * p.B * D * kDS);
+            next_ck += K;
+        }
+        constexpr int RG = (KD == 1) ? G : 1;   // steps per readout group
 
+#pragma unroll 8
+        for (int tt = 0; tt < TT; tt += RG) {
+            float part[RG][KD];
 #pragma unroll
-        for (int tt = 0; tt < TT; tt += G) {
-            float part[G];
-#pragma unroll
-            for (int j = 0; j < G; ++j) {
+            for (int j = 0; j < RG; ++j) {
                 const int r = tt + j;
-                if (want_ckpt && t0 + r == next_ck) {
-                    if (valid && next_ck < t_end) {
-                        float* dst = p.ckpt + ((next_ck / K * p.B + b) * D + d) * kDS + s0;
-#pragma unroll
-                        for (int s = 0; s < KS; ++s) dst[s] = h[s];
-                    }
+                if (!CKT && want_ckpt && t0 + r == next_ck) {
+                    if (next_ck < t_end) store_state(p.ckpt + (next_ck / K) * p.B * D * kDS);
                     next_ck += K;
                 }
-                const float dl = to_f32(dt[r * DT + cg]);
-                const float xv = to_f32(xt[r * DT + cg]);
-                const float dx = dl * xv;
-                if (MODE == kPass1) dsum += dl;
-                float acc = 0.f;
+                float dl[KD], xv[KD];
+                load_vals<TIO, KD>(dt + r * DT + c0, dl);
+                load_vals<TIO, KD>(xt + r * DT + c0, xv);
+                float2 bb[KP], cc[KP];
 #pragma unroll
-                for (int s = 0; s < KS; ++s) {
-                    const float a = ex2(dl * A2[s]);
-                    h[s] = fmaf(a, h[s], dx * bt[r * kDS + s0 + s]);
-                    if (READ) acc = fmaf(h[s], ct[r * kDS + s0 + s], acc);
-                }
-                part[j] = acc;
-            }
-            if (READ) ys[(tt + gl) * DT + cg] = reduce_scatter_steps<G>(part, gl);
-        }
-        __syncthreads();
-        if (READ) {
-            // y tile -> global, rows [t0, t_end), columns [d0, D)
-            TIO* yg = static_cast<TIO*>(p.y) + b * T * D;
-            const int64_t rows = min(int64_t(TT), t_end - t0);
-            if constexpr (VEC) {
-                constexpr int EPC = 16 / sizeof(TIO);
-                constexpr int CPR = DT / EPC;
-                for (int i = tid; i < TT * CPR; i += NT) {
-                    const int r = i / CPR, cc = i % CPR;
-                    const int64_t col = d0 + int64_t(cc) * EPC;
-                    if (r < rows && col < D) {
-                        const float* src = ys + r * DT + cc * EPC;
-                        uint4 v;
-                        if constexpr (C::BF) {
-                            __nv_bfloat162 q[4];
-#pragma unroll
-                            for (int k = 0; k < 4; ++k) q[k] = __floats2bfloat162_rn(src[2 * k], src[2 * k + 1]);
-                            v = *reinterpret_cast<const uint4*>(q);
-                        } else {
-                            v = *reinterpret_cast<const uint4*>(src);
-                        }
-                        *reinterpret_cast<uint4*>(yg + (t0 + r) * D + col) = v;
+                for (int q = 0; q < KP; q += 2) {
+                    const float4 b4 = *reinterpret_cast<const float4*>(bt + r * kDS + s0 + 2 * q);
+                    bb[q] = make_float2(b4.x, b4.y);
+                    bb[q + 1] = make_float2(b4.z, b4.w);
+                    if (READ) {
+                        const float4 c4 = *reinterpret_cast<const float4*>(ct + r * kDS + s0 + 2 * q);
+                        cc[q] = make_float2(c4.x, c4.y);
+                        cc[q + 1] = make_float2(c4.z, c4.w);
                     }
                 }
-            } else {
-                for (int i = tid; i < TT * DT; i += NT) {
-                    const int r = i / DT, cc = i % DT;
-                    if (r < rows && d0 + cc < D) yg[(t0 + r) * D + d0 + cc] = from_f32<TIO>(ys[i]);
+#pragma unroll
+                for (int k = 0; k < KD; ++k) {
+                    if (MODE == kPass1) dsum[k] += dl[k];
+                    const float dx = dl[k] * xv[k];
+                    // Scalar multiplies and readout, packed FMA for the state update:
+                    // on sm_103a this mix issues the fewest instructions per element.
+                    float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+                    for (int q = 0; q < KP; ++q) {
+                        const float2 a = make_float2(ex2(dl[k] * A2[k][q].x), ex2(dl[k] * A2[k][q].y));
+                        const float2 u = make_float2(dx * bb[q].x, dx * bb[q].y);
+                        h[k][q] = __ffma2_rn(a, h[k][q], u);
+                        if (READ) {
+                            acc0 = fmaf(h[k][q].x, cc[q].x, acc0);
+                            acc1 = fmaf(h[k][q].y, cc[q].y, acc1);
+                        }
+                    }
+                    part[j][k] = acc0 + acc1;
                 }
             }
+            if (READ) {
+                if constexpr (KD == 1) {
+                    float v[G];
+#pragma unroll
+                    for (int j = 0; j < G; ++j) v[j] = part[j][0];
+                    ys[(tt + gl) * DT + c0] = from_f32<TIO>(reduce_scatter_steps<G>(v, gl));
+                } else {
+                    // two lanes per channel group: lane gl keeps channels [gl*KD/2, (gl+1)*KD/2)
+                    constexpr int H = KD / 2;
+                    float out[H];
+#pragma unroll
+                    for (int i = 0; i < H; ++i) {
+                        const float send = gl ? part[0][i] : part[0][H + i];
+                        const float keep = gl ? part[0][H + i] : part[0][i];
+                        out[i] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+                    }
+                    store_vals<TIO, H>(ys + tt * DT + c0 + gl * H, out);
+                }
+            }
+        }
+        __syncwarp();
+        if (READ) {
+            // y tile -> global, 16-byte chunks
+            const int64_t rows = min(int64_t(TT), t_end - t0);
+            if (VEC && full_d && rows == TT) {
+                TIO* ydst = yg + t0 * D + d0;
+#pragma unroll
+                for (int k = 0; k < C::X_PL; ++k)
+                    if (C::X_CH % NT == 0 || lane + NT * k < C::X_CH)
+                        *reinterpret_cast<uint4*>(ydst + x_goff[k]) = *reinterpret_cast<const uint4*>(ys + x_soff[k]);
+            } else {
+                for (int i = lane; i < TT * DT; i += NT) {
+                    const int r = i / DT, cc = i % DT;
+                    if (r < rows && d0 + cc < D) yg[(t0 + r) * D + d0 + cc] = ys[i];
+                }
+            }
+            __syncwarp();
         }
     }
 
-    if (!valid) return;
     if (MODE == kPass1) {
-        const int64_t row = (b * nprev + chunk) * D + d;
 #pragma unroll
-        for (int s = 0; s < KS; ++s) p.ws_S[row * kDS + s0 + s] = h[s];
-        if (gl == 0) p.ws_Sd[row] = dsum;
+        for (int k = 0; k < KD; ++k) {
+            if (!valid[k]) continue;
+            const int64_t row = (b * nprev + chunk) * D + d0 + c0 + k;
+            float4* S = reinterpret_cast<float4*>(p.ws_S + row * kDS + s0);
+#pragma unroll
+            for (int q = 0; q < KP; q += 2) S[q / 2] = make_float4(h[k][q].x, h[k][q].y, h[k][q + 1].x, h[k][q + 1].y);
+            if (gl == 0) p.ws_Sd[row] = dsum[k];
+        }
         return;
     }
     const bool last = (MODE != kPass2) || (chunk == p.nchunk - 1);
-    if (last && p.hT != nullptr) {
-#pragma unroll
-        for (int s = 0; s < KS; ++s) p.hT[(b * D + d) * kDS + s0 + s] = h[s];
-    }
+    if (last && p.hT != nullptr) store_state(p.hT);
 }
 
-template <typename TIO, int G, bool VEC, int MODE>
+template <typename TIO, int G, int KD, bool VEC, int MODE, bool CKT>
 cudaError_t launch_fwd_t(const FwdLaunch& L, cudaStream_t stream) {
-    using C = FwdCfg<TIO, G>;
-    auto kern = fwd_kernel<TIO, G, VEC, MODE>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::SMEM));
-    if (e != cudaSuccess) return e;
+    using C = FwdCfg<TIO, G, KD>;
+    auto kern = fwd_kernel<TIO, G, KD, VEC, MODE, CKT>;
+    if (C::SMEM > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::SMEM));
+        if (e != cudaSuccess) return e;
+    }
     unsigned gy = 1;
     if (MODE == kPass1) gy = unsigned(L.nchunk - 1);
     if (MODE == kPass2) gy = unsigned(L.nchunk);
@@ -231,23 +346,30 @@ cudaError_t launch_fwd_t(const FwdLaunch& L, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-// All instantiations for one I/O type.
+// All instantiations for one I/O type. Checkpoints are checked once per tile when
+// every checkpoint step is a tile start (K and the chunk length multiples of 16).
 template <typename TIO>
 cudaError_t launch_fwd_io(const FwdLaunch& L, int mode, cudaStream_t stream) {
-#define SSM_FWD_VEC(G_, MODE_)                                               \
-    return L.vec ? launch_fwd_t<TIO, G_, true, MODE_>(L, stream)             \
-                 : launch_fwd_t<TIO, G_, false, MODE_>(L, stream)
+    constexpr int TT = FwdCfg<TIO, 4, 1>::TT;
+    const bool ckt = L.K == 0 || (L.K % TT == 0 && (mode == kSingle || mode == kCkptOnly || L.Lc % TT == 0));
+#define SSM_FWD_CK(G_, KD_, MODE_, VEC_)                                                   \
+    return ckt ? launch_fwd_t<TIO, G_, KD_, VEC_, MODE_, true>(L, stream)                 \
+               : launch_fwd_t<TIO, G_, KD_, VEC_, MODE_, false>(L, stream)
+#define SSM_FWD_VEC(G_, KD_, MODE_)                                                       \
+    if (L.vec) { SSM_FWD_CK(G_, KD_, MODE_, true); } else { SSM_FWD_CK(G_, KD_, MODE_, false); }
     switch (mode) {
         case kSingle:
-            if (L.G == 1) { SSM_FWD_VEC(1, kSingle); }
-            if (L.G == 2) { SSM_FWD_VEC(2, kSingle); }
-            SSM_FWD_VEC(4, kSingle);
-        case kPass1: SSM_FWD_VEC(4, kPass1);
-        case kPass2: SSM_FWD_VEC(4, kPass2);
-        case kCkptOnly: SSM_FWD_VEC(4, kCkptOnly);
+            if (L.G == 2) { SSM_FWD_VEC(2, 2, kSingle); }
+            SSM_FWD_VEC(4, 1, kSingle);
+        case kPass1:
+            if (L.vec) return launch_fwd_t<TIO, 4, 1, true, kPass1, true>(L, stream);
+            return launch_fwd_t<TIO, 4, 1, false, kPass1, true>(L, stream);
+        case kPass2: SSM_FWD_VEC(4, 1, kPass2);
+        case kCkptOnly: SSM_FWD_VEC(4, 1, kCkptOnly);
         default: return cudaErrorInvalidValue;
     }
 #undef SSM_FWD_VEC
+#undef SSM_FWD_CK
 }
 
 }  // namespace ssm

@@ -7,7 +7,8 @@
 
 namespace ssm {
 
-constexpr int kDS = 16;   // state size the kernels are built for
+constexpr int kDS = 16;                  // state size the kernels are built for
+constexpr int64_t kMaxD = int64_t(1) << 27;   // channels: in-tile offsets (16 rows x D) stay in 32 bits
 
 enum class IO { F32 = 0, BF16 = 1 };
 
@@ -34,7 +35,7 @@ struct FwdLaunch {
     int64_t Lc;     // chunk length (chunked modes; T in mode 0)
     int64_t nchunk; // number of chunks (1 in mode 0)
     IO io;
-    int G;          // lanes per chain: 1, 2 or 4
+    int G;          // lane layout: 2 (2 lanes x 4 channels per lane) or 4 (4 lanes x 1 channel)
     bool vec;       // 16-byte staging allowed
     bool ckpt_only; // mode 0 without readout (checkpoint rebuild for the backward)
 };
