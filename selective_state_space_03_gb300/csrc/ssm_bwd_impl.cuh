@@ -16,13 +16,22 @@
 //   level 3: per sub-chunk, in reverse order, rescan it from its sub-checkpoint
 //            into registers (h_t for LS steps);
 //   reverse: walk the sub-chunk backwards, recomputing a_t, carrying a_t g_t.
-// Thread layout: CTA of 256 threads = 64 channels of one batch, each channel's
-// 16 states on 4 neighbouring lanes (4 states per lane). Sums over s (gx,
-// gdelta) are reduce-scatters over the 4 lanes and 4 steps. Sums over d (gb,
-// gc) are reduce-scatters over the 8 channels of a warp, then shared-memory
-// atomics across the CTA's 8 warps, then one vector atomic add per 4 states
-// per CTA into global memory. gA is accumulated in registers over all steps of
-// the CTA and added atomically once.
+//
+// Layout: a CTA of 128 threads covers 32 channels of one batch; each channel's
+// 16 states are on 4 neighbouring lanes (4 states per lane), so a warp holds 8
+// channels. Per tile of LS steps the raw inputs land in shared memory through
+// cp.async and are converted once into one float4 (delta, delta*x, x, dy) per
+// (step, channel) and float32 b, c rows, so the inner loop reads one 16-byte
+// value per step for the channel and one per 4 states for b and c. The raw
+// buffer is refilled with the next tile while the converted one is used.
+// Sums over s (gx, gdelta) are reduce-scatters over the channel's 4 lanes and
+// 4 steps; sums over d (gb, gc) are reduce-scatters over the warp's 8 channels
+// into per-warp shared slots, summed over the CTA's warps once per tile and added
+// to global memory with one red.global.add.v4.f32 per 4 states per CTA. (On
+// sm_103a shuffles and shared loads share one pipe of ~1 warp-instruction per
+// clock per SM, and a 16-byte broadcast load takes 4 of its cycles, so the
+// reductions are built to spend as few of those cycles as possible.) gA is
+// accumulated in registers over the CTA's whole sweep and added atomically once.
 #pragma once
 
 #include <type_traits>
@@ -34,21 +43,33 @@ namespace ssm {
 
 template <typename TIO>
 struct BwdCfg {
-    static constexpr int NT = 256;
+    static constexpr int NT = 128;
+    static constexpr int NW = NT / 32;
     static constexpr int G = 4;
-    static constexpr int KS = kDS / G;
-    static constexpr int DT = NT / G;
-    static constexpr int LS = 16;                       // sub-chunk length
+    static constexpr int KS = kDS / G;                  // states per lane
+    static constexpr int DT = NT / G;                   // channels per CTA (32)
+    static constexpr int LS = 16;                       // sub-chunk (tile) length
     static constexpr int NSUB = int(kMaxBwdK) / LS;     // sub-checkpoints per chunk
     static constexpr bool BF = std::is_same<TIO, __nv_bfloat16>::value;
-    static constexpr size_t X_BYTES = size_t(2) * LS * DT * sizeof(TIO);   // one tensor, 2 buffers
-    static constexpr size_t BC_RAW = size_t(2) * LS * kDS * sizeof(TIO);
-    static constexpr size_t BC_F32 = BF ? size_t(LS) * kDS * 4 : 0;
-    static constexpr size_t SUB_BYTES = size_t(NSUB) * NT * KS * 4;
-    static constexpr size_t GX_BYTES = size_t(LS) * DT * 4;
-    static constexpr size_t RED_BYTES = size_t(LS) * 2 * kDS * 4;
-    static constexpr size_t SMEM = 3 * X_BYTES + 2 * BC_RAW + 2 * BC_F32 + SUB_BYTES + 2 * GX_BYTES + RED_BYTES;
+    static constexpr int EPC = 16 / int(sizeof(TIO));
+    static constexpr int X_CPR = DT / EPC;              // 16-byte chunks per raw tile row
+    static constexpr int X_CH = LS * X_CPR;
+    static constexpr int BC_CH = LS * kDS / EPC;
+    // shared memory (bytes)
+    static constexpr size_t RAW_X = size_t(LS) * DT * sizeof(TIO);          // one of x, delta, dy
+    static constexpr size_t RAW_BC = size_t(LS) * kDS * sizeof(TIO);        // one of b, c
+    static constexpr size_t CONV = size_t(LS) * DT * 16;                    // float4 per (step, channel)
+    static constexpr size_t BCF = size_t(LS) * kDS * 4;                     // one of b, c as float32
+    static constexpr size_t SUB = size_t(NSUB) * NT * 16;                   // float4 sub-checkpoints
+    static constexpr size_t GBC = size_t(NW) * LS * 2 * kDS * 4;            // per-warp sums of gb, gc for a tile
+    static constexpr size_t SMEM = 3 * RAW_X + 2 * RAW_BC + CONV + 2 * BCF + SUB + GBC;
 };
+
+__device__ __forceinline__ void red_add_v4(float* dst, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};"
+                 :: "l"(dst), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+}
+
 
 // Sum of v[k] over the 8 lanes of a warp that share (lane & 3); lane returns
 // the total of entry (lane >> 2).
@@ -76,46 +97,48 @@ __device__ __forceinline__ float warp_reduce_scatter8(const float (&v)[8], int l
     return keep + __shfl_xor_sync(0xffffffffu, send, 4);
 }
 
-__device__ __forceinline__ void red_add_v4(float* dst, float a, float b, float c, float d) {
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};"
-                 :: "l"(dst), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+__device__ __forceinline__ float4 operator+(const float4 a, const float4 b) {
+    return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
 }
 
 template <typename TIO, bool VEC>
-__global__ void __launch_bounds__(256, 2) bwd_kernel(const BwdLaunch p) {
+__global__ void __launch_bounds__(128, 3) bwd_kernel(const BwdLaunch p) {
     using C = BwdCfg<TIO>;
-    constexpr int NT = C::NT, KS = C::KS, DT = C::DT, LS = C::LS;
+    constexpr int NT = C::NT, KS = C::KS, DT = C::DT, LS = C::LS, EPC = C::EPC;
 
     extern __shared__ __align__(16) unsigned char smem[];
     unsigned char* ptr = smem;
-    TIO* xs = reinterpret_cast<TIO*>(ptr);  ptr += C::X_BYTES;
-    TIO* ds = reinterpret_cast<TIO*>(ptr);  ptr += C::X_BYTES;
-    TIO* dys = reinterpret_cast<TIO*>(ptr); ptr += C::X_BYTES;
-    TIO* bsr = reinterpret_cast<TIO*>(ptr); ptr += C::BC_RAW;
-    TIO* csr = reinterpret_cast<TIO*>(ptr); ptr += C::BC_RAW;
-    float* bsf = reinterpret_cast<float*>(ptr); ptr += C::BC_F32;
-    float* csf = reinterpret_cast<float*>(ptr); ptr += C::BC_F32;
-    float4* sub = reinterpret_cast<float4*>(ptr); ptr += C::SUB_BYTES;   // [NSUB][NT]
-    float* gxs = reinterpret_cast<float*>(ptr); ptr += C::GX_BYTES;      // [LS][DT]
-    float* gds = reinterpret_cast<float*>(ptr); ptr += C::GX_BYTES;      // [LS][DT]
-    float* red = reinterpret_cast<float*>(ptr);                          // [LS][2][16]
+    TIO* xr = reinterpret_cast<TIO*>(ptr);  ptr += C::RAW_X;
+    TIO* dr = reinterpret_cast<TIO*>(ptr);  ptr += C::RAW_X;
+    TIO* yr = reinterpret_cast<TIO*>(ptr);  ptr += C::RAW_X;
+    TIO* br = reinterpret_cast<TIO*>(ptr);  ptr += C::RAW_BC;
+    TIO* cr = reinterpret_cast<TIO*>(ptr);  ptr += C::RAW_BC;
+    float4* conv = reinterpret_cast<float4*>(ptr); ptr += C::CONV;     // [LS][DT]
+    float* bf = reinterpret_cast<float*>(ptr);     ptr += C::BCF;      // [LS][16]
+    float* cf = reinterpret_cast<float*>(ptr);     ptr += C::BCF;
+    float4* sub = reinterpret_cast<float4*>(ptr);  ptr += C::SUB;      // [NSUB][NT]
+    float* gbc = reinterpret_cast<float*>(ptr);                        // [NW][LS][2][16]
 
     const int tid = threadIdx.x;
-    const int lane = tid & 31;
-    const int cg = tid >> 2;
-    const int gl = tid & 3;
-    const int s0 = gl * KS;
+    const int lane = tid & 31, warp = tid >> 5;
+    const int cw = lane >> 2;               // channel within the warp
+    const int sg = lane & 3;                // state group within the channel
+    const int c = warp * 8 + cw;            // channel within the CTA
+    const int s0 = sg * KS;
     const int64_t T = p.T, D = p.D, K = p.K;
     const int64_t b = blockIdx.y;
     const int64_t d0 = int64_t(blockIdx.x) * DT;
-    const int64_t d = d0 + cg;
+    const int64_t d = d0 + c;
     const bool valid = d < D;
+    const bool full_d = d0 + DT <= D;
 
     const TIO* xg = static_cast<const TIO*>(p.x) + b * T * D;
     const TIO* dg = static_cast<const TIO*>(p.delta) + b * T * D;
     const TIO* dyg = static_cast<const TIO*>(p.dy) + b * T * D;
     const TIO* bg = static_cast<const TIO*>(p.b) + b * T * kDS;
     const TIO* cgl = static_cast<const TIO*>(p.c) + b * T * kDS;
+    float* gxg = p.gx + b * T * D;
+    float* gdg = p.gdelta + b * T * D;
 
     float A2[KS], Af[KS], gcarry[KS], gAacc[KS];
 #pragma unroll
@@ -125,24 +148,66 @@ __global__ void __launch_bounds__(256, 2) bwd_kernel(const BwdLaunch p) {
         gcarry[s] = (valid && p.ghT != nullptr) ? p.ghT[(b * D + d) * kDS + s0 + s] : 0.f;
         gAacc[s] = 0.f;
     }
-    for (int i = tid; i < LS * 2 * kDS; i += NT) red[i] = 0.f;
+
+    // this thread's 16-byte chunk of a full raw tile (x, delta, dy) and of b, c
+    const int xr_r = tid / C::X_CPR, xr_c = (tid % C::X_CPR) * EPC;
+    const int x_goff = xr_r * int(D) + xr_c, x_soff = xr_r * DT + xr_c;
+
+    auto stage = [&](int64_t t0, int64_t tend, bool rev) {
+        if (VEC && full_d && t0 + LS <= tend) {
+            if (tid < C::X_CH) {
+                const int64_t base = t0 * D + d0;
+                cp_async16(xr + x_soff, xg + base + x_goff, 16);
+                cp_async16(dr + x_soff, dg + base + x_goff, 16);
+                if (rev) cp_async16(yr + x_soff, dyg + base + x_goff, 16);
+            }
+            if (tid < C::BC_CH) {
+                cp_async16(br + tid * EPC, bg + t0 * kDS + tid * EPC, 16);
+                if (rev) cp_async16(cr + tid * EPC, cgl + t0 * kDS + tid * EPC, 16);
+            }
+        } else {
+            stage_tile<TIO, LS, DT, NT, VEC>(xr, xg, D, t0, tend, d0);
+            stage_tile<TIO, LS, DT, NT, VEC>(dr, dg, D, t0, tend, d0);
+            if (rev) stage_tile<TIO, LS, DT, NT, VEC>(yr, dyg, D, t0, tend, d0);
+            stage_tile<TIO, LS, kDS, NT, true>(br, bg, kDS, t0, tend, 0);
+            if (rev) stage_tile<TIO, LS, kDS, NT, true>(cr, cgl, kDS, t0, tend, 0);
+        }
+        cp_async_commit();
+    };
+    // raw tile -> (delta, delta*x, x, dy) per (step, channel) and float32 b, c rows
+    auto convert = [&](bool rev) {
+#pragma unroll
+        for (int k = 0; k < LS * DT / NT; ++k) {
+            const int i = tid + NT * k;
+            const float dl = to_f32(dr[i]), xv = to_f32(xr[i]);
+            conv[i] = make_float4(dl, dl * xv, xv, rev ? to_f32(yr[i]) : 0.f);
+        }
+#pragma unroll
+        for (int k = 0; k < LS * kDS / NT; ++k) {
+            const int i = tid + NT * k;
+            bf[i] = to_f32(br[i]);
+            if (rev) cf[i] = to_f32(cr[i]);
+        }
+    };
+    // gb, gc of the tile starting at t0: sum the warps' slots, add to global (rows below t_lim)
+    auto flush_gbc = [&](int64_t t0, int64_t t_lim) {
+        const int r = tid >> 3, tau = (tid >> 2) & 1, q = tid & 3;
+        const int off = r * 2 * kDS + tau * kDS + q * 4;
+        float4 v = *reinterpret_cast<const float4*>(gbc + off);
+#pragma unroll
+        for (int w = 1; w < C::NW; ++w) v = v + *reinterpret_cast<const float4*>(gbc + w * LS * 2 * kDS + off);
+        if (t0 + r < t_lim) {
+            float* dst = (tau == 0 ? p.gb : p.gc) + (b * T + t0 + r) * kDS + q * 4;
+            red_add_v4(dst, v.x, v.y, v.z, v.w);
+        }
+    };
 
     const int64_t nck = (T + K - 1) / K;
+    int64_t pend_t0 = -1, pend_lim = 0;       // tile whose gb/gc sums await their flush
     for (int64_t j = nck - 1; j >= 0; --j) {
         const int64_t cs = j * K;
         const int64_t ce = min(T, cs + K);
         const int nsub = int((ce - cs + LS - 1) / LS);
-
-        auto stage = [&](int i, int buf, bool rev) {
-            const int64_t t0 = cs + int64_t(i) * LS;
-            stage_tile<TIO, LS, DT, NT, VEC>(xs + buf * LS * DT, xg, D, t0, ce, d0);
-            stage_tile<TIO, LS, DT, NT, VEC>(ds + buf * LS * DT, dg, D, t0, ce, d0);
-            stage_tile<TIO, LS, kDS, NT, true>(bsr + buf * LS * kDS, bg, kDS, t0, ce, 0);
-            if (rev) {
-                stage_tile<TIO, LS, DT, NT, VEC>(dys + buf * LS * DT, dyg, D, t0, ce, d0);
-                stage_tile<TIO, LS, kDS, NT, true>(csr + buf * LS * kDS, cgl, kDS, t0, ce, 0);
-            }
-        };
 
         // ---- level 2: forward over the chunk, keeping sub-chunk start states
         float h[KS];
@@ -151,69 +216,38 @@ __global__ void __launch_bounds__(256, 2) bwd_kernel(const BwdLaunch p) {
 #pragma unroll
             for (int s = 0; s < KS; ++s) h[s] = valid ? src[s] : 0.f;
         }
-        stage(0, 0, false);
-        cp_async_commit();
+        stage(cs, ce, false);
         for (int i = 0; i < nsub; ++i) {
-            const int buf = i & 1;
-            if (i + 1 < nsub) {
-                stage(i + 1, buf ^ 1, false);
-                cp_async_commit();
-                cp_async_wait<1>();
-            } else {
-                cp_async_wait<0>();
-            }
+            cp_async_wait<0>();
             __syncthreads();
-            const float* bt;
-            if constexpr (C::BF) {
-                widen_bf16<NT>(bsf, reinterpret_cast<const __nv_bfloat16*>(bsr + buf * LS * kDS), LS * kDS);
-                __syncthreads();
-                bt = bsf;
-            } else {
-                bt = reinterpret_cast<const float*>(bsr + buf * LS * kDS);
-            }
+            convert(false);
+            __syncthreads();
+            if (i + 1 < nsub) stage(cs + int64_t(i + 1) * LS, ce, false);
             sub[i * NT + tid] = make_float4(h[0], h[1], h[2], h[3]);
-            const TIO* xt = xs + buf * LS * DT;
-            const TIO* dt = ds + buf * LS * DT;
 #pragma unroll 4
             for (int r = 0; r < LS; ++r) {
-                const float dl = to_f32(dt[r * DT + cg]);
-                const float dx = dl * to_f32(xt[r * DT + cg]);
-#pragma unroll
-                for (int s = 0; s < KS; ++s) h[s] = fmaf(ex2(dl * A2[s]), h[s], dx * bt[r * kDS + s0 + s]);
+                const float2 v = *reinterpret_cast<const float2*>(conv + r * DT + c);   // delta, delta*x
+                const float4 b4 = *reinterpret_cast<const float4*>(bf + r * kDS + s0);
+                h[0] = fmaf(ex2(v.x * A2[0]), h[0], v.y * b4.x);
+                h[1] = fmaf(ex2(v.x * A2[1]), h[1], v.y * b4.y);
+                h[2] = fmaf(ex2(v.x * A2[2]), h[2], v.y * b4.z);
+                h[3] = fmaf(ex2(v.x * A2[3]), h[3], v.y * b4.w);
             }
-            __syncthreads();
         }
 
         // ---- reverse over the sub-chunks
-        stage(nsub - 1, 0, true);
-        cp_async_commit();
+        stage(cs + int64_t(nsub - 1) * LS, ce, true);
         for (int ii = 0; ii < nsub; ++ii) {
             const int i = nsub - 1 - ii;
-            const int buf = ii & 1;
-            if (ii + 1 < nsub) {
-                stage(i - 1, buf ^ 1, true);
-                cp_async_commit();
-                cp_async_wait<1>();
-            } else {
-                cp_async_wait<0>();
-            }
-            __syncthreads();
-            const float* bt;
-            const float* ct;
-            if constexpr (C::BF) {
-                widen_bf16<NT>(bsf, reinterpret_cast<const __nv_bfloat16*>(bsr + buf * LS * kDS), LS * kDS);
-                widen_bf16<NT>(csf, reinterpret_cast<const __nv_bfloat16*>(csr + buf * LS * kDS), LS * kDS);
-                __syncthreads();
-                bt = bsf;
-                ct = csf;
-            } else {
-                bt = reinterpret_cast<const float*>(bsr + buf * LS * kDS);
-                ct = reinterpret_cast<const float*>(csr + buf * LS * kDS);
-            }
-            const TIO* xt = xs + buf * LS * DT;
-            const TIO* dt = ds + buf * LS * DT;
-            const TIO* dyt = dys + buf * LS * DT;
             const int64_t t0 = cs + int64_t(i) * LS;
+            cp_async_wait<0>();
+            __syncthreads();
+            if (pend_t0 >= 0) flush_gbc(pend_t0, pend_lim);
+            convert(true);
+            __syncthreads();
+            if (ii + 1 < nsub) stage(t0 - LS, ce, true);
+            pend_t0 = t0;
+            pend_lim = ce;
 
             // level 3: states of this sub-chunk into registers
             float hs[KS], hw[LS][KS];
@@ -223,93 +257,63 @@ __global__ void __launch_bounds__(256, 2) bwd_kernel(const BwdLaunch p) {
             }
 #pragma unroll
             for (int r = 0; r < LS; ++r) {
-                const float dl = to_f32(dt[r * DT + cg]);
-                const float dx = dl * to_f32(xt[r * DT + cg]);
+                const float2 v = *reinterpret_cast<const float2*>(conv + r * DT + c);
+                const float4 b4 = *reinterpret_cast<const float4*>(bf + r * kDS + s0);
+                const float bb[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
                 for (int s = 0; s < KS; ++s) {
                     const float prev = (r == 0) ? hs[s] : hw[r - 1][s];
-                    hw[r][s] = fmaf(ex2(dl * A2[s]), prev, dx * bt[r * kDS + s0 + s]);
+                    hw[r][s] = fmaf(ex2(v.x * A2[s]), prev, v.y * bb[s]);
                 }
             }
 
-            // reverse sweep over the sub-chunk, 4 steps at a time
+            float* gw = gbc + warp * LS * 2 * kDS;   // this warp's gb, gc sums for the tile
+            // reverse sweep over the sub-chunk, 4 steps per lane reduce-scatter group
 #pragma unroll
             for (int rg = LS - 4; rg >= 0; rg -= 4) {
                 float rr[4], qq[4];
 #pragma unroll
                 for (int jj = 3; jj >= 0; --jj) {
                     const int r = rg + jj;
-                    const float dl = to_f32(dt[r * DT + cg]);
-                    const float dx = dl * to_f32(xt[r * DT + cg]);
-                    const float dyv = to_f32(dyt[r * DT + cg]);
+                    const float4 v = conv[r * DT + c];          // delta, delta*x, x, dy
+                    const float4 b4 = *reinterpret_cast<const float4*>(bf + r * kDS + s0);
+                    const float4 c4 = *reinterpret_cast<const float4*>(cf + r * kDS + s0);
+                    const float bb[4] = {b4.x, b4.y, b4.z, b4.w};
+                    const float cc[4] = {c4.x, c4.y, c4.z, c4.w};
                     float racc = 0.f, qacc = 0.f, part[8];
 #pragma unroll
                     for (int s = 0; s < KS; ++s) {
-                        const float a = ex2(dl * A2[s]);
-                        const float g = fmaf(dyv, ct[r * kDS + s0 + s], gcarry[s]);
+                        const float a = ex2(v.x * A2[s]);
+                        const float g = fmaf(v.w, cc[s], gcarry[s]);
                         gcarry[s] = a * g;
                         const float hp = (r == 0) ? hs[s] : hw[r - 1][s];
                         const float pp = gcarry[s] * hp;
-                        gAacc[s] = fmaf(pp, dl, gAacc[s]);
+                        gAacc[s] = fmaf(pp, v.x, gAacc[s]);
                         racc = fmaf(pp, Af[s], racc);
-                        qacc = fmaf(g, bt[r * kDS + s0 + s], qacc);
-                        part[s] = g * dx;               // gb partial (this channel)
-                        part[4 + s] = dyv * hw[r][s];   // gc partial (this channel)
+                        qacc = fmaf(g, bb[s], qacc);
+                        part[s] = g * v.y;                      // gb term of this channel
+                        part[4 + s] = v.w * hw[r][s];           // gc term of this channel
                     }
                     rr[jj] = racc;
                     qq[jj] = qacc;
-                    const float v = warp_reduce_scatter8(part, lane);
-                    const int cw = lane >> 2;           // entry this lane now holds
-                    atomicAdd(&red[r * 2 * kDS + (cw >> 2) * kDS + s0 + (cw & 3)], v);
+                    // sum over the warp's 8 channels; this lane keeps entry (cw >> 2, cw & 3)
+                    gw[r * 2 * kDS + (cw >> 2) * kDS + s0 + (cw & 3)] = warp_reduce_scatter8(part, lane);
                 }
-                const float rs = reduce_scatter_steps<4>(rr, gl);
-                const float qs = reduce_scatter_steps<4>(qq, gl);
-                const int r = rg + gl;
-                const float dl = to_f32(dt[r * DT + cg]);
-                const float xv = to_f32(xt[r * DT + cg]);
-                gxs[r * DT + cg] = dl * qs;
-                gds[r * DT + cg] = rs + xv * qs;
-            }
-            __syncthreads();
-
-            // flush the sub-chunk: gx, gdelta tiles; gb, gc partial sums
-            const int64_t rows = min(int64_t(LS), ce - t0);
-            float* gxg = p.gx + b * T * D;
-            float* gdg = p.gdelta + b * T * D;
-            if constexpr (VEC) {
-                constexpr int CPR = DT / 4;
-                for (int k = tid; k < LS * CPR; k += NT) {
-                    const int r = k / CPR, cc = k % CPR;
-                    const int64_t col = d0 + int64_t(cc) * 4;
-                    if (r < rows && col < D) {
-                        *reinterpret_cast<float4*>(gxg + (t0 + r) * D + col) =
-                            *reinterpret_cast<const float4*>(gxs + r * DT + cc * 4);
-                        *reinterpret_cast<float4*>(gdg + (t0 + r) * D + col) =
-                            *reinterpret_cast<const float4*>(gds + r * DT + cc * 4);
-                    }
-                }
-            } else {
-                for (int k = tid; k < LS * DT; k += NT) {
-                    const int r = k / DT, cc = k % DT;
-                    if (r < rows && d0 + cc < D) {
-                        gxg[(t0 + r) * D + d0 + cc] = gxs[k];
-                        gdg[(t0 + r) * D + d0 + cc] = gds[k];
-                    }
+                // sums over the channel's 4 lanes: this lane takes step rg + sg
+                const float rs = reduce_scatter_steps<4>(rr, sg);
+                const float qs = reduce_scatter_steps<4>(qq, sg);
+                const int r = rg + sg;
+                const float4 v = conv[r * DT + c];
+                const int64_t t = t0 + r;
+                if (valid && t < ce) {
+                    gxg[t * D + d] = v.x * qs;
+                    gdg[t * D + d] = rs + v.z * qs;
                 }
             }
-            if (tid < LS * 8) {                         // LS rows x (gb, gc) x 4 quads of states
-                const int r = tid >> 3, tensor = (tid >> 2) & 1, q = tid & 3;
-                if (r < rows) {
-                    const float* src = red + r * 2 * kDS + tensor * kDS + q * 4;
-                    float* dst = (tensor == 0 ? p.gb : p.gc) + (b * T + t0 + r) * kDS + q * 4;
-                    red_add_v4(dst, src[0], src[1], src[2], src[3]);
-                }
-            }
-            __syncthreads();
-            for (int k = tid; k < LS * 2 * kDS; k += NT) red[k] = 0.f;
-            // the next sub-chunk's first barrier orders these zeros before its atomics
         }
     }
+    __syncthreads();
+    if (pend_t0 >= 0) flush_gbc(pend_t0, pend_lim);
 
     if (!valid) return;
 #pragma unroll
