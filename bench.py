@@ -130,7 +130,7 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- CPU oracle timing
 
-def oracle_sample(w, budget_s=12.0, seed=0, max_batches=8):
+def oracle_sample(w, budget_s=12.0, seed=0, max_batches=16):
     """Time the float64 oracle (forward with checkpoints + backward) on the first
     B' batches of workload w (all channels), B' grown until one run takes about
     budget_s seconds (at most max_batches). Returns (elements/s, cores, sample)."""
@@ -403,6 +403,33 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def run_profile_case(args):
+    """One warm-up and one more forward+backward of workload 5 (optionally with B/T
+    replaced), for profilers; prints nothing but 'ok'."""
+    import torch
+    import selective_state_space_03_gb300 as ssm
+    over = {k: v for k, v in (("B", args.B), ("T", args.T)) if v}
+    w = gen.workload(WORKLOAD, **over)
+    inp = gen.make_inputs(w, seed=0)
+    dev = torch.device("cuda", 0)
+
+    def to_dev(a):
+        if a is None:
+            return None
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(a).to(dev)
+
+    t = {k: to_dev(inp.get(k)) for k in ("x", "delta", "A", "b", "c", "h0", "dy")}
+    K = w.ckpt_interval
+    for _ in range(2):
+        _, _, ck = ssm.ssm_scan_fwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], ckpt_interval=K)
+        ssm.ssm_scan_bwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], ck, t["dy"], ckpt_interval=K)
+    torch.cuda.synchronize()
+    print("ok")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -411,7 +438,14 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extra", action="store_true", help="skip the other two workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle timing")
+    ap.add_argument("--profile", action="store_true",
+                    help="run one warm-up and one forward+backward for a profiler, no timing")
+    ap.add_argument("--B", type=int, default=0, help="with --profile: batch size instead of 16")
+    ap.add_argument("--T", type=int, default=0, help="with --profile: sequence length instead of 2048")
     args = ap.parse_args()
+    if args.profile:
+        run_profile_case(args)
+        return
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
     local_rank = int(os.environ.get("LOCAL_RANK", 0))

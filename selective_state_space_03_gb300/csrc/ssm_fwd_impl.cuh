@@ -229,7 +229,7 @@ __global__ void __launch_bounds__(32, FwdCfg<TIO, G, KD>::MINB) fwd_kernel(const
         }
         constexpr int RG = (KD == 1) ? G : 1;   // steps per readout group
 
-#pragma unroll 8
+#pragma unroll
         for (int tt = 0; tt < TT; tt += RG) {
             float part[RG][KD];
 #pragma unroll
