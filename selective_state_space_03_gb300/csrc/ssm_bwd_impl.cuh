@@ -14,7 +14,9 @@
 //   level 2: scan the chunk forward from its checkpoint and keep the state at
 //            the start of every LS-step sub-chunk in shared memory;
 //   level 3: per sub-chunk, in reverse order, rescan it from its sub-checkpoint
-//            into registers (h_t for LS steps);
+//            into a window of tensor memory (h_t for LS steps; TMEM keeps the
+//            64 registers the window would take free for occupancy, and its
+//            traffic bypasses the shared-memory pipe);
 //   reverse: walk the sub-chunk backwards, recomputing a_t, carrying a_t g_t.
 //
 // Layout: a CTA of 128 threads covers 32 channels of one batch; each channel's
@@ -38,6 +40,7 @@
 
 #include "ssm_common.cuh"
 #include "ssm_internal.h"
+#include "ssm_tmem.cuh"
 
 namespace ssm {
 
@@ -62,7 +65,11 @@ struct BwdCfg {
     static constexpr size_t BCF = size_t(LS) * kDS * 4;                     // one of b, c as float32
     static constexpr size_t SUB = size_t(NSUB) * NT * 16;                   // float4 sub-checkpoints
     static constexpr size_t GBC = size_t(NW) * LS * 2 * kDS * 4;            // per-warp sums of gb, gc for a tile
-    static constexpr size_t SMEM = 3 * RAW_X + 2 * RAW_BC + CONV + 2 * BCF + SUB + GBC;
+    // level-3 window per lane: LS steps x 4 states of h, then the same of b (b_t kept from
+    // level 3 so the reverse reads it from TMEM instead of shared memory)
+    static constexpr uint32_t TMEM_B = LS * KS;
+    static constexpr uint32_t TMEM_COLS = 2 * LS * KS;
+    static constexpr size_t SMEM = 3 * RAW_X + 2 * RAW_BC + CONV + 2 * BCF + SUB + GBC + 16;
 };
 
 __device__ __forceinline__ void red_add_v4(float* dst, float a, float b, float c, float d) {
@@ -102,7 +109,7 @@ __device__ __forceinline__ float4 operator+(const float4 a, const float4 b) {
 }
 
 template <typename TIO, bool VEC>
-__global__ void __launch_bounds__(128, 3) bwd_kernel(const BwdLaunch p) {
+__global__ void __launch_bounds__(128, 4) bwd_kernel(const BwdLaunch p) {
     using C = BwdCfg<TIO>;
     constexpr int NT = C::NT, KS = C::KS, DT = C::DT, LS = C::LS, EPC = C::EPC;
 
@@ -117,7 +124,8 @@ __global__ void __launch_bounds__(128, 3) bwd_kernel(const BwdLaunch p) {
     float* bf = reinterpret_cast<float*>(ptr);     ptr += C::BCF;      // [LS][16]
     float* cf = reinterpret_cast<float*>(ptr);     ptr += C::BCF;
     float4* sub = reinterpret_cast<float4*>(ptr);  ptr += C::SUB;      // [NSUB][NT]
-    float* gbc = reinterpret_cast<float*>(ptr);                        // [NW][LS][2][16]
+    float* gbc = reinterpret_cast<float*>(ptr);    ptr += C::GBC;      // [NW][LS][2][16]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ptr);
 
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
@@ -148,6 +156,17 @@ __global__ void __launch_bounds__(128, 3) bwd_kernel(const BwdLaunch p) {
         gcarry[s] = (valid && p.ghT != nullptr) ? p.ghT[(b * D + d) * kDS + s0 + s] : 0.f;
         gAacc[s] = 0.f;
     }
+
+    // level-3 window in tensor memory: this warp's 32 lanes x LS*4 columns
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tmem_fence_before_sync();
+    __syncthreads();
+    tmem_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+    const uint32_t tw = tmem_base + (uint32_t((warp & 3) * 32) << 16);
 
     // this thread's 16-byte chunk of a full raw tile (x, delta, dy) and of b, c
     const int xr_r = tid / C::X_CPR, xr_c = (tid % C::X_CPR) * EPC;
@@ -249,36 +268,51 @@ __global__ void __launch_bounds__(128, 3) bwd_kernel(const BwdLaunch p) {
             pend_t0 = t0;
             pend_lim = ce;
 
-            // level 3: states of this sub-chunk into registers
-            float hs[KS], hw[LS][KS];
+            // level 3: states of this sub-chunk into the TMEM window (4 columns per step)
+            float hs[KS];
             {
                 const float4 v = sub[i * NT + tid];
                 hs[0] = v.x; hs[1] = v.y; hs[2] = v.z; hs[3] = v.w;
             }
+            {
+                float hc[KS] = {hs[0], hs[1], hs[2], hs[3]};
 #pragma unroll
-            for (int r = 0; r < LS; ++r) {
-                const float2 v = *reinterpret_cast<const float2*>(conv + r * DT + c);
-                const float4 b4 = *reinterpret_cast<const float4*>(bf + r * kDS + s0);
-                const float bb[4] = {b4.x, b4.y, b4.z, b4.w};
+                for (int r = 0; r < LS; ++r) {
+                    const float2 v = *reinterpret_cast<const float2*>(conv + r * DT + c);
+                    const float4 b4 = *reinterpret_cast<const float4*>(bf + r * kDS + s0);
+                    const float bb[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
-                for (int s = 0; s < KS; ++s) {
-                    const float prev = (r == 0) ? hs[s] : hw[r - 1][s];
-                    hw[r][s] = fmaf(ex2(v.x * A2[s]), prev, v.y * bb[s]);
+                    for (int s = 0; s < KS; ++s) hc[s] = fmaf(ex2(v.x * A2[s]), hc[s], v.y * bb[s]);
+                    tmem_st4(tw + uint32_t(r * KS), hc[0], hc[1], hc[2], hc[3]);
+                    tmem_st4(tw + C::TMEM_B + uint32_t(r * KS), b4.x, b4.y, b4.z, b4.w);
                 }
+                tmem_wait_st();
             }
 
             float* gw = gbc + warp * LS * 2 * kDS;   // this warp's gb, gc sums for the tile
             // reverse sweep over the sub-chunk, 4 steps per lane reduce-scatter group
 #pragma unroll
             for (int rg = LS - 4; rg >= 0; rg -= 4) {
+                float hg[16], bgr[16], hprev[KS];   // h and b for steps rg..rg+3, h for step rg-1
+                tmem_ld16(tw + uint32_t(rg * KS), hg);
+                tmem_ld16(tw + C::TMEM_B + uint32_t(rg * KS), bgr);
+                if (rg > 0) {
+                    tmem_ld4(tw + uint32_t((rg - 1) * KS), hprev);
+                } else {
+#pragma unroll
+                    for (int s = 0; s < KS; ++s) hprev[s] = hs[s];
+                }
+                tmem_wait_ld();
                 float rr[4], qq[4];
 #pragma unroll
                 for (int jj = 3; jj >= 0; --jj) {
                     const int r = rg + jj;
-                    const float4 v = conv[r * DT + c];          // delta, delta*x, x, dy
-                    const float4 b4 = *reinterpret_cast<const float4*>(bf + r * kDS + s0);
+                    // delta, delta*x and dy of this step (x is read once per 4 steps, below)
+                    const float2 v2 = *reinterpret_cast<const float2*>(conv + r * DT + c);
+                    const float dyv = reinterpret_cast<const float*>(conv + r * DT + c)[3];
+                    const float4 v = make_float4(v2.x, v2.y, 0.f, dyv);
                     const float4 c4 = *reinterpret_cast<const float4*>(cf + r * kDS + s0);
-                    const float bb[4] = {b4.x, b4.y, b4.z, b4.w};
+                    const float bb[4] = {bgr[jj * KS], bgr[jj * KS + 1], bgr[jj * KS + 2], bgr[jj * KS + 3]};
                     const float cc[4] = {c4.x, c4.y, c4.z, c4.w};
                     float racc = 0.f, qacc = 0.f, part[8];
 #pragma unroll
@@ -286,13 +320,13 @@ __global__ void __launch_bounds__(128, 3) bwd_kernel(const BwdLaunch p) {
                         const float a = ex2(v.x * A2[s]);
                         const float g = fmaf(v.w, cc[s], gcarry[s]);
                         gcarry[s] = a * g;
-                        const float hp = (r == 0) ? hs[s] : hw[r - 1][s];
+                        const float hp = (jj == 0) ? hprev[s] : hg[(jj - 1) * KS + s];
                         const float pp = gcarry[s] * hp;
                         gAacc[s] = fmaf(pp, v.x, gAacc[s]);
                         racc = fmaf(pp, Af[s], racc);
                         qacc = fmaf(g, bb[s], qacc);
                         part[s] = g * v.y;                      // gb term of this channel
-                        part[4 + s] = v.w * hw[r][s];           // gc term of this channel
+                        part[4 + s] = v.w * hg[jj * KS + s];    // gc term of this channel
                     }
                     rr[jj] = racc;
                     qq[jj] = qacc;
@@ -303,17 +337,21 @@ __global__ void __launch_bounds__(128, 3) bwd_kernel(const BwdLaunch p) {
                 const float rs = reduce_scatter_steps<4>(rr, sg);
                 const float qs = reduce_scatter_steps<4>(qq, sg);
                 const int r = rg + sg;
-                const float4 v = conv[r * DT + c];
+                const float* vr = reinterpret_cast<const float*>(conv + r * DT + c);
+                const float dl = vr[0], xv = vr[2];
                 const int64_t t = t0 + r;
                 if (valid && t < ce) {
-                    gxg[t * D + d] = v.x * qs;
-                    gdg[t * D + d] = rs + v.z * qs;
+                    gxg[t * D + d] = dl * qs;
+                    gdg[t * D + d] = rs + xv * qs;
                 }
             }
         }
     }
+    tmem_fence_before_sync();
     __syncthreads();
+    tmem_fence_after_sync();
     if (pend_t0 >= 0) flush_gbc(pend_t0, pend_lim);
+    if (warp == 0) tmem_dealloc(tmem_base, C::TMEM_COLS);
 
     if (!valid) return;
 #pragma unroll
