@@ -74,6 +74,25 @@ EX2_PER_SM_CLK = 32     # GB300 MUFU ex2 throughput, measured on the box
 FP32_PER_SM_CLK = 128   # FP32 FMA lanes per SM
 
 
+# ---------------------------------------------------------------- multi-rank aggregation
+
+def max_over_ranks(ms, device=None):
+    """The slowest rank's time (ms); the identity on one process."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(ms)
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(elements_per_rank_step, steps, world, max_ms):
+    """Whole-job elements/s: every rank processes its own copy of the workload
+    (weak scaling), timed by the slowest rank."""
+    return world * elements_per_rank_step * steps / (max_ms / 1e3)
+
+
 # ---------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -221,12 +240,9 @@ def run_ours(args, rank, world, local_rank):
     total_ms = start.elapsed_time(end)
     fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
     bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
-    if dist:
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(total_ms, dev)
     ms_per_step = total_ms / args.steps
-    value = world * el * args.steps / (total_ms / 1e3)
+    value = job_throughput(el, args.steps, world, total_ms)
 
     # ---- end to end through the public API with host buffers
     pin = {k: (torch.from_numpy(np.ascontiguousarray(inp[k]).view(np.int16)).view(torch.bfloat16)
@@ -261,10 +277,7 @@ def run_ours(args, rank, world, local_rank):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if dist:
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(e2e_ms, dev)
 
     # ---- other large workloads (forward only), one line each
     extra = {}
