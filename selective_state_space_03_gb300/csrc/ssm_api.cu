@@ -102,6 +102,19 @@ cudaError_t run_fwd(const ssm_scan_desc& d, FwdLaunch L, int mode, cudaStream_t 
     return d.io == SSM_IO_BF16 ? launch_fwd_bf16(L, mode, st) : launch_fwd_f32(L, mode, st);
 }
 
+// Backward layout: 2 channels per lane (64 per CTA, 2 CTAs per SM) when that
+// still gives at least two full waves of CTAs; otherwise 1 (32 per CTA, 4 per
+// SM), which keeps more SMs busy on shapes with few (b, d) chains.
+int bwd_channels_per_lane(const ssm_scan_desc& d) {
+    int kd = d.B * cdiv(d.D, 64) >= int64_t(device_sm_count()) * 4 ? 2 : 1;
+    // testing aid: force the layout (1 or 2)
+    if (const char* env = std::getenv("SSM_SCAN_FORCE_BWD_KD")) {
+        const int k = std::atoi(env);
+        if (k == 1 || k == 2) kd = k;
+    }
+    return kd;
+}
+
 int64_t bwd_internal_K(const ssm_scan_desc& d) {
     return (d.ckpt_interval > 0 && d.ckpt_interval <= kMaxBwdK) ? d.ckpt_interval : kMaxBwdK;
 }
@@ -255,6 +268,7 @@ ssm_status ssm_scan_bwd(const ssm_scan_desc* desc, const void* x, const void* de
     L.B = d.B; L.T = d.T; L.D = d.D; L.K = K;
     L.io = d.io == SSM_IO_BF16 ? IO::BF16 : IO::F32;
     L.vec = vec_ok(d);
+    L.kd = bwd_channels_per_lane(d);
     const cudaError_t e = d.io == SSM_IO_BF16 ? launch_bwd_bf16(L, s) : launch_bwd_f32(L, s);
     return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }

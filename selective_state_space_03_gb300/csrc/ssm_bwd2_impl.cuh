@@ -1,0 +1,413 @@
+// Backward scan kernel, two channels per lane.
+//
+// Same gradients and the same two-level recomputation as `bwd_kernel` (page
+// "pssa_kernels.py", `scan_bwd`, with the ruDNN page's chunk-boundary
+// rematerialisation), laid out for shapes with many (b, d) chains:
+//
+//   a lane holds 4 states of 2 neighbouring channels (8 chains), a warp 16
+//   channels, a CTA of 128 threads 64 channels.
+//
+// What the second channel buys, per element: the b and c values a lane reads
+// from shared memory serve 8 chains instead of 4; the per-step sums over d of
+// gb and gc first add the lane's two channels in registers, so the 8-lane
+// reduce-scatter (shuffles and selects) is paid once per 8 elements instead of
+// once per 4; the (delta, delta*x) pair of both channels arrives in one 16-byte
+// shared load. The instruction count per element drops by about a quarter.
+//
+// Where the extra per-thread state goes: the level-2 sub-checkpoints (the
+// state entering every 16th step of the chunk, 8 floats per thread per
+// sub-chunk) are parked in this CTA's own rows of the gx output for the chunk,
+// which the reverse sweep overwrites only after it has read them back (the
+// sub-checkpoint of sub-chunk i sits in the 16 rows of sub-chunk i, one state
+// per row, one channel per column; the last sub-chunk of a chunk, which may be
+// short, keeps its start state in registers). The round trip stays in L2. The
+// level-3 window (h_t of both channels, 16 steps, 128 columns) is in tensor
+// memory and b_t comes from shared memory, so shared memory per CTA is ~35 KB
+// and three CTAs (12 warps) are resident per SM, each thread with up to 168
+// registers.
+#pragma once
+
+#include "ssm_bwd_impl.cuh"
+
+namespace ssm {
+
+template <typename TIO>
+struct Bwd2Cfg {
+    static constexpr int NT = 128;
+    static constexpr int NW = NT / 32;
+    static constexpr int G = 4;                         // lanes per channel pair
+    static constexpr int KS = kDS / G;                  // states per lane (4)
+    static constexpr int KD = 2;                        // channels per lane
+    static constexpr int NP = NT / G;                   // channel pairs per CTA (32)
+    static constexpr int DT = NP * KD;                  // channels per CTA (64)
+    static constexpr int LS = 16;                       // sub-chunk (tile) length
+    static constexpr int EPC = 16 / int(sizeof(TIO));
+    static constexpr int X_CPR = DT / EPC;              // 16-byte chunks per raw tile row
+    static constexpr int X_CH = LS * X_CPR;             // chunks per raw tile (128 bf16, 256 f32)
+    static constexpr int X_PT = X_CH / NT;              // chunks per thread
+    static constexpr int BC_CH = LS * kDS / EPC;
+    static_assert(X_CH % NT == 0, "raw tile chunks must split evenly over the CTA");
+    // shared memory (bytes)
+    static constexpr size_t RAW_X = size_t(LS) * DT * sizeof(TIO);          // one of x, delta, dy
+    static constexpr size_t RAW_BC = size_t(LS) * kDS * sizeof(TIO);        // one of b, c
+    static constexpr size_t CONV1 = size_t(LS) * NP * 16;                   // (d0, d0*x0, d1, d1*x1)
+    static constexpr size_t CONV2 = size_t(LS) * NP * 16;                   // (dy0, dy1, x0, x1)
+    static constexpr size_t BCF = size_t(LS) * kDS * 4;                     // one of b, c as float32
+    static constexpr size_t GBC = size_t(NW) * LS * 2 * kDS * 4;            // per-warp gb, gc sums of a tile
+    static constexpr size_t SMEM = 3 * RAW_X + 2 * RAW_BC + CONV1 + CONV2 + 2 * BCF + GBC + 16;
+    // tensor memory columns per lane: h of both channels per step
+    static constexpr uint32_t TMEM_H_STEP = KD * KS;                        // 8
+    static constexpr uint32_t TMEM_COLS = LS * TMEM_H_STEP;                 // 128
+    // 3 resident CTAs per SM take 384 of the 512 columns; a CTA that ever found them all
+    // taken would wait in tcgen05.alloc for a resident CTA to finish, never the reverse
+    static_assert(3 * TMEM_COLS <= 512, "three resident CTAs must fit in tensor memory");
+};
+
+
+template <typename TIO, bool VEC>
+__global__ void __launch_bounds__(128, 3) bwd2_kernel(const BwdLaunch p) {
+    using C = Bwd2Cfg<TIO>;
+    constexpr int NT = C::NT, KS = C::KS, NP = C::NP, DT = C::DT, LS = C::LS, EPC = C::EPC;
+    constexpr int HS = int(C::TMEM_H_STEP);
+
+    extern __shared__ __align__(16) unsigned char smem[];
+    unsigned char* ptr = smem;
+    TIO* xr = reinterpret_cast<TIO*>(ptr);  ptr += C::RAW_X;
+    TIO* dr = reinterpret_cast<TIO*>(ptr);  ptr += C::RAW_X;
+    TIO* yr = reinterpret_cast<TIO*>(ptr);  ptr += C::RAW_X;
+    TIO* br = reinterpret_cast<TIO*>(ptr);  ptr += C::RAW_BC;
+    TIO* cr = reinterpret_cast<TIO*>(ptr);  ptr += C::RAW_BC;
+    float4* conv1 = reinterpret_cast<float4*>(ptr); ptr += C::CONV1;   // [LS][NP]
+    float4* conv2 = reinterpret_cast<float4*>(ptr); ptr += C::CONV2;   // [LS][NP]
+    float* bf = reinterpret_cast<float*>(ptr);      ptr += C::BCF;     // [LS][16]
+    float* cf = reinterpret_cast<float*>(ptr);      ptr += C::BCF;
+    float* gbc = reinterpret_cast<float*>(ptr);     ptr += C::GBC;     // [NW][LS][2][16]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ptr);
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
+    const int cw = lane >> 2;               // channel pair within the warp
+    const int sg = lane & 3;                // state group within the pair
+    const int pc = warp * 8 + cw;           // channel pair within the CTA
+    const int s0 = sg * KS;
+    const int64_t T = p.T, D = p.D, K = p.K;
+    const int64_t b = blockIdx.y;
+    const int64_t d0 = int64_t(blockIdx.x) * DT;
+    const int64_t dch[2] = {d0 + 2 * pc, d0 + 2 * pc + 1};
+    const bool valid[2] = {dch[0] < D, dch[1] < D};
+    const bool full_d = d0 + DT <= D;
+
+    const TIO* xg = static_cast<const TIO*>(p.x) + b * T * D;
+    const TIO* dg = static_cast<const TIO*>(p.delta) + b * T * D;
+    const TIO* dyg = static_cast<const TIO*>(p.dy) + b * T * D;
+    const TIO* bg = static_cast<const TIO*>(p.b) + b * T * kDS;
+    const TIO* cgl = static_cast<const TIO*>(p.c) + b * T * kDS;
+    float* gxg = p.gx + b * T * D;
+    float* gdg = p.gdelta + b * T * D;
+
+    // per channel k and state s of this lane: A*log2(e), the carried adjoint a_{t+1} g_{t+1}, gA
+    float A2[2][KS], gcar[2][KS], gAacc[2][KS];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f), g4 = a4;
+        if (valid[k]) {
+            a4 = *reinterpret_cast<const float4*>(p.A + dch[k] * kDS + s0);
+            if (p.ghT != nullptr) g4 = *reinterpret_cast<const float4*>(p.ghT + (b * D + dch[k]) * kDS + s0);
+        }
+        const float av[4] = {a4.x, a4.y, a4.z, a4.w}, gv[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+        for (int s = 0; s < KS; ++s) {
+            A2[k][s] = av[s] * kLog2e;
+            gcar[k][s] = gv[s];
+            gAacc[k][s] = 0.f;
+        }
+    }
+
+    // level-3 window in tensor memory: this warp's 32 lanes x 128 columns
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tmem_fence_before_sync();
+    __syncthreads();
+    tmem_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+    const uint32_t tw = tmem_base + (uint32_t((warp & 3) * 32) << 16);
+
+    // this thread's 16-byte chunks of a full raw tile (x, delta, dy) and of b, c
+    int x_goff[C::X_PT], x_soff[C::X_PT];
+#pragma unroll
+    for (int q = 0; q < C::X_PT; ++q) {
+        const int i = tid + q * NT;
+        const int r = i / C::X_CPR, col = (i % C::X_CPR) * EPC;
+        x_goff[q] = r * int(D) + col;
+        x_soff[q] = r * DT + col;
+    }
+
+    auto stage = [&](int64_t t0, int64_t tend, bool rev) {
+        if (VEC && full_d && t0 + LS <= tend) {
+            const int64_t base = t0 * D + d0;
+#pragma unroll
+            for (int q = 0; q < C::X_PT; ++q) {
+                cp_async16(xr + x_soff[q], xg + base + x_goff[q], 16);
+                cp_async16(dr + x_soff[q], dg + base + x_goff[q], 16);
+                if (rev) cp_async16(yr + x_soff[q], dyg + base + x_goff[q], 16);
+            }
+            if (tid < C::BC_CH) {
+                cp_async16(br + tid * EPC, bg + t0 * kDS + tid * EPC, 16);
+                if (rev) cp_async16(cr + tid * EPC, cgl + t0 * kDS + tid * EPC, 16);
+            }
+        } else {
+            stage_tile<TIO, LS, DT, NT, VEC>(xr, xg, D, t0, tend, d0);
+            stage_tile<TIO, LS, DT, NT, VEC>(dr, dg, D, t0, tend, d0);
+            if (rev) stage_tile<TIO, LS, DT, NT, VEC>(yr, dyg, D, t0, tend, d0);
+            stage_tile<TIO, LS, kDS, NT, true>(br, bg, kDS, t0, tend, 0);
+            if (rev) stage_tile<TIO, LS, kDS, NT, true>(cr, cgl, kDS, t0, tend, 0);
+        }
+        cp_async_commit();
+    };
+    // raw tile -> (d0, d0*x0, d1, d1*x1) and (dy0, dy1, x0, x1) per (step, pair); float32 b, c rows
+    auto convert = [&](bool rev) {
+#pragma unroll
+        for (int q = 0; q < LS * NP / NT; ++q) {
+            const int i = tid + NT * q;
+            const int r = i / NP, pp = i % NP;
+            float dl[2], xv[2];
+            load_vals<TIO, 2>(dr + r * DT + 2 * pp, dl);
+            load_vals<TIO, 2>(xr + r * DT + 2 * pp, xv);
+            conv1[i] = make_float4(dl[0], dl[0] * xv[0], dl[1], dl[1] * xv[1]);
+            if (rev) {
+                float dyv[2];
+                load_vals<TIO, 2>(yr + r * DT + 2 * pp, dyv);
+                conv2[i] = make_float4(dyv[0], dyv[1], xv[0], xv[1]);
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < LS * kDS / NT; ++q) {
+            const int i = tid + NT * q;
+            bf[i] = to_f32(br[i]);
+            if (rev) cf[i] = to_f32(cr[i]);
+        }
+    };
+    // gb, gc of the tile starting at t0: sum the warps' slots, add to global (rows below t_lim)
+    auto flush_gbc = [&](int64_t t0, int64_t t_lim) {
+        const int r = tid >> 3, tau = (tid >> 2) & 1, q = tid & 3;
+        const int off = r * 2 * kDS + tau * kDS + q * 4;
+        float4 v = *reinterpret_cast<const float4*>(gbc + off);
+#pragma unroll
+        for (int w = 1; w < C::NW; ++w) v = v + *reinterpret_cast<const float4*>(gbc + w * LS * 2 * kDS + off);
+        if (t0 + r < t_lim) {
+            float* dst = (tau == 0 ? p.gb : p.gc) + (b * T + t0 + r) * kDS + q * 4;
+            red_add_v4(dst, v.x, v.y, v.z, v.w);
+        }
+    };
+
+    const int64_t nck = (T + K - 1) / K;
+    int64_t pend_t0 = -1, pend_lim = 0;       // tile whose gb/gc sums await their flush
+    for (int64_t j = nck - 1; j >= 0; --j) {
+        const int64_t cs = j * K;
+        const int64_t ce = min(T, cs + K);
+        const int nsub = int((ce - cs + LS - 1) / LS);
+
+        // ---- level 2: forward over the chunk, keeping sub-chunk start states
+        float h[2][KS];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (valid[k]) v = *reinterpret_cast<const float4*>(p.ckpt + ((j * p.B + b) * D + dch[k]) * kDS + s0);
+            h[k][0] = v.x; h[k][1] = v.y; h[k][2] = v.z; h[k][3] = v.w;
+        }
+        float hlast[2 * KS];                 // start state of the chunk's last sub-chunk
+        stage(cs, ce, false);
+        for (int i = 0; i < nsub; ++i) {
+            cp_async_wait<0>();
+            __syncthreads();
+            convert(false);
+            __syncthreads();
+            if (i + 1 < nsub) stage(cs + int64_t(i + 1) * LS, ce, false);
+            if (i + 1 < nsub) {
+                // full sub-chunk: park its start state in its own gx rows (state s0+s in row t0+s0+s)
+                float* dst = gxg + (cs + int64_t(i) * LS + s0) * D + dch[0];
+#pragma unroll
+                for (int s = 0; s < KS; ++s) {
+                    if (VEC && valid[1]) {
+                        *reinterpret_cast<float2*>(dst + s * D) = make_float2(h[0][s], h[1][s]);
+                    } else {
+                        if (valid[0]) dst[s * D] = h[0][s];
+                        if (valid[1]) dst[s * D + 1] = h[1][s];
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int s = 0; s < KS; ++s) { hlast[s] = h[0][s]; hlast[KS + s] = h[1][s]; }
+            }
+#pragma unroll 4
+            for (int r = 0; r < LS; ++r) {
+                const float4 v = conv1[r * NP + pc];                                   // d0, d0 x0, d1, d1 x1
+                const float4 b4 = *reinterpret_cast<const float4*>(bf + r * kDS + s0);
+                const float bb[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+                for (int s = 0; s < KS; ++s) {
+                    h[0][s] = fmaf(ex2(v.x * A2[0][s]), h[0][s], v.y * bb[s]);
+                    h[1][s] = fmaf(ex2(v.z * A2[1][s]), h[1][s], v.w * bb[s]);
+                }
+            }
+        }
+
+        // ---- reverse over the sub-chunks
+        stage(cs + int64_t(nsub - 1) * LS, ce, true);
+        for (int ii = 0; ii < nsub; ++ii) {
+            const int i = nsub - 1 - ii;
+            const int64_t t0 = cs + int64_t(i) * LS;
+            cp_async_wait<0>();
+            __syncthreads();
+            // start state of this sub-chunk, read back before the barrier that precedes any
+            // gx store of the sub-chunk
+            float hs[2 * KS];
+            if (ii == 0) {
+#pragma unroll
+                for (int e = 0; e < 2 * KS; ++e) hs[e] = hlast[e];
+            } else {
+                const float* src = gxg + (t0 + s0) * D + dch[0];
+#pragma unroll
+                for (int s = 0; s < KS; ++s) {
+                    if (VEC && valid[1]) {
+                        const float2 v = *reinterpret_cast<const float2*>(src + s * D);
+                        hs[s] = v.x; hs[KS + s] = v.y;
+                    } else {
+                        hs[s] = valid[0] ? src[s * D] : 0.f;
+                        hs[KS + s] = valid[1] ? src[s * D + 1] : 0.f;
+                    }
+                }
+            }
+            if (pend_t0 >= 0) flush_gbc(pend_t0, pend_lim);
+            convert(true);
+            __syncthreads();
+            if (ii + 1 < nsub) stage(t0 - LS, ce, true);
+            pend_t0 = t0;
+            pend_lim = ce;
+
+            // level 3: states of this sub-chunk into the window (8 columns per step)
+            {
+                float hc[2 * KS];
+#pragma unroll
+                for (int e = 0; e < 2 * KS; ++e) hc[e] = hs[e];
+#pragma unroll
+                for (int r = 0; r < LS; ++r) {
+                    const float4 v = conv1[r * NP + pc];
+                    const float4 b4 = *reinterpret_cast<const float4*>(bf + r * kDS + s0);
+                    const float bb[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+                    for (int s = 0; s < KS; ++s) {
+                        hc[s] = fmaf(ex2(v.x * A2[0][s]), hc[s], v.y * bb[s]);
+                        hc[KS + s] = fmaf(ex2(v.z * A2[1][s]), hc[KS + s], v.w * bb[s]);
+                    }
+                    tmem_st8(tw + uint32_t(r * HS), hc);
+                }
+                tmem_wait_st();
+            }
+
+            float* gw = gbc + warp * LS * 2 * kDS;   // this warp's gb, gc sums for the tile
+            // reverse sweep over the sub-chunk, 4 steps per lane reduce-scatter group
+#pragma unroll
+            for (int rg = LS - 4; rg >= 0; rg -= 4) {
+                float hg[4 * HS], hprev[HS];   // h for steps rg..rg+3 and for step rg-1
+                tmem_ld32(tw + uint32_t(rg * HS), hg);
+                if (rg > 0) {
+                    tmem_ld8(tw + uint32_t((rg - 1) * HS), hprev);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < HS; ++e) hprev[e] = hs[e];
+                }
+                tmem_wait_ld();
+                float rr[2][4], qq[2][4];
+#pragma unroll
+                for (int jj = 3; jj >= 0; --jj) {
+                    const int r = rg + jj;
+                    const float4 v = conv1[r * NP + pc];                                           // d0, d0 x0, d1, d1 x1
+                    const float2 dyv = *reinterpret_cast<const float2*>(conv2 + r * NP + pc);      // dy0, dy1
+                    const float4 c4 = *reinterpret_cast<const float4*>(cf + r * kDS + s0);
+                    const float4 b4 = *reinterpret_cast<const float4*>(bf + r * kDS + s0);
+                    const float cc[4] = {c4.x, c4.y, c4.z, c4.w}, bb[4] = {b4.x, b4.y, b4.z, b4.w};
+                    const float dl[2] = {v.x, v.z}, dx[2] = {v.y, v.w}, dyk[2] = {dyv.x, dyv.y};
+                    float part[8];
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        float racc = 0.f, qacc = 0.f;
+#pragma unroll
+                        for (int s = 0; s < KS; ++s) {
+                            const float a = ex2(dl[k] * A2[k][s]);
+                            const float g = fmaf(dyk[k], cc[s], gcar[k][s]);
+                            gcar[k][s] = a * g;
+                            const float hp = (jj == 0) ? hprev[k * KS + s] : hg[(jj - 1) * HS + k * KS + s];
+                            const float pp = gcar[k][s] * hp;
+                            gAacc[k][s] = fmaf(pp, dl[k], gAacc[k][s]);
+                            racc = fmaf(pp, A2[k][s], racc);      // times ln 2 below
+                            qacc = fmaf(g, bb[s], qacc);
+                            const float ht = hg[jj * HS + k * KS + s];
+                            if (k == 0) {
+                                part[s] = g * dx[0];                      // gb terms of the lane's channels
+                                part[KS + s] = dyk[0] * ht;               // gc terms
+                            } else {
+                                part[s] = fmaf(g, dx[1], part[s]);
+                                part[KS + s] = fmaf(dyk[1], ht, part[KS + s]);
+                            }
+                        }
+                        rr[k][jj] = racc;
+                        qq[k][jj] = qacc;
+                    }
+                    // sum over the warp's 8 channel pairs; this lane keeps entry (cw >> 2, cw & 3)
+                    gw[r * 2 * kDS + (cw >> 2) * kDS + s0 + (cw & 3)] = warp_reduce_scatter8(part, lane);
+                }
+                // sums over the pair's 4 lanes: this lane takes step rg + sg of both channels
+                float rs[2], qs[2];
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    rs[k] = reduce_scatter_steps<4>(rr[k], sg);
+                    qs[k] = reduce_scatter_steps<4>(qq[k], sg);
+                }
+                const int r = rg + sg;
+                const float4 v = conv1[r * NP + pc];
+                const float4 w = conv2[r * NP + pc];
+                const int64_t t = t0 + r;
+                if (t < ce) {
+                    const float gx0 = v.x * qs[0], gx1 = v.z * qs[1];
+                    constexpr float kLn2 = 0.6931471805599453f;                       // A = A2 ln 2
+                    const float gd0 = fmaf(rs[0], kLn2, w.z * qs[0]), gd1 = fmaf(rs[1], kLn2, w.w * qs[1]);
+                    if (VEC && valid[1]) {
+                        *reinterpret_cast<float2*>(gxg + t * D + dch[0]) = make_float2(gx0, gx1);
+                        *reinterpret_cast<float2*>(gdg + t * D + dch[0]) = make_float2(gd0, gd1);
+                    } else {
+                        if (valid[0]) { gxg[t * D + dch[0]] = gx0; gdg[t * D + dch[0]] = gd0; }
+                        if (valid[1]) { gxg[t * D + dch[1]] = gx1; gdg[t * D + dch[1]] = gd1; }
+                    }
+                }
+            }
+        }
+    }
+    tmem_fence_before_sync();
+    __syncthreads();
+    tmem_fence_after_sync();
+    if (pend_t0 >= 0) flush_gbc(pend_t0, pend_lim);
+    if (warp == 0) tmem_dealloc(tmem_base, C::TMEM_COLS);
+
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        if (!valid[k]) continue;
+        *reinterpret_cast<float4*>(p.gh0 + (b * D + dch[k]) * kDS + s0) =
+            make_float4(gcar[k][0], gcar[k][1], gcar[k][2], gcar[k][3]);
+        red_add_v4(p.gA + dch[k] * kDS + s0, gAacc[k][0], gAacc[k][1], gAacc[k][2], gAacc[k][3]);
+    }
+}
+
+template <typename TIO>
+cudaError_t launch_bwd2_io(const BwdLaunch& L, cudaStream_t stream) {
+    using C = Bwd2Cfg<TIO>;
+    auto kern = L.vec ? bwd2_kernel<TIO, true> : bwd2_kernel<TIO, false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::SMEM));
+    if (e != cudaSuccess) return e;
+    const dim3 grid(unsigned((L.D + C::DT - 1) / C::DT), unsigned(L.B));
+    kern<<<grid, C::NT, C::SMEM, stream>>>(L);
+    return cudaGetLastError();
+}
+}  // namespace ssm

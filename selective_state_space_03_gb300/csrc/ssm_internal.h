@@ -61,6 +61,7 @@ struct BwdLaunch {
     int64_t K;           // checkpoint interval of ckpt, 1 <= K <= kMaxBwdK
     IO io;
     bool vec;
+    int kd;              // channels per lane: 1 (32 channels per CTA) or 2 (64 per CTA)
 };
 
 constexpr int64_t kMaxBwdK = 256;   // largest checkpoint interval the backward reads directly

@@ -7,6 +7,7 @@ and check the Euler identities of the loss on the full outputs.
 Tolerances: float32 I/O 1e-4 (y, hT) and 1e-3 (gradients); bf16 I/O 1e-2;
 all as max |got - ref| / (1 + |ref|).
 """
+import contextlib
 import os
 
 import numpy as np
@@ -34,22 +35,29 @@ def ssm():
     return m
 
 
-def run_case(w, K, chunk_len=0, seed=0, ghT=False, bwd=True, lanes=None, ckpt_to_bwd=True):
+@contextlib.contextmanager
+def forced(var, value):
+    """Set a layout override of the library (read at each call) for the block."""
+    old = os.environ.get(var)
+    if value is not None:
+        os.environ[var] = str(value)
+    try:
+        yield
+    finally:
+        if value is not None:
+            if old is None:
+                del os.environ[var]
+            else:
+                os.environ[var] = old
+
+
+def run_case(w, K, chunk_len=0, seed=0, ghT=False, bwd=True, lanes=None, ckpt_to_bwd=True, bwd_kd=None):
     import torch
     inp = gen.make_inputs(w, seed=seed, with_grad_inputs=bwd, with_ghT=ghT)
     t = dev_inputs(inp)
-    env_old = os.environ.get("SSM_SCAN_FORCE_LANES")
-    if lanes is not None:
-        os.environ["SSM_SCAN_FORCE_LANES"] = str(lanes)
-    try:
+    with forced("SSM_SCAN_FORCE_LANES", lanes):
         y, hT, ckpt = ssm().ssm_scan_fwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], ckpt_interval=K,
                                          chunk_len=chunk_len)
-    finally:
-        if lanes is not None:
-            if env_old is None:
-                del os.environ["SSM_SCAN_FORCE_LANES"]
-            else:
-                os.environ["SSM_SCAN_FORCE_LANES"] = env_old
     torch.cuda.synchronize()
     ref = oracle.fwd(inp["x"], inp["delta"], inp["A"], inp["b"], inp["c"], inp["h0"], ckpt_interval=K)
     assert_close(to_host(y), ref["y"], w.io, "fwd", "y")
@@ -58,8 +66,9 @@ def run_case(w, K, chunk_len=0, seed=0, ghT=False, bwd=True, lanes=None, ckpt_to
         assert_close(to_host(ckpt), ref["ckpt"], w.io, "fwd", "ckpt")
     if not bwd:
         return
-    g = ssm().ssm_scan_bwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], ckpt if ckpt_to_bwd else None,
-                           t["dy"], t["ghT"], ckpt_interval=K)
+    with forced("SSM_SCAN_FORCE_BWD_KD", bwd_kd):
+        g = ssm().ssm_scan_bwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"],
+                               ckpt if ckpt_to_bwd else None, t["dy"], t["ghT"], ckpt_interval=K)
     torch.cuda.synchronize()
     gref = oracle.bwd(inp["x"], inp["delta"], inp["A"], inp["b"], inp["c"], inp["h0"], inp["dy"], inp.get("ghT"))
     for k in GRADS:
@@ -99,17 +108,32 @@ def test_lanes_per_chain_variants(io, lanes):
 
 
 @pytest.mark.parametrize("io", ["f32", "bf16"])
-def test_unaligned_channel_count(io):
+@pytest.mark.parametrize("bwd_kd", [1, 2])
+def test_backward_channels_per_lane(io, bwd_kd):
+    # both backward layouts on several CTAs with a partial last one (D = 200: 3 x 64 + 8)
+    run_case(gen.workload(2, B=3, T=300, D=200, io=io, h0_std=0.1), K=64, ghT=True, bwd_kd=bwd_kd)
+
+
+def test_workload2_two_channel_backward():
+    run_case(gen.workload(2), K=256, bwd_kd=2)
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("bwd_kd", [1, 2])
+def test_unaligned_channel_count(io, bwd_kd):
     # D * sizeof(io) not a multiple of 16 bytes: element-wise staging path
     D = 37 if io == "f32" else 20
-    run_case(gen.workload(2, B=2, T=77, D=D, io=io, h0_std=0.1), K=24, ghT=True)
+    run_case(gen.workload(2, B=2, T=77, D=D, io=io, h0_std=0.1), K=24, ghT=True, bwd_kd=bwd_kd)
+    if bwd_kd == 2:
+        return
     run_case(gen.workload(2, B=2, T=77, D=D, io=io, h0_std=0.1), K=24, chunk_len=20, bwd=False)
     run_case(gen.workload(2, B=2, T=77, D=D, io=io, h0_std=0.1), K=24, chunk_len=-1, lanes=2, bwd=False)
 
 
 @pytest.mark.parametrize("T,K", [(1, 1), (33, 16), (20, 64), (230, 50), (257, 256)])
-def test_ragged_lengths_and_intervals(T, K):
-    run_case(gen.workload(2, B=2, T=T, D=40, h0_std=0.1), K=K, ghT=True)
+@pytest.mark.parametrize("bwd_kd", [1, 2])
+def test_ragged_lengths_and_intervals(T, K, bwd_kd):
+    run_case(gen.workload(2, B=2, T=T, D=40, h0_std=0.1), K=K, ghT=True, bwd_kd=bwd_kd)
 
 
 @pytest.mark.parametrize("chunk_len", [32, 50, 129])
@@ -120,6 +144,7 @@ def test_chunked_ragged_chunks(chunk_len):
 def test_backward_rebuilds_checkpoints():
     # no checkpoints passed: the backward rebuilds them in its workspace
     run_case(gen.workload(2, B=2, T=300, D=40, h0_std=0.1), K=64, ghT=True, ckpt_to_bwd=False)
+    run_case(gen.workload(2, B=2, T=300, D=40, h0_std=0.1), K=64, ghT=True, ckpt_to_bwd=False, bwd_kd=2)
     # interval longer than the backward reads directly
     run_case(gen.workload(2, B=2, T=700, D=40, h0_std=0.1), K=512, ghT=True)
 
@@ -161,7 +186,8 @@ def test_empty_sizes():
         assert torch.all(g["gb"] == 0) and torch.all(g["gc"] == 0)
 
 
-def test_outputs_stay_in_bounds_and_forward_is_deterministic():
+@pytest.mark.parametrize("bwd_kd", [1, 2])
+def test_outputs_stay_in_bounds_and_forward_is_deterministic(bwd_kd):
     import torch
     m = ssm()
     w = gen.workload(2, B=2, T=70, D=36, h0_std=0.1)
@@ -189,8 +215,9 @@ def test_outputs_stay_in_bounds_and_forward_is_deterministic():
         grads[k] = inner
     shapes = {"gx": (B, T, D), "gdelta": (B, T, D), "gA": (D, 16), "gb": (B, T, 16), "gc": (B, T, 16),
               "gh0": (B, D, 16)}
-    m.ssm_scan_bwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], ck.view(3, B, D, 16), t["dy"], t["ghT"],
-                   ckpt_interval=32, grads={k: v.view(shapes[k]) for k, v in grads.items()})
+    with forced("SSM_SCAN_FORCE_BWD_KD", bwd_kd):
+        m.ssm_scan_bwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], ck.view(3, B, D, 16), t["dy"],
+                       t["ghT"], ckpt_interval=32, grads={k: v.view(shapes[k]) for k, v in grads.items()})
     torch.cuda.synchronize()
     for full in [yb, hb, cb] + bufs:
         assert torch.all(full[:pad] == canary) and torch.all(full[-pad:] == canary)
