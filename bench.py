@@ -351,6 +351,20 @@ def other_workloads(torch, ssm, dev):
             return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
         return torch.from_numpy(a).to(dev)
 
+    w2 = gen.workload(2)
+    i2 = gen.make_inputs(w2)
+    t2 = {k: dev_t(i2.get(k)) for k in ("x", "delta", "A", "b", "c", "h0", "dy")}
+    K2 = w2.ckpt_interval
+    y2, h2, ck2 = ssm.ssm_scan_fwd(t2["x"], t2["delta"], t2["A"], t2["b"], t2["c"], t2["h0"], ckpt_interval=K2)
+    ms_f = timed(lambda: ssm.ssm_scan_fwd(t2["x"], t2["delta"], t2["A"], t2["b"], t2["c"], t2["h0"],
+                                          ckpt_interval=K2, y=y2, hT=h2, ckpt=ck2))
+    g2 = ssm.ssm_scan_bwd(t2["x"], t2["delta"], t2["A"], t2["b"], t2["c"], t2["h0"], ck2, t2["dy"],
+                          ckpt_interval=K2)
+    ms_b = timed(lambda: ssm.ssm_scan_bwd(t2["x"], t2["delta"], t2["A"], t2["b"], t2["c"], t2["h0"], ck2,
+                                          t2["dy"], ckpt_interval=K2, grads=g2))
+    out[w2.name] = {"fwd_ms": ms_f, "bwd_ms": ms_b, "elem_per_s": gen.elements(w2) / ((ms_f + ms_b) / 1e3),
+                    "l2": "flushed"}
+    del t2, y2, h2, ck2, g2, i2
     w3 = gen.workload(3)
     i3 = gen.make_inputs(w3)
     t3 = {k: dev_t(i3.get(k)) for k in ("x", "delta", "A", "b", "c", "h0")}

@@ -89,9 +89,20 @@ size_t ssm_scan_ckpt_bytes(const ssm_scan_desc* desc);
 size_t ssm_scan_fwd_workspace_bytes(const ssm_scan_desc* desc);
 
 /* Bytes of device scratch memory ssm_scan_bwd needs for this desc when it is
- * called with ckpt == NULL (it then rebuilds checkpoints there); the backward
- * with checkpoints from the forward needs none. */
+ * called with ckpt == NULL: the carries below plus the checkpoints it rebuilds. */
 size_t ssm_scan_bwd_workspace_bytes(const ssm_scan_desc* desc);
+
+/* Bytes of optional scratch memory for the chunk-parallel backward, 0 when the
+ * library does not use that schedule for this desc. It is used for shapes with
+ * few (b, d) chains (one CTA per chain block would leave SMs idle) and at least
+ * two checkpoint chunks: a carry pass computes, per chunk, the adjoint a_t g_t
+ * at the chunk's start with zero adjoint entering it, plus the chunk's delta
+ * sum; each chunk then runs on its own CTAs with the adjoint entering it folded
+ * from the later chunks (the adjoint recurrence is linear, as the state
+ * recurrence is for the chunked forward). A call with the forward's checkpoints
+ * uses the schedule when workspace_bytes >= this value and sweeps each chain in
+ * one CTA otherwise; both compute the same function up to rounding. */
+size_t ssm_scan_bwd_carry_bytes(const ssm_scan_desc* desc);
 
 /* Forward scan: y, hT and (if K > 0 and ckpt != NULL) the checkpoints.
  *   h0    may be NULL (zero initial state)
@@ -113,6 +124,10 @@ ssm_status ssm_scan_fwd(const ssm_scan_desc* desc,
  *         NULL: the backward then rebuilds them from h0 in the workspace
  *   h0    may be NULL (zero initial state); used only when ckpt is NULL
  *   ghT   may be NULL (hT not differentiated, as on the pssa page)
+ *   workspace/workspace_bytes: with ckpt == NULL (or K outside 1..256) at
+ *         least ssm_scan_bwd_workspace_bytes(desc), else SSM_ERR_WORKSPACE;
+ *         with checkpoints, optional (see ssm_scan_bwd_carry_bytes); NULL or
+ *         16-byte aligned
  * gA, gb and gc are sums over many (b, d) chains accumulated with atomic adds,
  * so their last bits can differ from run to run. */
 ssm_status ssm_scan_bwd(const ssm_scan_desc* desc,

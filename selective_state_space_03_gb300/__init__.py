@@ -28,7 +28,7 @@ MAX_BWD_CKPT_INTERVAL = 256   # longest checkpoint interval ssm_scan_bwd reads w
 STATUS = {0: "SSM_OK", 1: "SSM_ERR_INVALID_ARG", 2: "SSM_ERR_UNSUPPORTED", 3: "SSM_ERR_MISALIGNED",
           4: "SSM_ERR_WORKSPACE", 5: "SSM_ERR_CUDA"}
 EXPORTS = ("ssm_scan_ckpt_bytes", "ssm_scan_fwd_workspace_bytes", "ssm_scan_bwd_workspace_bytes",
-           "ssm_scan_fwd", "ssm_scan_bwd", "ssm_status_str")
+           "ssm_scan_bwd_carry_bytes", "ssm_scan_fwd", "ssm_scan_bwd", "ssm_status_str")
 
 
 class ssm_scan_desc(ctypes.Structure):
@@ -57,7 +57,8 @@ def lib() -> ctypes.CDLL:
                                    f"g.build()\"` (needs nvcc); there is no CPU fallback")
             L = ctypes.CDLL(LIB_PATH)
             vp, sz, dp = ctypes.c_void_p, ctypes.c_size_t, ctypes.POINTER(ssm_scan_desc)
-            for name in ("ssm_scan_ckpt_bytes", "ssm_scan_fwd_workspace_bytes", "ssm_scan_bwd_workspace_bytes"):
+            for name in ("ssm_scan_ckpt_bytes", "ssm_scan_fwd_workspace_bytes", "ssm_scan_bwd_workspace_bytes",
+                         "ssm_scan_bwd_carry_bytes"):
                 getattr(L, name).argtypes = [dp]
                 getattr(L, name).restype = sz
             L.ssm_scan_fwd.argtypes = [dp] + [vp] * 9 + [vp, sz, vp]
@@ -177,7 +178,8 @@ def ssm_scan_bwd(x, delta, A, b, c, h0, ckpt, dy, ghT=None, *, ckpt_interval=0, 
     # the library rebuilds checkpoints in the workspace when none are given or
     # when they are further apart than the backward reads directly
     rebuild = ckpt is None or not (0 < ckpt_interval <= MAX_BWD_CKPT_INTERVAL)
-    need = L.ssm_scan_bwd_workspace_bytes(ctypes.byref(desc)) if rebuild else 0
+    # (with checkpoints, the workspace only holds the optional chunk-parallel carries)
+    need = (L.ssm_scan_bwd_workspace_bytes if rebuild else L.ssm_scan_bwd_carry_bytes)(ctypes.byref(desc))
     if workspace is None:
         workspace, wsb = _workspace(need, dev)
     else:

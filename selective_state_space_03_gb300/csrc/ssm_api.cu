@@ -12,6 +12,8 @@ cudaError_t launch_fwd_f32(const FwdLaunch& L, int mode, cudaStream_t stream);
 cudaError_t launch_fwd_bf16(const FwdLaunch& L, int mode, cudaStream_t stream);
 cudaError_t launch_bwd_f32(const BwdLaunch& L, cudaStream_t stream);
 cudaError_t launch_bwd_bf16(const BwdLaunch& L, cudaStream_t stream);
+cudaError_t launch_bwd_carry_f32(const BwdLaunch& L, cudaStream_t stream);
+cudaError_t launch_bwd_carry_bf16(const BwdLaunch& L, cudaStream_t stream);
 
 int device_sm_count() {
     static int cache[64] = {0};
@@ -119,6 +121,31 @@ int64_t bwd_internal_K(const ssm_scan_desc& d) {
     return (d.ckpt_interval > 0 && d.ckpt_interval <= kMaxBwdK) ? d.ckpt_interval : kMaxBwdK;
 }
 
+// Chunk-parallel backward: when one CTA per (channel block, batch) would not fill one
+// wave of the GPU (4 CTAs per SM of the one-channel layout) and there are at least two
+// checkpoint chunks, each chunk gets its own CTA (a carry pass first supplies the adjoint
+// entering it). Needs the carries in the workspace.
+bool bwd_chunk_parallel(const ssm_scan_desc& d) {
+    const int64_t nck = cdiv(d.T, bwd_internal_K(d));
+    if (nck < 2 || nck > 65535) return false;
+    bool on = bwd_channels_per_lane(d) == 1 && d.B * cdiv(d.D, 32) < int64_t(device_sm_count()) * 4;
+    // testing aid: force the schedule on (1) or off (0)
+    if (const char* env = std::getenv("SSM_SCAN_FORCE_BWD_TPAR")) {
+        const int k = std::atoi(env);
+        if (k == 0 || k == 1) on = k == 1;
+    }
+    return on;
+}
+
+// Workspace of the chunk-parallel backward: carry_Z [nck][B][D][16], then carry_S [nck][B][D].
+size_t bwd_carry_Z_bytes(const ssm_scan_desc& d) {
+    return align_up(size_t(cdiv(d.T, bwd_internal_K(d))) * size_t(d.B) * size_t(d.D) * kDS * 4);
+}
+size_t bwd_carry_bytes(const ssm_scan_desc& d) {
+    if (!bwd_chunk_parallel(d)) return 0;
+    return bwd_carry_Z_bytes(d) + align_up(size_t(cdiv(d.T, bwd_internal_K(d))) * size_t(d.B) * size_t(d.D) * 4);
+}
+
 }  // namespace
 }  // namespace ssm
 
@@ -149,9 +176,15 @@ size_t ssm_scan_fwd_workspace_bytes(const ssm_scan_desc* d) {
     return P.mode == 2 ? P.ws_S + P.ws_Sd : 0;
 }
 
+size_t ssm_scan_bwd_carry_bytes(const ssm_scan_desc* d) {
+    if (check_desc(d) != SSM_OK || d->B == 0 || d->T == 0 || d->D == 0) return 0;
+    return bwd_carry_bytes(*d);
+}
+
 size_t ssm_scan_bwd_workspace_bytes(const ssm_scan_desc* d) {
     if (check_desc(d) != SSM_OK || d->B == 0 || d->T == 0 || d->D == 0) return 0;
-    return align_up(size_t(cdiv(d->T, bwd_internal_K(*d))) * size_t(d->B) * size_t(d->D) * kDS * 4);
+    return bwd_carry_bytes(*d) +
+           align_up(size_t(cdiv(d->T, bwd_internal_K(*d))) * size_t(d->B) * size_t(d->D) * kDS * 4);
 }
 
 ssm_status ssm_scan_fwd(const ssm_scan_desc* desc, const void* x, const void* delta, const float* A,
@@ -236,25 +269,31 @@ ssm_status ssm_scan_bwd(const ssm_scan_desc* desc, const void* x, const void* de
         return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
     }
 
+    // workspace: [carries of the chunk-parallel schedule][rebuilt checkpoints]
+    const size_t carry_bytes = bwd_carry_bytes(d);
+    if (workspace != nullptr && !aligned16(workspace)) return SSM_ERR_MISALIGNED;
     // checkpoints: the forward's, or rebuilt in the workspace
     const float* ck = ckpt;
     int64_t K = d.ckpt_interval;
     const bool rebuild = (ckpt == nullptr) || K <= 0 || K > kMaxBwdK;
+    // with the forward's checkpoints the carries are optional: without room for them the
+    // backward sweeps every chunk in one CTA
+    const bool tpar = carry_bytes > 0 && workspace != nullptr && workspace_bytes >= carry_bytes;
     if (rebuild) {
         K = bwd_internal_K(d);
         const size_t need = ssm_scan_bwd_workspace_bytes(desc);
         if (workspace == nullptr || workspace_bytes < need) return SSM_ERR_WORKSPACE;
-        if (!aligned16(workspace)) return SSM_ERR_MISALIGNED;
         FwdLaunch L{};
         L.x = x; L.delta = delta; L.A = A; L.b = b; L.c = c; L.h0 = h0;
-        L.y = nullptr; L.hT = nullptr; L.ckpt = static_cast<float*>(workspace);
+        L.y = nullptr; L.hT = nullptr;
+        L.ckpt = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + carry_bytes);
         L.B = d.B; L.T = d.T; L.D = d.D; L.K = K; L.Lc = d.T; L.nchunk = 1;
         L.io = d.io == SSM_IO_BF16 ? IO::BF16 : IO::F32;
         L.vec = vec_ok(d);
         L.G = 4;
         L.ckpt_only = true;
         if (run_fwd(d, L, 3, s) != cudaSuccess) return SSM_ERR_CUDA;
-        ck = static_cast<const float*>(workspace);
+        ck = L.ckpt;
     }
 
     if (cudaMemsetAsync(gA, 0, size_t(d.D) * kDS * 4, s) != cudaSuccess) return SSM_ERR_CUDA;
@@ -269,6 +308,14 @@ ssm_status ssm_scan_bwd(const ssm_scan_desc* desc, const void* x, const void* de
     L.io = d.io == SSM_IO_BF16 ? IO::BF16 : IO::F32;
     L.vec = vec_ok(d);
     L.kd = bwd_channels_per_lane(d);
+    L.tpar = tpar;
+    if (tpar) {
+        L.kd = 1;
+        L.carry_Z = static_cast<float*>(workspace);
+        L.carry_S = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + bwd_carry_Z_bytes(d));
+        const cudaError_t e1 = d.io == SSM_IO_BF16 ? launch_bwd_carry_bf16(L, s) : launch_bwd_carry_f32(L, s);
+        if (e1 != cudaSuccess) return SSM_ERR_CUDA;
+    }
     const cudaError_t e = d.io == SSM_IO_BF16 ? launch_bwd_bf16(L, s) : launch_bwd_f32(L, s);
     return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }

@@ -309,7 +309,7 @@ __global__ void __launch_bounds__(128, 3) bwd2_kernel(const BwdLaunch p) {
 
             float* gw = gbc + warp * LS * 2 * kDS;   // this warp's gb, gc sums for the tile
             // reverse sweep over the sub-chunk, 4 steps per lane reduce-scatter group
-#pragma unroll
+#pragma unroll 2
             for (int rg = LS - 4; rg >= 0; rg -= 4) {
                 float hg[4 * HS], hprev[HS];   // h for steps rg..rg+3 and for step rg-1
                 tmem_ld32(tw + uint32_t(rg * HS), hg);

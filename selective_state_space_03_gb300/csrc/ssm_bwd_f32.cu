@@ -5,4 +5,7 @@ namespace ssm {
 cudaError_t launch_bwd_f32(const BwdLaunch& L, cudaStream_t stream) {
     return L.kd == 2 ? launch_bwd2_io<float>(L, stream) : launch_bwd_io<float>(L, stream);
 }
+cudaError_t launch_bwd_carry_f32(const BwdLaunch& L, cudaStream_t stream) {
+    return launch_bwd_carry_io<float>(L, stream);
+}
 }  // namespace ssm

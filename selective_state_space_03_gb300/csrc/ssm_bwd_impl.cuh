@@ -222,8 +222,24 @@ __global__ void __launch_bounds__(128, 4) bwd_kernel(const BwdLaunch p) {
     };
 
     const int64_t nck = (T + K - 1) / K;
+    // chunks this CTA sweeps: all of them, or (chunk-parallel schedule) chunk blockIdx.z with
+    // the adjoint entering it folded from the later chunks' carries
+    int64_t jhi = nck - 1, jlo = 0;
+    if (p.tpar) {
+        jhi = jlo = blockIdx.z;
+        if (valid) {
+            for (int64_t jj = nck - 1; jj > jlo; --jj) {
+                const float4 z = *reinterpret_cast<const float4*>(p.carry_Z + ((jj * p.B + b) * D + d) * kDS + s0);
+                const float sd = p.carry_S[(jj * p.B + b) * D + d];
+                gcarry[0] = fmaf(ex2(A2[0] * sd), gcarry[0], z.x);
+                gcarry[1] = fmaf(ex2(A2[1] * sd), gcarry[1], z.y);
+                gcarry[2] = fmaf(ex2(A2[2] * sd), gcarry[2], z.z);
+                gcarry[3] = fmaf(ex2(A2[3] * sd), gcarry[3], z.w);
+            }
+        }
+    }
     int64_t pend_t0 = -1, pend_lim = 0;       // tile whose gb/gc sums await their flush
-    for (int64_t j = nck - 1; j >= 0; --j) {
+    for (int64_t j = jhi; j >= jlo; --j) {
         const int64_t cs = j * K;
         const int64_t ce = min(T, cs + K);
         const int nsub = int((ce - cs + LS - 1) / LS);
@@ -356,9 +372,91 @@ __global__ void __launch_bounds__(128, 4) bwd_kernel(const BwdLaunch p) {
     if (!valid) return;
 #pragma unroll
     for (int s = 0; s < KS; ++s) {
-        p.gh0[(b * D + d) * kDS + s0 + s] = gcarry[s];
+        if (jlo == 0) p.gh0[(b * D + d) * kDS + s0 + s] = gcarry[s];
         atomicAdd(&p.gA[d * kDS + s0 + s], gAacc[s]);
     }
+}
+
+// Chunk-parallel backward, pass 1. The adjoint is linear in what enters a chunk from
+// its end: with G_in the carried adjoint a_{ce} g_{ce} entering chunk [cs, ce),
+//   a_{cs} g_{cs} = Z + exp(A * sum_{t in chunk} delta_t) * G_in,
+// where Z is a_{cs} g_{cs} of the same chunk with zero adjoint entering it (the
+// forward's chunked scan splits the state recurrence the same way). This kernel
+// computes Z and the delta sum of chunks 1..nck-1 (chunk 0 passes its adjoint only
+// to gh0, which pass 2 computes); pass 2 folds them into each chunk's G_in.
+// Layout as bwd_kernel: 32 channels x 4 lanes of 4 states per CTA, one CTA per
+// (channel block, batch, chunk).
+template <typename TIO, bool VEC>
+__global__ void __launch_bounds__(128) bwd_carry_kernel(const BwdLaunch p) {
+    constexpr int NT = 128, KS = 4, DT = 32, LS = 16;
+    __shared__ __align__(16) TIO dr[2][LS * DT], yr[2][LS * DT], cr[2][LS * kDS];
+
+    const int tid = threadIdx.x;
+    const int c = tid >> 2, sg = tid & 3, s0 = sg * KS;
+    const int64_t T = p.T, D = p.D, K = p.K;
+    const int64_t b = blockIdx.y;
+    const int64_t j = int64_t(blockIdx.z) + 1;
+    const int64_t d0 = int64_t(blockIdx.x) * DT;
+    const int64_t d = d0 + c;
+    const bool valid = d < D;
+    const int64_t cs = j * K, ce = min(T, cs + K);
+    const int ntile = int((ce - cs + LS - 1) / LS);
+
+    const TIO* dg = static_cast<const TIO*>(p.delta) + b * T * D;
+    const TIO* dyg = static_cast<const TIO*>(p.dy) + b * T * D;
+    const TIO* cgl = static_cast<const TIO*>(p.c) + b * T * kDS;
+
+    float A2[KS], gcar[KS];
+#pragma unroll
+    for (int s = 0; s < KS; ++s) {
+        A2[s] = valid ? p.A[d * kDS + s0 + s] * kLog2e : 0.f;
+        gcar[s] = 0.f;
+    }
+    float dsum = 0.f;
+
+    auto stage = [&](int buf, int64_t t0) {
+        stage_tile<TIO, LS, DT, NT, VEC>(dr[buf], dg, D, t0, ce, d0);
+        stage_tile<TIO, LS, DT, NT, VEC>(yr[buf], dyg, D, t0, ce, d0);
+        stage_tile<TIO, LS, kDS, NT, true>(cr[buf], cgl, kDS, t0, ce, 0);
+        cp_async_commit();
+    };
+    stage(0, cs + int64_t(ntile - 1) * LS);
+    for (int ii = 0; ii < ntile; ++ii) {
+        const int buf = ii & 1;
+        if (ii + 1 < ntile) {
+            stage(buf ^ 1, cs + int64_t(ntile - 2 - ii) * LS);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncthreads();
+#pragma unroll 4
+        for (int r = LS - 1; r >= 0; --r) {      // rows past ce are zero: a = 1, g unchanged
+            const float dl = to_f32(dr[buf][r * DT + c]), dy = to_f32(yr[buf][r * DT + c]);
+            float cc[KS];
+            load_vals<TIO, KS>(cr[buf] + r * kDS + s0, cc);
+#pragma unroll
+            for (int s = 0; s < KS; ++s) {
+                const float g = fmaf(dy, cc[s], gcar[s]);
+                gcar[s] = ex2(dl * A2[s]) * g;
+            }
+            dsum += dl;
+        }
+        __syncthreads();
+    }
+    if (!valid) return;
+    *reinterpret_cast<float4*>(p.carry_Z + ((j * p.B + b) * D + d) * kDS + s0) =
+        make_float4(gcar[0], gcar[1], gcar[2], gcar[3]);
+    if (sg == 0) p.carry_S[(j * p.B + b) * D + d] = dsum;
+}
+
+template <typename TIO>
+cudaError_t launch_bwd_carry_io(const BwdLaunch& L, cudaStream_t stream) {
+    auto kern = L.vec ? bwd_carry_kernel<TIO, true> : bwd_carry_kernel<TIO, false>;
+    const int64_t nck = (L.T + L.K - 1) / L.K;
+    const dim3 grid(unsigned((L.D + 31) / 32), unsigned(L.B), unsigned(nck - 1));
+    kern<<<grid, 128, 0, stream>>>(L);
+    return cudaGetLastError();
 }
 
 template <typename TIO>
@@ -367,7 +465,8 @@ cudaError_t launch_bwd_io(const BwdLaunch& L, cudaStream_t stream) {
     auto kern = L.vec ? bwd_kernel<TIO, true> : bwd_kernel<TIO, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::SMEM));
     if (e != cudaSuccess) return e;
-    const dim3 grid(unsigned((L.D + C::DT - 1) / C::DT), unsigned(L.B));
+    const unsigned nz = L.tpar ? unsigned((L.T + L.K - 1) / L.K) : 1u;
+    const dim3 grid(unsigned((L.D + C::DT - 1) / C::DT), unsigned(L.B), nz);
     kern<<<grid, C::NT, C::SMEM, stream>>>(L);
     return cudaGetLastError();
 }

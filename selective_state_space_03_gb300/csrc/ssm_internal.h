@@ -62,11 +62,18 @@ struct BwdLaunch {
     IO io;
     bool vec;
     int kd;              // channels per lane: 1 (32 channels per CTA) or 2 (64 per CTA)
+    // chunk-parallel schedule (kd == 1 only): one CTA per (channel block, batch, chunk); the
+    // adjoint entering each chunk comes from the carries of all later chunks
+    bool tpar;
+    float* carry_Z;      // [nck][B][D][16]: a_{cs} g_{cs} of chunk j with zero adjoint entering it
+    float* carry_S;      // [nck][B][D]: sum of delta over chunk j
 };
 
 constexpr int64_t kMaxBwdK = 256;   // largest checkpoint interval the backward reads directly
 
 cudaError_t launch_bwd(const BwdLaunch& L, cudaStream_t stream);
+cudaError_t launch_bwd_carry_f32(const BwdLaunch& L, cudaStream_t stream);
+cudaError_t launch_bwd_carry_bf16(const BwdLaunch& L, cudaStream_t stream);
 
 int device_sm_count();
 

@@ -51,7 +51,8 @@ def forced(var, value):
                 os.environ[var] = old
 
 
-def run_case(w, K, chunk_len=0, seed=0, ghT=False, bwd=True, lanes=None, ckpt_to_bwd=True, bwd_kd=None):
+def run_case(w, K, chunk_len=0, seed=0, ghT=False, bwd=True, lanes=None, ckpt_to_bwd=True, bwd_kd=None,
+             bwd_tpar=None, bwd_workspace=None):
     import torch
     inp = gen.make_inputs(w, seed=seed, with_grad_inputs=bwd, with_ghT=ghT)
     t = dev_inputs(inp)
@@ -66,9 +67,10 @@ def run_case(w, K, chunk_len=0, seed=0, ghT=False, bwd=True, lanes=None, ckpt_to
         assert_close(to_host(ckpt), ref["ckpt"], w.io, "fwd", "ckpt")
     if not bwd:
         return
-    with forced("SSM_SCAN_FORCE_BWD_KD", bwd_kd):
+    with forced("SSM_SCAN_FORCE_BWD_KD", bwd_kd), forced("SSM_SCAN_FORCE_BWD_TPAR", bwd_tpar):
         g = ssm().ssm_scan_bwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"],
-                               ckpt if ckpt_to_bwd else None, t["dy"], t["ghT"], ckpt_interval=K)
+                               ckpt if ckpt_to_bwd else None, t["dy"], t["ghT"], ckpt_interval=K,
+                               workspace=bwd_workspace)
     torch.cuda.synchronize()
     gref = oracle.bwd(inp["x"], inp["delta"], inp["A"], inp["b"], inp["c"], inp["h0"], inp["dy"], inp.get("ghT"))
     for k in GRADS:
@@ -116,6 +118,26 @@ def test_backward_channels_per_lane(io, bwd_kd):
 
 def test_workload2_two_channel_backward():
     run_case(gen.workload(2), K=256, bwd_kd=2)
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("T,K", [(230, 50), (512, 256), (33, 16)])
+def test_chunk_parallel_backward(io, T, K):
+    # one CTA per (channel block, batch, chunk), adjoint entering each chunk from the carries
+    run_case(gen.workload(2, B=2, T=T, D=40, io=io, h0_std=0.1), K=K, ghT=True, bwd_tpar=1)
+
+
+def test_chunk_parallel_backward_rebuild_and_fallback():
+    import torch
+    w = gen.workload(2, B=3, T=300, D=72, h0_std=0.1)
+    # checkpoints rebuilt in the workspace behind the carries
+    run_case(w, K=64, ghT=True, ckpt_to_bwd=False, bwd_tpar=1)
+    # no room for the carries: the same call sweeps each chain in one CTA
+    run_case(w, K=64, ghT=True, bwd_tpar=1, bwd_workspace=torch.empty(0, dtype=torch.uint8, device="cuda:0"))
+
+
+def test_workload2_sequential_backward():
+    run_case(gen.workload(2), K=256, bwd_tpar=0)
 
 
 @pytest.mark.parametrize("io", ["f32", "bf16"])
