@@ -201,7 +201,8 @@ def run_ours(args, rank, world, local_rank):
     desc = ssm.make_desc(w.B, w.T, w.D, w.DS, ssm.SSM_IO_BF16, K, 0)
     import ctypes
     fwd_kernels = 2 if ssm.lib().ssm_scan_fwd_workspace_bytes(ctypes.byref(desc)) else 1
-    kernels_per_step = fwd_kernels + 1
+    bwd_kernels = 2 if ssm.lib().ssm_scan_bwd_carry_bytes(ctypes.byref(desc)) else 1
+    kernels_per_step = fwd_kernels + bwd_kernels
 
     def fwd():
         ssm.ssm_scan_fwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], ckpt_interval=K, y=y, hT=hT,
@@ -244,7 +245,10 @@ def run_ours(args, rank, world, local_rank):
     ms_per_step = total_ms / args.steps
     value = job_throughput(el, args.steps, world, total_ms)
 
-    # ---- end to end through the public API with host buffers
+    # ---- end to end through the public API with host buffers. Every step copies its inputs
+    # from pinned host memory and all its outputs (y, hT and the six gradients) back; the steps
+    # are pipelined over three streams (copy in, compute, copy out) with two device buffer sets,
+    # so step i's compute overlaps step i+1's upload and step i-1's download.
     pin = {k: (torch.from_numpy(np.ascontiguousarray(inp[k]).view(np.int16)).view(torch.bfloat16)
                if inp[k].dtype == np.uint16 else torch.from_numpy(np.ascontiguousarray(inp[k]))).pin_memory()
            for k in ("x", "delta", "A", "b", "c", "dy")}
@@ -254,30 +258,67 @@ def run_ours(args, rank, world, local_rank):
         outs_h[k] = torch.empty(v.shape, dtype=v.dtype).pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in pin.values())
     d2h = sum(v.numel() * v.element_size() for v in outs_h.values())
-    dev_out = {"y": y, "hT": hT, **grads}
-    e2e_steps = max(2, min(args.steps, 5))
+    sets = []
+    for _ in range(2):
+        tin = {k: torch.empty_like(t[k]) for k in pin}
+        tin["h0"] = t["h0"]
+        sets.append({"in": tin, "y": torch.empty_like(y), "hT": torch.empty_like(hT), "ckpt": torch.empty_like(ckpt),
+                     "g": {k: torch.empty_like(v) for k, v in grads.items()}})
+    s_in, s_comp = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    s_outs = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]   # downloads split over two streams
+    out_keys = [["y", "gx", "gA", "gh0"], ["gdelta", "gb", "gc", "hT"]]
+    assert sorted(sum(out_keys, [])) == sorted(outs_h)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_comp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [[torch.cuda.Event() for _ in range(2)] for _ in range(2)]
+    e2e_steps = max(4, min(args.steps, 10))
 
-    def e2e_step():
-        for k, v in pin.items():
-            t[k].copy_(v, non_blocking=True)
-        fwd()
-        bwd()
-        for k, v in outs_h.items():
-            v.copy_(dev_out[k], non_blocking=True)
+    def e2e_run(n):
+        for i in range(n):
+            q = i % 2
+            S = sets[q]
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(ev_comp[q])          # set q's inputs free again
+                for k, v in pin.items():
+                    S["in"][k].copy_(v, non_blocking=True)
+                ev_in[q].record(s_in)
+            with torch.cuda.stream(s_comp):
+                s_comp.wait_event(ev_in[q])
+                if i >= 2:
+                    for o in range(2):
+                        s_comp.wait_event(ev_out[o][q])  # set q's outputs downloaded
+                ti = S["in"]
+                ssm.ssm_scan_fwd(ti["x"], ti["delta"], ti["A"], ti["b"], ti["c"], ti["h0"], ckpt_interval=K,
+                                 y=S["y"], hT=S["hT"], ckpt=S["ckpt"])
+                ssm.ssm_scan_bwd(ti["x"], ti["delta"], ti["A"], ti["b"], ti["c"], ti["h0"], S["ckpt"], ti["dy"],
+                                 ckpt_interval=K, grads=S["g"])
+                ev_comp[q].record(s_comp)
+            dev_outs = {"y": S["y"], "hT": S["hT"], **S["g"]}
+            for o, so in enumerate(s_outs):
+                with torch.cuda.stream(so):
+                    so.wait_event(ev_comp[q])
+                    for k in out_keys[o]:
+                        outs_h[k].copy_(dev_outs[k], non_blocking=True)
+                    ev_out[o][q].record(so)
 
-    e2e_step()
+    e2e_run(2)
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
+    e0.record(s_in)
+    e2e_run(e2e_steps)
+    s_last = s_outs[0]
+    for st in (s_in, s_comp, s_outs[1]):
+        s_last.wait_stream(st)
+    e1.record(s_last)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     e2e_ms = max_over_ranks(e2e_ms, dev)
+    # the last step's outputs are on the host: check one of them against the device copy
+    assert torch.equal(outs_h["hT"], sets[(e2e_steps - 1) % 2]["hT"].cpu())
 
     # ---- other large workloads (forward only), one line each
     extra = {}
@@ -314,7 +355,8 @@ def run_ours(args, rank, world, local_rank):
                      "hbm": {"achieved": bwd_bytes / (bwd_ms / 1e3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
                              "frac": bwd_bytes / (bwd_ms / 1e3) / 1e9 / hbm_peak, "peak_kind": peak_kind}},
         "e2e": {"value": el / (e2e_ms / 1e3) * world, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": e2e_steps,
+                "schedule": "copy-in, compute and two copy-out streams; two device buffer sets"},
         "gpu_launches": kernels_per_step * args.steps,
         "clocks": clk,
         "other_workloads": extra,
@@ -390,6 +432,57 @@ def other_workloads(torch, ssm, dev):
     ms = timed(f4, reps=3)
     out[w4.name] = {"fwd_ms": ms, "elem_per_s": gen.elements(w4) / (ms / 1e3), "calls": w4.T // L,
                     "l2": "flushed before the 16 calls"}
+    # single-step decode at workload 5's width: one step per call, state in place; L2 flushed
+    # before every step (the 5 MB state would otherwise stay in L2)
+    wd = gen.workload(5, T=1)
+    idd = gen.make_inputs(wd, with_grad_inputs=False)
+    td = {k: dev_t(idd.get(k)) for k in ("x", "delta", "A", "b", "c")}
+    xs, ds, bs, cs = (td[k][:, 0].contiguous() for k in ("x", "delta", "b", "c"))
+    hd = torch.zeros((wd.B, wd.D, 16), dtype=torch.float32, device=dev)
+    yd = torch.empty_like(xs)
+    ssm.ssm_scan_step(xs, ds, td["A"], bs, cs, hd, y=yd)
+    ts = []
+    for _ in range(50):
+        flush.zero_()
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        ssm.ssm_scan_step(xs, ds, td["A"], bs, cs, hd, y=yd)
+        b_.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b_))
+    us_cold = statistics.median(ts) * 1e3
+    nbytes = 2 * wd.B * wd.D * 16 * 4 + 3 * wd.B * wd.D * 2 + 2 * wd.B * 16 * 2 + wd.D * 16 * 4
+    # steady state: 32 sessions' states (168 MB, more than L2) stepped round-robin, 64 steps
+    # captured in one CUDA graph so host launch overhead is not timed
+    nsess, nstep = 32, 64
+    hss = [torch.zeros_like(hd) for _ in range(nsess)]
+    sg = torch.cuda.Stream(dev)
+    sg.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(sg):
+        for k in range(nsess):
+            ssm.ssm_scan_step(xs, ds, td["A"], bs, cs, hss[k], y=yd)
+    torch.cuda.current_stream().wait_stream(sg)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=sg):
+        for k in range(nstep):
+            ssm.ssm_scan_step(xs, ds, td["A"], bs, cs, hss[k % nsess], y=yd)
+    graph.replay()
+    torch.cuda.synchronize()
+    reps = 10
+    a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        graph.replay()
+    b_.record()
+    torch.cuda.synchronize()
+    us = a.elapsed_time(b_) * 1e3 / (reps * nstep)
+    out["decode_step_bf16_B16_D5120"] = {
+        "us_per_step": us, "elem_per_s": wd.B * wd.D * 16 / (us / 1e6), "hbm_gbs": nbytes / (us / 1e6) / 1e9,
+        "hbm_frac": nbytes / (us / 1e6) / 1e9 / load_peaks()[0], "bytes_per_step": nbytes,
+        "schedule": f"{nstep} steps over {nsess} sessions' states in one CUDA graph (states exceed L2)",
+        "us_single_step_after_l2_flush": us_cold}
+    del hss
     return out
 
 
@@ -431,12 +524,12 @@ def run_reference(args, rank, world):
 
 
 def run_profile_case(args):
-    """One warm-up and one more forward+backward of workload 5 (optionally with B/T
-    replaced), for profilers; prints nothing but 'ok'."""
+    """One warm-up and one more forward(+backward) of workload 5, or of the workload
+    --workload names (optionally with B/T replaced), for profilers; prints nothing but 'ok'."""
     import torch
     import selective_state_space_03_gb300 as ssm
     over = {k: v for k, v in (("B", args.B), ("T", args.T)) if v}
-    w = gen.workload(WORKLOAD, **over)
+    w = gen.workload(args.workload or WORKLOAD, **over)
     inp = gen.make_inputs(w, seed=0)
     dev = torch.device("cuda", 0)
 
@@ -452,7 +545,8 @@ def run_profile_case(args):
     K = w.ckpt_interval
     for _ in range(2):
         _, _, ck = ssm.ssm_scan_fwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], ckpt_interval=K)
-        ssm.ssm_scan_bwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], ck, t["dy"], ckpt_interval=K)
+        if w.bwd:
+            ssm.ssm_scan_bwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], ck, t["dy"], ckpt_interval=K)
     torch.cuda.synchronize()
     print("ok")
 
@@ -467,6 +561,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle timing")
     ap.add_argument("--profile", action="store_true",
                     help="run one warm-up and one forward+backward for a profiler, no timing")
+    ap.add_argument("--workload", type=int, default=0, help="with --profile: workload 1-5 instead of 5")
     ap.add_argument("--B", type=int, default=0, help="with --profile: batch size instead of 16")
     ap.add_argument("--T", type=int, default=0, help="with --profile: sequence length instead of 2048")
     args = ap.parse_args()

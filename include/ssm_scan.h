@@ -165,6 +165,22 @@ ssm_status ssm_scan_fwd_noalloc(const ssm_scan_desc* desc,
                                 const void* b, const void* c, const float* h0,
                                 void* y, float* hT, float* ckpt, void* stream);
 
+/* One step of the scan for every (b, d) chain, the state updated in place:
+ * the decode form of the recurrence (one token per call, the state carried
+ * between calls, as the ruDNN page's fused recurrent decode does for KDA).
+ *     h[b,d,s] <- exp(delta[b,d] A[d,s]) h[b,d,s] + delta[b,d] b[b,s] x[b,d]
+ *     y[b,d]   <- sum_s h[b,d,s] c[b,s]
+ * i.e. ssm_scan_fwd with T = 1 and hT written over h0. desc->T must be 1;
+ * ckpt_interval and chunk_len are ignored.
+ *   x, delta, y   (B, D)      io dtype
+ *   b, c          (B, DS)     io dtype
+ *   A             (D, DS)     float32
+ *   h             (B, D, DS)  float32, read and overwritten (not NULL)
+ * No workspace; B == 0 or D == 0 launches nothing. Errors as ssm_scan_fwd. */
+ssm_status ssm_scan_step(const ssm_scan_desc* desc,
+                         const void* x, const void* delta, const float* A,
+                         const void* b, const void* c, float* h, void* y, void* stream);
+
 /* Static description of a status code. */
 const char* ssm_status_str(ssm_status status);
 

@@ -225,6 +225,31 @@ def ssm_scan_fwd_noalloc(x, delta, A, b, c, h0=None, *, ckpt_interval=0, chunk_l
     return y, hT, ckpt
 
 
+def ssm_scan_step(x, delta, A, b, c, h, *, y=None, stream=None):
+    """One decode step through ssm_scan_step: x, delta (B, D), b, c (B, DS) in the I/O
+    dtype, A (D, DS) and the state h (B, D, DS) float32, which is updated in place.
+    Returns y (B, D)."""
+    torch = _torch()
+    L = lib()
+    fn = L.ssm_scan_step
+    fn.argtypes = [ctypes.POINTER(ssm_scan_desc)] + [ctypes.c_void_p] * 8
+    fn.restype = ctypes.c_int
+    B, D = x.shape
+    DS = A.shape[1]
+    dev = x.device
+    for t_, shape, dt, name in ((delta, (B, D), x.dtype, "delta"), (A, (D, DS), torch.float32, "A"),
+                                (b, (B, DS), x.dtype, "b"), (c, (B, DS), x.dtype, "c"),
+                                (h, (B, D, DS), torch.float32, "h")):
+        _check(t_, shape, dt, name, dev)
+    desc = make_desc(B, 1, D, DS, _io_of(x), 0, 0)
+    if y is None:
+        y = torch.empty((B, D), dtype=x.dtype, device=dev)
+    st = fn(ctypes.byref(desc), _ptr(x), _ptr(delta), _ptr(A), _ptr(b), _ptr(c), _ptr(h), _ptr(y), _stream(stream))
+    if st != 0:
+        raise SSMError(st, "ssm_scan_step")
+    return y
+
+
 def selective_scan(x, delta, A, b, c, h0=None, ckpt_interval=256):
     """Differentiable scan: returns (y, hT). Gradients flow to x, delta, A, b, c and h0;
     hT is differentiated too (its gradient enters the backward as ghT)."""

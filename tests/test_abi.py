@@ -128,3 +128,32 @@ def test_size_queries(L):
     assert L.ssm_scan_fwd_workspace_bytes(ctypes.byref(desc(T=0))) == 0
     assert L.ssm_scan_bwd_workspace_bytes(ctypes.byref(desc(B=0))) == 0
     assert L.ssm_scan_ckpt_bytes(None) == 0
+
+
+def step(L, d, x=FAKE, delta=FAKE, A=FAKE, b=FAKE, c=FAKE, h=FAKE, y=FAKE):
+    P = ctypes.c_void_p
+    return L.ssm_scan_step(ctypes.byref(d), P(x), P(delta), P(A), P(b), P(c), P(h), P(y), None)
+
+
+def test_step_argument_checks(L):
+    assert step(L, desc(T=2)) == 1                       # one step per call
+    assert step(L, desc(T=1, DS=8)) == 2
+    assert step(L, desc(T=1, io=5)) == 1
+    assert step(L, desc(T=1), h=None) == 1
+    assert step(L, desc(T=1), x=None) == 1
+    assert step(L, desc(T=1), h=FAKE + 4) == 3
+    assert step(L, desc(T=1), y=FAKE + 2) == 3
+    assert step(L, desc(T=1, B=0)) == 0                  # nothing to do, nothing launched
+    assert step(L, desc(T=1, D=0)) == 0
+
+
+def test_backward_carry_workspace(L):
+    # few chains and ten checkpoint chunks: the chunk-parallel schedule's carries
+    d = desc(B=2, T=1000, D=32, ckpt_interval=100)
+    carry = L.ssm_scan_bwd_carry_bytes(ctypes.byref(d))
+    assert carry >= 10 * 2 * 32 * (16 + 1) * 4
+    assert L.ssm_scan_bwd_workspace_bytes(ctypes.byref(d)) >= carry + 10 * 2 * 32 * 16 * 4
+    # one chunk: nothing to carry
+    assert L.ssm_scan_bwd_carry_bytes(ctypes.byref(desc(B=2, T=100, D=32, ckpt_interval=100))) == 0
+    # with checkpoints the carries are optional: a misaligned workspace is still rejected
+    assert bwd(L, d, ws=FAKE + 8, wsb=carry) == 3

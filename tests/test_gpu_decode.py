@@ -1,0 +1,81 @@
+"""GPU parity of the single-step decode entry (ssm_scan_step) against the oracle.
+
+One step with state h is the scan over T = 1 with h0 = h; T steps applied one
+after another in place must give the scan over T steps (outputs per step, the
+final state). Tolerances as for the forward: float32 I/O 1e-4, bf16 I/O 1e-2,
+as max |got - ref| / (1 + |ref|).
+"""
+import numpy as np
+import pytest
+
+import gen
+import oracle
+from gpu_util import assert_close, dev_inputs, to_host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _setup():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from selective_state_space_03_gb300 import build
+    build.build()
+    torch.cuda.set_device(0)
+
+
+def ssm():
+    import selective_state_space_03_gb300 as m
+    return m
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("B,D", [(1, 1), (3, 37), (4, 200), (16, 5120)])
+def test_one_step_is_the_scan_over_one_step(io, B, D):
+    w = gen.workload(2, B=B, T=1, D=D, io=io, h0_std=0.5)
+    inp = gen.make_inputs(w, seed=3)
+    t = dev_inputs(inp)
+    h = t["h0"].clone()
+    y = ssm().ssm_scan_step(t["x"][:, 0].contiguous(), t["delta"][:, 0].contiguous(), t["A"],
+                            t["b"][:, 0].contiguous(), t["c"][:, 0].contiguous(), h)
+    ref = oracle.fwd(inp["x"], inp["delta"], inp["A"], inp["b"], inp["c"], inp["h0"])
+    assert_close(to_host(y)[:, None, :], ref["y"], io, "fwd", "y")
+    assert_close(to_host(h), ref["hT"], io, "fwd", "hT")
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_steps_in_place_follow_the_scan(io):
+    import torch
+    w = gen.workload(2, B=2, T=40, D=72, io=io, h0_std=0.1)
+    inp = gen.make_inputs(w, seed=5)
+    t = dev_inputs(inp)
+    h = t["h0"].clone()
+    ys = []
+    for k in range(w.T):
+        ys.append(ssm().ssm_scan_step(t["x"][:, k].contiguous(), t["delta"][:, k].contiguous(), t["A"],
+                                      t["b"][:, k].contiguous(), t["c"][:, k].contiguous(), h))
+    torch.cuda.synchronize()
+    ref = oracle.fwd(inp["x"], inp["delta"], inp["A"], inp["b"], inp["c"], inp["h0"])
+    got = np.stack([to_host(v) for v in ys], axis=1)
+    assert_close(got, ref["y"], io, "fwd", "y")
+    assert_close(to_host(h), ref["hT"], io, "fwd", "hT")
+
+
+def test_step_writes_only_its_outputs():
+    import torch
+    B, D = 3, 40
+    w = gen.workload(2, B=B, T=1, D=D, h0_std=0.1)
+    inp = gen.make_inputs(w)
+    t = dev_inputs(inp)
+    pad, canary = 64, 777.0
+    hb = torch.full((B * D * 16 + 2 * pad,), canary, device="cuda:0")
+    yb = torch.full((B * D + 2 * pad,), canary, device="cuda:0")
+    h = hb[pad:pad + B * D * 16]
+    h.copy_(t["h0"].reshape(-1))
+    y = yb[pad:pad + B * D]
+    ssm().ssm_scan_step(t["x"][:, 0].contiguous(), t["delta"][:, 0].contiguous(), t["A"],
+                        t["b"][:, 0].contiguous(), t["c"][:, 0].contiguous(), h.view(B, D, 16), y=y.view(B, D))
+    torch.cuda.synchronize()
+    for full in (hb, yb):
+        assert torch.all(full[:pad] == canary) and torch.all(full[-pad:] == canary)
