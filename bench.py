@@ -201,7 +201,7 @@ def run_ours(args, rank, world, local_rank):
     desc = ssm.make_desc(w.B, w.T, w.D, w.DS, ssm.SSM_IO_BF16, K, 0)
     import ctypes
     fwd_kernels = 2 if ssm.lib().ssm_scan_fwd_workspace_bytes(ctypes.byref(desc)) else 1
-    bwd_kernels = 2 if ssm.lib().ssm_scan_bwd_carry_bytes(ctypes.byref(desc)) else 1
+    bwd_kernels = 2 if ssm.lib().ssm_scan_bwd_ckpt_workspace_bytes(ctypes.byref(desc)) else 1
     kernels_per_step = fwd_kernels + bwd_kernels
 
     def fwd():
@@ -244,6 +244,27 @@ def run_ours(args, rank, world, local_rank):
     total_ms = max_over_ranks(total_ms, dev)
     ms_per_step = total_ms / args.steps
     value = job_throughput(el, args.steps, world, total_ms)
+
+    # the same backward with fixed-order (bitwise reproducible) gb, gc, gA sums
+    ddesc = ssm.make_desc(w.B, w.T, w.D, w.DS, ssm.SSM_IO_BF16, K, 0, ssm.SSM_SCAN_DETERMINISTIC)
+    det_ws = torch.empty(ssm.lib().ssm_scan_bwd_ckpt_workspace_bytes(ctypes.byref(ddesc)), dtype=torch.uint8,
+                         device=dev)
+    g_det = {k: torch.empty_like(v) for k, v in grads.items()}
+
+    def bwd_det():
+        ssm.ssm_scan_bwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], ckpt, t["dy"], ckpt_interval=K,
+                         grads=g_det, workspace=det_ws, deterministic=True)
+
+    bwd_det()
+    torch.cuda.synchronize()
+    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    d0.record(stream)
+    for _ in range(5):
+        bwd_det()
+    d1.record(stream)
+    torch.cuda.synchronize()
+    bwd_det_ms = d0.elapsed_time(d1) / 5
+    del det_ws, g_det
 
     # ---- end to end through the public API with host buffers. Every step copies its inputs
     # from pinned host memory and all its outputs (y, hT and the six gradients) back; the steps
@@ -341,7 +362,7 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": w.name, "B": w.B, "T": w.T, "D": w.D, "DS": w.DS, "io": w.io,
                    "state_and_grads": "f32", "ckpt_interval": K, "l2": "inputs larger than L2 (no flush)",
                    "parallelism": f"replicas x{world}"},
-        "kernels": {"fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+        "kernels": {"fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "bwd_deterministic_ms": bwd_det_ms,
                     "fwd_elem_per_s": el / (fwd_ms / 1e3), "bwd_elem_per_s": el / (bwd_ms / 1e3),
                     "fwd_hbm_gbs": fwd_bytes / (fwd_ms / 1e3) / 1e9, "bwd_hbm_gbs": bwd_bytes / (bwd_ms / 1e3) / 1e9,
                     "fwd_hbm_frac": fwd_bytes / (fwd_ms / 1e3) / 1e9 / hbm_peak,

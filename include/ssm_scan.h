@@ -62,7 +62,7 @@ typedef enum { SSM_IO_F32 = 0, SSM_IO_BF16 = 1 } ssm_io_dtype;
 
 typedef enum {
     SSM_OK = 0,
-    SSM_ERR_INVALID_ARG = 1,  /* NULL required pointer, negative size, bad enum, B > 65535 */
+    SSM_ERR_INVALID_ARG = 1,  /* NULL required pointer, negative size, bad enum or flag, B > 65535 */
     SSM_ERR_UNSUPPORTED = 2,  /* DS != 16, or D > 2^27 */
     SSM_ERR_MISALIGNED = 3,   /* a data pointer is not 16-byte aligned */
     SSM_ERR_WORKSPACE = 4,    /* workspace NULL or smaller than the query returned */
@@ -77,8 +77,15 @@ typedef struct {
     int32_t chunk_len;      /* forward schedule: 0 = chosen by the library; > 0 = chunked
                                two-pass scan with chunks of this many steps; < 0 = one
                                pass over T. Every schedule computes the same function. */
-    int32_t reserved;       /* must be 0 */
+    int32_t flags;          /* 0 or SSM_SCAN_DETERMINISTIC; other bits must be 0 */
 } ssm_scan_desc;
+
+/* ssm_scan_desc.flags: the backward sums gb, gc and gA from per-CTA partials in
+ * the workspace in a fixed order instead of with atomic adds, so every output
+ * is bitwise identical from run to run for the same desc, inputs and GPU
+ * model. The forward and ssm_scan_step ignore the flag (they have no sums
+ * across CTAs). */
+#define SSM_SCAN_DETERMINISTIC 1
 
 /* Bytes of the checkpoint buffer: ceil(T/K)*B*D*DS*4, 0 when K == 0. */
 size_t ssm_scan_ckpt_bytes(const ssm_scan_desc* desc);
@@ -89,20 +96,25 @@ size_t ssm_scan_ckpt_bytes(const ssm_scan_desc* desc);
 size_t ssm_scan_fwd_workspace_bytes(const ssm_scan_desc* desc);
 
 /* Bytes of device scratch memory ssm_scan_bwd needs for this desc when it is
- * called with ckpt == NULL: the carries below plus the checkpoints it rebuilds. */
+ * called with ckpt == NULL: what ssm_scan_bwd_ckpt_workspace_bytes counts plus
+ * the checkpoints it rebuilds. */
 size_t ssm_scan_bwd_workspace_bytes(const ssm_scan_desc* desc);
 
-/* Bytes of optional scratch memory for the chunk-parallel backward, 0 when the
- * library does not use that schedule for this desc. It is used for shapes with
- * few (b, d) chains (one CTA per chain block would leave SMs idle) and at least
- * two checkpoint chunks: a carry pass computes, per chunk, the adjoint a_t g_t
- * at the chunk's start with zero adjoint entering it, plus the chunk's delta
- * sum; each chunk then runs on its own CTAs with the adjoint entering it folded
- * from the later chunks (the adjoint recurrence is linear, as the state
- * recurrence is for the chunked forward). A call with the forward's checkpoints
- * uses the schedule when workspace_bytes >= this value and sweeps each chain in
- * one CTA otherwise; both compute the same function up to rounding. */
-size_t ssm_scan_bwd_carry_bytes(const ssm_scan_desc* desc);
+/* Bytes of device scratch memory for a backward call with the forward's
+ * checkpoints; 0 for most shapes. It holds
+ *  - with SSM_SCAN_DETERMINISTIC, the per-CTA partial sums of gb, gc and gA
+ *    (required: a smaller workspace gives SSM_ERR_WORKSPACE);
+ *  - for shapes with few (b, d) chains (one CTA per chain block would leave
+ *    SMs idle) and at least two checkpoint chunks, the carries of the
+ *    chunk-parallel backward: a carry pass computes, per chunk, the adjoint
+ *    a_t g_t at the chunk's start with zero adjoint entering it, plus the
+ *    chunk's delta sum; each chunk then runs on its own CTAs with the adjoint
+ *    entering it folded from the later chunks (the adjoint recurrence is
+ *    linear, as the state recurrence is for the chunked forward). Without
+ *    SSM_SCAN_DETERMINISTIC these carries are optional: with less workspace
+ *    the backward sweeps each chain in one CTA, computing the same function up
+ *    to rounding. */
+size_t ssm_scan_bwd_ckpt_workspace_bytes(const ssm_scan_desc* desc);
 
 /* Forward scan: y, hT and (if K > 0 and ckpt != NULL) the checkpoints.
  *   h0    may be NULL (zero initial state)
@@ -126,8 +138,8 @@ ssm_status ssm_scan_fwd(const ssm_scan_desc* desc,
  *   ghT   may be NULL (hT not differentiated, as on the pssa page)
  *   workspace/workspace_bytes: with ckpt == NULL (or K outside 1..256) at
  *         least ssm_scan_bwd_workspace_bytes(desc), else SSM_ERR_WORKSPACE;
- *         with checkpoints, optional (see ssm_scan_bwd_carry_bytes); NULL or
- *         16-byte aligned
+ *         with checkpoints, ssm_scan_bwd_ckpt_workspace_bytes(desc) (see
+ *         there for what is optional); NULL or 16-byte aligned
  * gA, gb and gc are sums over many (b, d) chains accumulated with atomic adds,
  * so their last bits can differ from run to run. */
 ssm_status ssm_scan_bwd(const ssm_scan_desc* desc,

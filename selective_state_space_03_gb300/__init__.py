@@ -28,13 +28,13 @@ MAX_BWD_CKPT_INTERVAL = 256   # longest checkpoint interval ssm_scan_bwd reads w
 STATUS = {0: "SSM_OK", 1: "SSM_ERR_INVALID_ARG", 2: "SSM_ERR_UNSUPPORTED", 3: "SSM_ERR_MISALIGNED",
           4: "SSM_ERR_WORKSPACE", 5: "SSM_ERR_CUDA"}
 EXPORTS = ("ssm_scan_ckpt_bytes", "ssm_scan_fwd_workspace_bytes", "ssm_scan_bwd_workspace_bytes",
-           "ssm_scan_bwd_carry_bytes", "ssm_scan_fwd", "ssm_scan_bwd", "ssm_status_str")
+           "ssm_scan_bwd_ckpt_workspace_bytes", "ssm_scan_fwd", "ssm_scan_bwd", "ssm_scan_step", "ssm_status_str")
 
 
 class ssm_scan_desc(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int64), ("T", ctypes.c_int64), ("D", ctypes.c_int64), ("DS", ctypes.c_int64),
                 ("io", ctypes.c_int32), ("ckpt_interval", ctypes.c_int32), ("chunk_len", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("flags", ctypes.c_int32)]
 
 
 class SSMError(RuntimeError):
@@ -58,7 +58,7 @@ def lib() -> ctypes.CDLL:
             L = ctypes.CDLL(LIB_PATH)
             vp, sz, dp = ctypes.c_void_p, ctypes.c_size_t, ctypes.POINTER(ssm_scan_desc)
             for name in ("ssm_scan_ckpt_bytes", "ssm_scan_fwd_workspace_bytes", "ssm_scan_bwd_workspace_bytes",
-                         "ssm_scan_bwd_carry_bytes"):
+                         "ssm_scan_bwd_ckpt_workspace_bytes"):
                 getattr(L, name).argtypes = [dp]
                 getattr(L, name).restype = sz
             L.ssm_scan_fwd.argtypes = [dp] + [vp] * 9 + [vp, sz, vp]
@@ -71,8 +71,11 @@ def lib() -> ctypes.CDLL:
     return _lib
 
 
-def make_desc(B, T, D, DS=16, io=SSM_IO_F32, ckpt_interval=0, chunk_len=0) -> ssm_scan_desc:
-    return ssm_scan_desc(int(B), int(T), int(D), int(DS), int(io), int(ckpt_interval), int(chunk_len), 0)
+SSM_SCAN_DETERMINISTIC = 1
+
+
+def make_desc(B, T, D, DS=16, io=SSM_IO_F32, ckpt_interval=0, chunk_len=0, flags=0) -> ssm_scan_desc:
+    return ssm_scan_desc(int(B), int(T), int(D), int(DS), int(io), int(ckpt_interval), int(chunk_len), int(flags))
 
 
 # ---------------------------------------------------------------- torch marshalling
@@ -153,8 +156,10 @@ def ssm_scan_fwd(x, delta, A, b, c, h0=None, *, ckpt_interval=0, chunk_len=0, y=
 
 
 def ssm_scan_bwd(x, delta, A, b, c, h0, ckpt, dy, ghT=None, *, ckpt_interval=0, grads=None, workspace=None,
-                 stream=None):
-    """Backward scan. Returns dict(gx, gdelta, gA, gb, gc, gh0), all float32."""
+                 deterministic=False, stream=None):
+    """Backward scan. Returns dict(gx, gdelta, gA, gb, gc, gh0), all float32.
+    deterministic=True sets SSM_SCAN_DETERMINISTIC (fixed-order sums, bitwise
+    reproducible gb, gc, gA)."""
     torch = _torch()
     B, T, D = x.shape
     DS = A.shape[1]
@@ -163,7 +168,7 @@ def ssm_scan_bwd(x, delta, A, b, c, h0, ckpt, dy, ghT=None, *, ckpt_interval=0, 
     _check(dy, (B, T, D), x.dtype, "dy", dev)
     _check(ghT, (B, D, DS), torch.float32, "ghT", dev)
     _check(h0, (B, D, DS), torch.float32, "h0", dev)
-    desc = make_desc(B, T, D, DS, io, ckpt_interval, 0)
+    desc = make_desc(B, T, D, DS, io, ckpt_interval, 0, SSM_SCAN_DETERMINISTIC if deterministic else 0)
     L = lib()
     f32 = dict(dtype=torch.float32, device=dev)
     g = grads or {}
@@ -178,8 +183,8 @@ def ssm_scan_bwd(x, delta, A, b, c, h0, ckpt, dy, ghT=None, *, ckpt_interval=0, 
     # the library rebuilds checkpoints in the workspace when none are given or
     # when they are further apart than the backward reads directly
     rebuild = ckpt is None or not (0 < ckpt_interval <= MAX_BWD_CKPT_INTERVAL)
-    # (with checkpoints, the workspace only holds the optional chunk-parallel carries)
-    need = (L.ssm_scan_bwd_workspace_bytes if rebuild else L.ssm_scan_bwd_carry_bytes)(ctypes.byref(desc))
+    # (with checkpoints, the workspace holds the chunk-parallel carries and deterministic partials)
+    need = (L.ssm_scan_bwd_workspace_bytes if rebuild else L.ssm_scan_bwd_ckpt_workspace_bytes)(ctypes.byref(desc))
     if workspace is None:
         workspace, wsb = _workspace(need, dev)
     else:
@@ -291,5 +296,6 @@ class _Lazy:
 
 _ScanFn = _Lazy()
 
-__all__ = ["lib", "ssm_scan_desc", "make_desc", "ssm_scan_fwd", "ssm_scan_bwd", "selective_scan", "SSMError",
-           "EXPORTS", "LIB_PATH", "SSM_IO_F32", "SSM_IO_BF16"]
+__all__ = ["lib", "ssm_scan_desc", "make_desc", "ssm_scan_fwd", "ssm_scan_bwd", "ssm_scan_step",
+           "ssm_scan_fwd_noalloc", "selective_scan", "SSMError", "EXPORTS", "LIB_PATH", "SSM_IO_F32", "SSM_IO_BF16",
+           "SSM_SCAN_DETERMINISTIC"]

@@ -44,7 +44,7 @@ ssm_status check_desc(const ssm_scan_desc* d) {
     if (d == nullptr) return SSM_ERR_INVALID_ARG;
     if (d->B < 0 || d->T < 0 || d->D < 0 || d->DS < 0) return SSM_ERR_INVALID_ARG;
     if (d->io != SSM_IO_F32 && d->io != SSM_IO_BF16) return SSM_ERR_INVALID_ARG;
-    if (d->ckpt_interval < 0 || d->reserved != 0) return SSM_ERR_INVALID_ARG;
+    if (d->ckpt_interval < 0 || (d->flags & ~SSM_SCAN_DETERMINISTIC) != 0) return SSM_ERR_INVALID_ARG;
     if (d->B > 65535) return SSM_ERR_INVALID_ARG;
     if (d->DS != kDS) return SSM_ERR_UNSUPPORTED;
     if (d->D > kMaxD) return SSM_ERR_UNSUPPORTED;     // kernels use 32-bit in-tile offsets
@@ -146,6 +146,32 @@ size_t bwd_carry_bytes(const ssm_scan_desc& d) {
     return bwd_carry_Z_bytes(d) + align_up(size_t(cdiv(d.T, bwd_internal_K(d))) * size_t(d.B) * size_t(d.D) * 4);
 }
 
+// Backward workspace, in this order: chunk-parallel carries, deterministic partials of
+// gb/gc and of gA, rebuilt checkpoints. A call with the forward's checkpoints uses the
+// first three (`with_ckpt`), a call without them all four.
+struct BwdWorkspace {
+    size_t carry = 0, part_gbc = 0, part_gA = 0, rebuild = 0;
+    int64_t nblk = 0, nz = 1;      // channel blocks and chunks per (b, block) of the partials
+    size_t with_ckpt() const { return carry + part_gbc + part_gA; }
+    size_t total() const { return with_ckpt() + rebuild; }
+};
+
+BwdWorkspace bwd_workspace(const ssm_scan_desc& d) {
+    BwdWorkspace w;
+    const int64_t nck = cdiv(d.T, bwd_internal_K(d));
+    w.carry = bwd_carry_bytes(d);
+    const bool tpar = w.carry > 0;
+    const int kd = tpar ? 1 : bwd_channels_per_lane(d);
+    w.nblk = cdiv(d.D, kd == 2 ? 64 : 32);
+    w.nz = tpar ? nck : 1;
+    if (d.flags & SSM_SCAN_DETERMINISTIC) {
+        w.part_gbc = align_up(size_t(w.nblk) * size_t(d.B) * size_t(d.T) * 2 * kDS * 4);
+        w.part_gA = align_up(size_t(d.B) * size_t(w.nz) * size_t(d.D) * kDS * 4);
+    }
+    w.rebuild = align_up(size_t(nck) * size_t(d.B) * size_t(d.D) * kDS * 4);
+    return w;
+}
+
 }  // namespace
 }  // namespace ssm
 
@@ -176,15 +202,14 @@ size_t ssm_scan_fwd_workspace_bytes(const ssm_scan_desc* d) {
     return P.mode == 2 ? P.ws_S + P.ws_Sd : 0;
 }
 
-size_t ssm_scan_bwd_carry_bytes(const ssm_scan_desc* d) {
+size_t ssm_scan_bwd_ckpt_workspace_bytes(const ssm_scan_desc* d) {
     if (check_desc(d) != SSM_OK || d->B == 0 || d->T == 0 || d->D == 0) return 0;
-    return bwd_carry_bytes(*d);
+    return bwd_workspace(*d).with_ckpt();
 }
 
 size_t ssm_scan_bwd_workspace_bytes(const ssm_scan_desc* d) {
     if (check_desc(d) != SSM_OK || d->B == 0 || d->T == 0 || d->D == 0) return 0;
-    return bwd_carry_bytes(*d) +
-           align_up(size_t(cdiv(d->T, bwd_internal_K(*d))) * size_t(d->B) * size_t(d->D) * kDS * 4);
+    return bwd_workspace(*d).total();
 }
 
 ssm_status ssm_scan_fwd(const ssm_scan_desc* desc, const void* x, const void* delta, const float* A,
@@ -269,24 +294,26 @@ ssm_status ssm_scan_bwd(const ssm_scan_desc* desc, const void* x, const void* de
         return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
     }
 
-    // workspace: [carries of the chunk-parallel schedule][rebuilt checkpoints]
-    const size_t carry_bytes = bwd_carry_bytes(d);
+    // workspace: [carries][deterministic partials][rebuilt checkpoints]
+    const BwdWorkspace W = bwd_workspace(d);
+    const bool det = (d.flags & SSM_SCAN_DETERMINISTIC) != 0;
     if (workspace != nullptr && !aligned16(workspace)) return SSM_ERR_MISALIGNED;
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
     // checkpoints: the forward's, or rebuilt in the workspace
     const float* ck = ckpt;
     int64_t K = d.ckpt_interval;
     const bool rebuild = (ckpt == nullptr) || K <= 0 || K > kMaxBwdK;
-    // with the forward's checkpoints the carries are optional: without room for them the
-    // backward sweeps every chunk in one CTA
-    const bool tpar = carry_bytes > 0 && workspace != nullptr && workspace_bytes >= carry_bytes;
+    if (rebuild && (workspace == nullptr || workspace_bytes < W.total())) return SSM_ERR_WORKSPACE;
+    if (det && (workspace == nullptr || workspace_bytes < W.with_ckpt())) return SSM_ERR_WORKSPACE;
+    // with the forward's checkpoints and no deterministic partials the carries are optional:
+    // without room for them the backward sweeps every chain in one CTA
+    const bool tpar = W.carry > 0 && workspace != nullptr && workspace_bytes >= W.carry;
     if (rebuild) {
         K = bwd_internal_K(d);
-        const size_t need = ssm_scan_bwd_workspace_bytes(desc);
-        if (workspace == nullptr || workspace_bytes < need) return SSM_ERR_WORKSPACE;
         FwdLaunch L{};
         L.x = x; L.delta = delta; L.A = A; L.b = b; L.c = c; L.h0 = h0;
         L.y = nullptr; L.hT = nullptr;
-        L.ckpt = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + carry_bytes);
+        L.ckpt = reinterpret_cast<float*>(ws + W.with_ckpt());
         L.B = d.B; L.T = d.T; L.D = d.D; L.K = K; L.Lc = d.T; L.nchunk = 1;
         L.io = d.io == SSM_IO_BF16 ? IO::BF16 : IO::F32;
         L.vec = vec_ok(d);
@@ -296,10 +323,12 @@ ssm_status ssm_scan_bwd(const ssm_scan_desc* desc, const void* x, const void* de
         ck = L.ckpt;
     }
 
-    if (cudaMemsetAsync(gA, 0, size_t(d.D) * kDS * 4, s) != cudaSuccess) return SSM_ERR_CUDA;
-    const size_t bts = size_t(d.B) * size_t(d.T) * kDS * 4;
-    if (cudaMemsetAsync(gb, 0, bts, s) != cudaSuccess) return SSM_ERR_CUDA;
-    if (cudaMemsetAsync(gc, 0, bts, s) != cudaSuccess) return SSM_ERR_CUDA;
+    if (!det) {   // atomic accumulation targets (the deterministic sums overwrite them instead)
+        if (cudaMemsetAsync(gA, 0, size_t(d.D) * kDS * 4, s) != cudaSuccess) return SSM_ERR_CUDA;
+        const size_t bts = size_t(d.B) * size_t(d.T) * kDS * 4;
+        if (cudaMemsetAsync(gb, 0, bts, s) != cudaSuccess) return SSM_ERR_CUDA;
+        if (cudaMemsetAsync(gc, 0, bts, s) != cudaSuccess) return SSM_ERR_CUDA;
+    }
 
     BwdLaunch L{};
     L.x = x; L.delta = delta; L.A = A; L.b = b; L.c = c; L.ckpt = ck; L.dy = dy; L.ghT = ghT;
@@ -311,12 +340,18 @@ ssm_status ssm_scan_bwd(const ssm_scan_desc* desc, const void* x, const void* de
     L.tpar = tpar;
     if (tpar) {
         L.kd = 1;
-        L.carry_Z = static_cast<float*>(workspace);
-        L.carry_S = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + bwd_carry_Z_bytes(d));
+        L.carry_Z = reinterpret_cast<float*>(ws);
+        L.carry_S = reinterpret_cast<float*>(ws + bwd_carry_Z_bytes(d));
         const cudaError_t e1 = d.io == SSM_IO_BF16 ? launch_bwd_carry_bf16(L, s) : launch_bwd_carry_f32(L, s);
         if (e1 != cudaSuccess) return SSM_ERR_CUDA;
     }
-    const cudaError_t e = d.io == SSM_IO_BF16 ? launch_bwd_bf16(L, s) : launch_bwd_f32(L, s);
+    L.det = det;
+    if (det) {
+        L.part_gbc = reinterpret_cast<float*>(ws + W.carry);
+        L.part_gA = reinterpret_cast<float*>(ws + W.carry + W.part_gbc);
+    }
+    cudaError_t e = d.io == SSM_IO_BF16 ? launch_bwd_bf16(L, s) : launch_bwd_f32(L, s);
+    if (e == cudaSuccess && det) e = launch_bwd_reduce(L, W.nblk, W.nz, s);
     return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 

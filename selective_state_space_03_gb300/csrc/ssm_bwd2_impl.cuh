@@ -197,8 +197,13 @@ __global__ void __launch_bounds__(128, 3) bwd2_kernel(const BwdLaunch p) {
 #pragma unroll
         for (int w = 1; w < C::NW; ++w) v = v + *reinterpret_cast<const float4*>(gbc + w * LS * 2 * kDS + off);
         if (t0 + r < t_lim) {
-            float* dst = (tau == 0 ? p.gb : p.gc) + (b * T + t0 + r) * kDS + q * 4;
-            red_add_v4(dst, v.x, v.y, v.z, v.w);
+            if (p.det) {
+                *reinterpret_cast<float4*>(p.part_gbc + ((int64_t(blockIdx.x) * p.B + b) * T + t0 + r) * (2 * kDS) +
+                                           tau * kDS + q * 4) = v;
+            } else {
+                float* dst = (tau == 0 ? p.gb : p.gc) + (b * T + t0 + r) * kDS + q * 4;
+                red_add_v4(dst, v.x, v.y, v.z, v.w);
+            }
         }
     };
 
@@ -396,7 +401,12 @@ __global__ void __launch_bounds__(128, 3) bwd2_kernel(const BwdLaunch p) {
         if (!valid[k]) continue;
         *reinterpret_cast<float4*>(p.gh0 + (b * D + dch[k]) * kDS + s0) =
             make_float4(gcar[k][0], gcar[k][1], gcar[k][2], gcar[k][3]);
-        red_add_v4(p.gA + dch[k] * kDS + s0, gAacc[k][0], gAacc[k][1], gAacc[k][2], gAacc[k][3]);
+        if (p.det) {
+            *reinterpret_cast<float4*>(p.part_gA + (b * D + dch[k]) * kDS + s0) =
+                make_float4(gAacc[k][0], gAacc[k][1], gAacc[k][2], gAacc[k][3]);
+        } else {
+            red_add_v4(p.gA + dch[k] * kDS + s0, gAacc[k][0], gAacc[k][1], gAacc[k][2], gAacc[k][3]);
+        }
     }
 }
 

@@ -216,8 +216,13 @@ __global__ void __launch_bounds__(128, 4) bwd_kernel(const BwdLaunch p) {
 #pragma unroll
         for (int w = 1; w < C::NW; ++w) v = v + *reinterpret_cast<const float4*>(gbc + w * LS * 2 * kDS + off);
         if (t0 + r < t_lim) {
-            float* dst = (tau == 0 ? p.gb : p.gc) + (b * T + t0 + r) * kDS + q * 4;
-            red_add_v4(dst, v.x, v.y, v.z, v.w);
+            if (p.det) {
+                *reinterpret_cast<float4*>(p.part_gbc + ((int64_t(blockIdx.x) * p.B + b) * T + t0 + r) * (2 * kDS) +
+                                           tau * kDS + q * 4) = v;
+            } else {
+                float* dst = (tau == 0 ? p.gb : p.gc) + (b * T + t0 + r) * kDS + q * 4;
+                red_add_v4(dst, v.x, v.y, v.z, v.w);
+            }
         }
     };
 
@@ -371,9 +376,13 @@ __global__ void __launch_bounds__(128, 4) bwd_kernel(const BwdLaunch p) {
 
     if (!valid) return;
 #pragma unroll
-    for (int s = 0; s < KS; ++s) {
+    for (int s = 0; s < KS; ++s)
         if (jlo == 0) p.gh0[(b * D + d) * kDS + s0 + s] = gcarry[s];
-        atomicAdd(&p.gA[d * kDS + s0 + s], gAacc[s]);
+    if (p.det) {
+        *reinterpret_cast<float4*>(p.part_gA + ((b * gridDim.z + blockIdx.z) * D + d) * kDS + s0) =
+            make_float4(gAacc[0], gAacc[1], gAacc[2], gAacc[3]);
+    } else {
+        red_add_v4(p.gA + d * kDS + s0, gAacc[0], gAacc[1], gAacc[2], gAacc[3]);
     }
 }
 

@@ -67,7 +67,14 @@ struct BwdLaunch {
     bool tpar;
     float* carry_Z;      // [nck][B][D][16]: a_{cs} g_{cs} of chunk j with zero adjoint entering it
     float* carry_S;      // [nck][B][D]: sum of delta over chunk j
+    // deterministic sums: partials instead of atomic adds, reduced in a fixed order afterwards
+    bool det;
+    float* part_gbc;     // [channel blocks][B][T][2][16]: per-CTA sums over d of gb (0) and gc (1)
+    float* part_gA;      // [B * chunks][D][16]: per-CTA sums over t of gA (chunks = gridDim.z)
 };
+
+// Deterministic backward: sums of the per-CTA partials in a fixed order into gb, gc and gA.
+cudaError_t launch_bwd_reduce(const BwdLaunch& L, int64_t nblk, int64_t nz, cudaStream_t stream);
 
 constexpr int64_t kMaxBwdK = 256;   // largest checkpoint interval the backward reads directly
 

@@ -46,7 +46,7 @@ def test_library_exports_every_declared_symbol(L):
 
 def desc(**kw):
     import selective_state_space_03_gb300 as ssm
-    base = dict(B=2, T=64, D=32, DS=16, io=0, ckpt_interval=0, chunk_len=0)
+    base = dict(B=2, T=64, D=32, DS=16, io=0, ckpt_interval=0, chunk_len=0, flags=0)
     base.update(kw)
     return ssm.make_desc(**base)
 
@@ -85,7 +85,7 @@ def test_invalid_descriptors(L):
     assert fwd(L, desc(ckpt_interval=-1)) == 1
     assert fwd(L, desc(B=70000)) == 1
     d = desc()
-    d.reserved = 3
+    d.flags = 6
     assert fwd(L, d) == 1
     assert fwd(L, desc(DS=8)) == 2
     assert fwd(L, desc(DS=32)) == 2
@@ -150,10 +150,25 @@ def test_step_argument_checks(L):
 def test_backward_carry_workspace(L):
     # few chains and ten checkpoint chunks: the chunk-parallel schedule's carries
     d = desc(B=2, T=1000, D=32, ckpt_interval=100)
-    carry = L.ssm_scan_bwd_carry_bytes(ctypes.byref(d))
+    carry = L.ssm_scan_bwd_ckpt_workspace_bytes(ctypes.byref(d))
     assert carry >= 10 * 2 * 32 * (16 + 1) * 4
     assert L.ssm_scan_bwd_workspace_bytes(ctypes.byref(d)) >= carry + 10 * 2 * 32 * 16 * 4
     # one chunk: nothing to carry
-    assert L.ssm_scan_bwd_carry_bytes(ctypes.byref(desc(B=2, T=100, D=32, ckpt_interval=100))) == 0
+    assert L.ssm_scan_bwd_ckpt_workspace_bytes(ctypes.byref(desc(B=2, T=100, D=32, ckpt_interval=100))) == 0
     # with checkpoints the carries are optional: a misaligned workspace is still rejected
     assert bwd(L, d, ws=FAKE + 8, wsb=carry) == 3
+
+
+def test_deterministic_flag_workspace(L):
+    # one chunk, many channel blocks: partials of gb/gc per block and of gA per batch
+    d = desc(B=2, T=100, D=320, ckpt_interval=100, flags=1)
+    need = L.ssm_scan_bwd_ckpt_workspace_bytes(ctypes.byref(d))
+    assert need >= 10 * 2 * 100 * 32 * 4 + 2 * 320 * 16 * 4
+    assert bwd(L, d) == 4                                # the partials are required
+    assert bwd(L, d, ws=FAKE, wsb=need - 1) == 4
+    assert L.ssm_scan_bwd_workspace_bytes(ctypes.byref(d)) >= need + 2 * 320 * 16 * 4
+    # without the flag the same shape needs no workspace
+    assert L.ssm_scan_bwd_ckpt_workspace_bytes(ctypes.byref(desc(B=2, T=100, D=320, ckpt_interval=100))) == 0
+    # unknown flag bits are rejected
+    assert bwd(L, desc(flags=2)) == 1
+    assert step(L, desc(T=1, flags=4)) == 1

@@ -52,7 +52,7 @@ def forced(var, value):
 
 
 def run_case(w, K, chunk_len=0, seed=0, ghT=False, bwd=True, lanes=None, ckpt_to_bwd=True, bwd_kd=None,
-             bwd_tpar=None, bwd_workspace=None):
+             bwd_tpar=None, bwd_workspace=None, deterministic=False):
     import torch
     inp = gen.make_inputs(w, seed=seed, with_grad_inputs=bwd, with_ghT=ghT)
     t = dev_inputs(inp)
@@ -70,7 +70,7 @@ def run_case(w, K, chunk_len=0, seed=0, ghT=False, bwd=True, lanes=None, ckpt_to
     with forced("SSM_SCAN_FORCE_BWD_KD", bwd_kd), forced("SSM_SCAN_FORCE_BWD_TPAR", bwd_tpar):
         g = ssm().ssm_scan_bwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"],
                                ckpt if ckpt_to_bwd else None, t["dy"], t["ghT"], ckpt_interval=K,
-                               workspace=bwd_workspace)
+                               workspace=bwd_workspace, deterministic=deterministic)
     torch.cuda.synchronize()
     gref = oracle.bwd(inp["x"], inp["delta"], inp["A"], inp["b"], inp["c"], inp["h0"], inp["dy"], inp.get("ghT"))
     for k in GRADS:
@@ -138,6 +138,29 @@ def test_chunk_parallel_backward_rebuild_and_fallback():
 
 def test_workload2_sequential_backward():
     run_case(gen.workload(2), K=256, bwd_tpar=0)
+
+
+@pytest.mark.parametrize("layout", ["kd1", "kd2", "chunk_parallel"])
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_deterministic_backward(layout, io):
+    import torch
+    env = {"kd1": dict(bwd_kd=1, bwd_tpar=0), "kd2": dict(bwd_kd=2, bwd_tpar=0),
+           "chunk_parallel": dict(bwd_kd=1, bwd_tpar=1)}[layout]
+    w = gen.workload(2, B=3, T=300, D=680, io=io, h0_std=0.1)    # 11-22 channel blocks sum into gb, gc
+    # against the oracle
+    run_case(w, K=64, ghT=True, deterministic=True, **env)
+    # bitwise the same on every run
+    inp = gen.make_inputs(w, seed=1, with_grad_inputs=True, with_ghT=True)
+    t = dev_inputs(inp)
+    _, _, ck = ssm().ssm_scan_fwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], ckpt_interval=64)
+    runs = []
+    with forced("SSM_SCAN_FORCE_BWD_KD", env["bwd_kd"]), forced("SSM_SCAN_FORCE_BWD_TPAR", env["bwd_tpar"]):
+        for _ in range(3):
+            runs.append(ssm().ssm_scan_bwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], ck, t["dy"],
+                                           t["ghT"], ckpt_interval=64, deterministic=True))
+    torch.cuda.synchronize()
+    for k in GRADS:
+        assert torch.equal(runs[0][k], runs[1][k]) and torch.equal(runs[0][k], runs[2][k]), k
 
 
 @pytest.mark.parametrize("io", ["f32", "bf16"])
