@@ -7,12 +7,17 @@ receive the arrays it returns.
 Recipe (the benchmark workloads of the selective-scan pages, restated):
   * every tensor has its own counter-based stream: numpy's Philox4x32-10 bit
     generator keyed by (seed, tensor id); ids A=0, delta=1, x=2, b=3, c=4,
-    h0=5, dy=6, ghT=7;
+    h0=5, dy=6, ghT=7, D_skip=8;
   * normals are numpy ``standard_normal`` draws in float64;
   * ``A = -exp(A_log)``: either ``A_log[d, s] = log(s + 1)`` (so ``A = -(s+1)``,
     the "int" recipe) or ``A_log = log(U[1, 16])`` (the "uniform" recipe),
     computed in float64 and rounded to float32 (A is always float32);
   * ``delta = softplus(z + shift)``, z ~ N(0, 1), evaluated stably in float64;
+    with ``raw_delta`` the array holds ``z + shift`` itself (for the fused
+    softplus prologue, which applies softplus inside the scan);
+  * the skip weights ``D_skip`` (one per channel, float32) ~ N(0, 1) when asked
+    for (the trace page initialises them to ones; random values make a wrong
+    channel index visible);
   * x, b, c, dy ~ N(0, 1); h0 is zero or N(0, std^2) and always float32;
   * float64 values are rounded to float32 (round to nearest even); for bf16 I/O
     the float32 value is then rounded to bf16 (round to nearest even). bf16
@@ -27,7 +32,7 @@ from dataclasses import dataclass, replace
 
 import numpy as np
 
-TENSOR_IDS = {"A": 0, "delta": 1, "x": 2, "b": 3, "c": 4, "h0": 5, "dy": 6, "ghT": 7}
+TENSOR_IDS = {"A": 0, "delta": 1, "x": 2, "b": 3, "c": 4, "h0": 5, "dy": 6, "ghT": 7, "D_skip": 8}
 
 
 @dataclass(frozen=True)
@@ -98,7 +103,7 @@ def _softplus64(z: np.ndarray) -> np.ndarray:
 
 
 def make_inputs(w: Workload, seed: int = 0, with_grad_inputs: bool | None = None,
-                with_ghT: bool = False) -> dict:
+                with_ghT: bool = False, raw_delta: bool = False, with_skip: bool = False) -> dict:
     """Draw the inputs of workload ``w``.
 
     Returns a dict with x, delta, b, c (``w.io`` storage), A and h0 (float32,
@@ -118,7 +123,7 @@ def make_inputs(w: Workload, seed: int = 0, with_grad_inputs: bool | None = None
     out["A"] = (-np.exp(A_log)).astype(np.float32)
     z = _normal(seed, "delta", (B, T, D))
     z += w.delta_shift
-    out["delta"] = _store(_softplus64(z), w.io)
+    out["delta"] = _store(z if raw_delta else _softplus64(z), w.io)
     del z
     out["x"] = _store(_normal(seed, "x", (B, T, D)), w.io)
     out["b"] = _store(_normal(seed, "b", (B, T, DS)), w.io)
@@ -131,6 +136,8 @@ def make_inputs(w: Workload, seed: int = 0, with_grad_inputs: bool | None = None
         out["dy"] = _store(_normal(seed, "dy", (B, T, D)), w.io)
     if with_ghT:
         out["ghT"] = _normal(seed, "ghT", (B, D, DS)).astype(np.float32)
+    if with_skip:
+        out["D_skip"] = _normal(seed, "D_skip", (D,)).astype(np.float32)
     return out
 
 

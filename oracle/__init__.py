@@ -13,6 +13,13 @@ Inputs are upcast exactly to float64 here: float32 arrays directly, bf16 arrays
 Parity pins: every function here is pinned by ``tests/test_oracle.py`` against
 closed forms, an explicit O(T^2) sum, invariants, finite differences, Euler
 identities of the loss and a hand-worked dyadic example under ``tests/golden/``.
+
+The fused variants (``fwd_fused``, ``bwd_fused``) add what the model on the
+POPCORNBENCH trace page ("FW-GLM-5-1__l2_p30", its forward() op list and
+kernel) does around the scan: delta = softplus(delta_raw) before it and the
+skip y + x * D (one weight per channel) after it. They are written here in
+numpy, as plain elementwise steps around the C scan, with the chain rule for
+their gradients.
 """
 from __future__ import annotations
 
@@ -128,3 +135,42 @@ def loss(y, hT, dy, ghT=None) -> float:
     if ghT is not None:
         L += float(np.sum(to_f64(ghT) * hT))
     return L
+
+
+def softplus(v):
+    """log(1 + e^v) in float64 (the softplus the trace page applies to delta), overflow-free."""
+    return np.logaddexp(0.0, v)
+
+
+def sigmoid(v):
+    """1 / (1 + e^-v) in float64: the derivative of softplus."""
+    return 0.5 * (1.0 + np.tanh(0.5 * v))
+
+
+def fwd_fused(x, delta, A, b, c, h0=None, D_skip=None, delta_softplus: bool = False, ckpt_interval: int = 0):
+    """Forward with the trace page's prologue and epilogue: the scan runs on
+    softplus(delta) when ``delta_softplus`` (delta then holds the raw values),
+    and y gets + x * D_skip[d] when ``D_skip`` (shape (D,)) is given."""
+    dl = to_f64(delta)
+    if delta_softplus:
+        dl = softplus(dl)
+    out = fwd(x, dl, A, b, c, h0, ckpt_interval)
+    if D_skip is not None:
+        out["y"] = out["y"] + to_f64(x) * to_f64(D_skip)[None, None, :]
+    return out
+
+
+def bwd_fused(x, delta, A, b, c, h0, dy, ghT=None, D_skip=None, delta_softplus: bool = False):
+    """Backward of ``fwd_fused`` for L = sum(dy*y) + sum(ghT*hT). gdelta is with
+    respect to the raw delta when ``delta_softplus``; with ``D_skip`` the skip adds
+    dy * D_skip to gx and returns gD_skip[d] = sum_{b,t} dy * x."""
+    raw = to_f64(delta)
+    dl = softplus(raw) if delta_softplus else raw
+    g = bwd(x, dl, A, b, c, h0, dy, ghT)
+    if delta_softplus:
+        g["gdelta"] = g["gdelta"] * sigmoid(raw)
+    if D_skip is not None:
+        dy64, x64 = to_f64(dy), to_f64(x)
+        g["gx"] = g["gx"] + dy64 * to_f64(D_skip)[None, None, :]
+        g["gD_skip"] = np.einsum("btd,btd->d", dy64, x64)
+    return g

@@ -270,6 +270,92 @@ def test_backward_matches_torch_autograd_float64():
     np.testing.assert_allclose(run_fwd(p)["y"], y.detach().numpy(), rtol=1e-12, atol=1e-13)
 
 
+# ---------------------------------------------------------------- fused prologue / epilogue pins
+
+def test_softplus_and_sigmoid_values():
+    v = np.linspace(-30.0, 30.0, 121)
+    assert oracle.softplus(np.array(0.0)) == pytest.approx(math.log(2.0), rel=1e-15)
+    np.testing.assert_allclose(oracle.softplus(v) - oracle.softplus(-v), v, rtol=0, atol=1e-13)   # sp(v) - sp(-v) = v
+    np.testing.assert_allclose(oracle.softplus(np.array([50.0, 700.0])), [50.0, 700.0], rtol=1e-15)
+    np.testing.assert_allclose(oracle.softplus(np.array([-40.0])), [math.exp(-40.0)], rtol=1e-12)
+    assert oracle.sigmoid(np.array(0.0)) == 0.5
+    np.testing.assert_allclose(oracle.sigmoid(v) + oracle.sigmoid(-v), 1.0, rtol=0, atol=1e-15)
+    h = 1e-5
+    num = (oracle.softplus(v + h) - oracle.softplus(v - h)) / (2 * h)                             # d softplus = sigmoid
+    np.testing.assert_allclose(oracle.sigmoid(v), num, rtol=0, atol=1e-9)
+
+
+def fused_problem(seed, B, T, D, DS, ghT=True):
+    p = rand_problem(seed, B, T, D, DS, ghT=ghT)
+    r = np.random.default_rng(seed + 1000)
+    p["delta"] = r.standard_normal((B, T, D)) - 1.0       # raw values, softplus applied by the scan
+    p["D_skip"] = r.standard_normal(D)
+    return p
+
+
+def fused_fwd(p, **kw):
+    return oracle.fwd_fused(p["x"], p["delta"], p["A"], p["b"], p["c"], p["h0"], p["D_skip"], delta_softplus=True,
+                            **kw)
+
+
+def fused_bwd(p):
+    return oracle.bwd_fused(p["x"], p["delta"], p["A"], p["b"], p["c"], p["h0"], p["dy"], p["ghT"], p["D_skip"],
+                            delta_softplus=True)
+
+
+def test_fused_skip_alone_when_readout_is_zero():
+    p = fused_problem(21, B=2, T=9, D=5, DS=16)
+    p["c"] = np.zeros_like(p["c"])
+    y = fused_fwd(p)["y"]
+    assert np.array_equal(y, p["x"] * p["D_skip"][None, None, :])
+
+
+def test_fused_backward_central_finite_differences():
+    p = fused_problem(22, B=2, T=5, D=3, DS=4)
+    g = fused_bwd(p)
+
+    def loss():
+        f = fused_fwd(p)
+        return oracle.loss(f["y"], f["hT"], p["dy"], p["ghT"])
+
+    names = {"x": "gx", "delta": "gdelta", "A": "gA", "b": "gb", "c": "gc", "h0": "gh0", "D_skip": "gD_skip"}
+    for name, gname in names.items():
+        theta = p[name]
+        num = np.zeros_like(theta)
+        for i in np.ndindex(theta.shape):
+            step = 1e-6 * max(1.0, abs(theta[i]))
+            old = theta[i]
+            theta[i] = old + step
+            lp = loss()
+            theta[i] = old - step
+            lm = loss()
+            theta[i] = old
+            num[i] = (lp - lm) / (2 * step)
+        scale = max(1.0, np.max(np.abs(num)))
+        np.testing.assert_allclose(g[gname], num, rtol=0, atol=1e-7 * scale, err_msg=gname)
+
+
+def test_fused_backward_matches_torch_autograd_float64():
+    torch = pytest.importorskip("torch")
+    p = fused_problem(23, B=2, T=7, D=5, DS=16)
+    keys = ("x", "delta", "A", "b", "c", "h0", "D_skip")
+    tp = {k: torch.tensor(p[k], dtype=torch.float64, requires_grad=True) for k in keys}
+    dl_all = torch.nn.functional.softplus(tp["delta"])
+    h = tp["h0"]
+    ys = []
+    for t in range(p["x"].shape[1]):
+        dt = dl_all[:, t, :, None]
+        h = torch.exp(dt * tp["A"]) * h + dt * tp["b"][:, t, None, :] * tp["x"][:, t, :, None]
+        ys.append((h * tp["c"][:, t, None, :]).sum(-1))
+    y = torch.stack(ys, 1) + tp["x"] * tp["D_skip"]
+    L = (y * torch.tensor(p["dy"])).sum() + (h * torch.tensor(p["ghT"])).sum()
+    grads = torch.autograd.grad(L, [tp[k] for k in keys])
+    g = fused_bwd(p)
+    for name, tg in zip(("gx", "gdelta", "gA", "gb", "gc", "gh0", "gD_skip"), grads):
+        np.testing.assert_allclose(g[name], tg.numpy(), rtol=1e-11, atol=1e-12, err_msg=name)
+    np.testing.assert_allclose(fused_fwd(p)["y"], y.detach().numpy(), rtol=1e-12, atol=1e-13)
+
+
 def test_oracle_deterministic_across_thread_counts():
     p = rand_problem(14, B=2, T=30, D=37, DS=16, ghT=True)
     g1 = run_bwd(p)
