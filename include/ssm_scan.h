@@ -77,7 +77,8 @@ typedef struct {
     int32_t chunk_len;      /* forward schedule: 0 = chosen by the library; > 0 = chunked
                                two-pass scan with chunks of this many steps; < 0 = one
                                pass over T. Every schedule computes the same function. */
-    int32_t flags;          /* 0 or SSM_SCAN_DETERMINISTIC; other bits must be 0 */
+    int32_t flags;          /* SSM_SCAN_DETERMINISTIC | SSM_SCAN_DELTA_SOFTPLUS or 0;
+                               other bits must be 0 */
 } ssm_scan_desc;
 
 /* ssm_scan_desc.flags: the backward sums gb, gc and gA from per-CTA partials in
@@ -86,6 +87,14 @@ typedef struct {
  * model. The forward and ssm_scan_step ignore the flag (they have no sums
  * across CTAs). */
 #define SSM_SCAN_DETERMINISTIC 1
+
+/* ssm_scan_desc.flags: delta holds raw pre-activation values and every entry
+ * point scans with softplus(delta) = log(1 + exp(delta)) instead, computed in
+ * float32 inside the kernels; the backward's gdelta is then with respect to
+ * the raw values (gdelta_raw = gdelta * sigmoid(delta_raw)). This is the
+ * activation the model on the POPCORNBENCH trace page ("FW-GLM-5-1__l2_p30",
+ * its forward() op list) applies to its delta projection before the scan. */
+#define SSM_SCAN_DELTA_SOFTPLUS 2
 
 /* Bytes of the checkpoint buffer: ceil(T/K)*B*D*DS*4, 0 when K == 0. */
 size_t ssm_scan_ckpt_bytes(const ssm_scan_desc* desc);
@@ -149,6 +158,30 @@ ssm_status ssm_scan_bwd(const ssm_scan_desc* desc,
                         float* gx, float* gdelta, float* gA, float* gb, float* gc,
                         float* gh0,
                         void* workspace, size_t workspace_bytes, void* stream);
+
+/* The forward with the trace page's skip connection fused into its readout:
+ * y[b,t,d] = <h_t, c_t> + D_skip[d] * x[b,t,d] (its forward() op list, and the
+ * skip its kernel adds before storing y). D_skip is (D) float32 or NULL (no
+ * skip: then this is ssm_scan_fwd). Everything else as ssm_scan_fwd, including
+ * SSM_SCAN_DELTA_SOFTPLUS. */
+ssm_status ssm_scan_fwd_fused(const ssm_scan_desc* desc,
+                              const void* x, const void* delta, const float* A,
+                              const void* b, const void* c, const float* D_skip, const float* h0,
+                              void* y, float* hT, float* ckpt,
+                              void* workspace, size_t workspace_bytes, void* stream);
+
+/* The backward of ssm_scan_fwd_fused with the same D_skip: gx gets
+ * + dy * D_skip[d] and gD_skip[d] = sum_{b,t} dy[b,t,d] * x[b,t,d] ((D)
+ * float32, required when D_skip is not NULL; accumulated with atomic adds, or
+ * in a fixed order under SSM_SCAN_DETERMINISTIC). Everything else as
+ * ssm_scan_bwd. */
+ssm_status ssm_scan_bwd_fused(const ssm_scan_desc* desc,
+                              const void* x, const void* delta, const float* A,
+                              const void* b, const void* c, const float* D_skip, const float* h0,
+                              const float* ckpt, const void* dy, const float* ghT,
+                              float* gx, float* gdelta, float* gA, float* gb, float* gc,
+                              float* gh0, float* gD_skip,
+                              void* workspace, size_t workspace_bytes, void* stream);
 
 /* Forward scan that allocates nothing and takes no workspace. The pages have
  * no counterpart of this call; it exists for callers that cannot allocate

@@ -28,7 +28,8 @@ MAX_BWD_CKPT_INTERVAL = 256   # longest checkpoint interval ssm_scan_bwd reads w
 STATUS = {0: "SSM_OK", 1: "SSM_ERR_INVALID_ARG", 2: "SSM_ERR_UNSUPPORTED", 3: "SSM_ERR_MISALIGNED",
           4: "SSM_ERR_WORKSPACE", 5: "SSM_ERR_CUDA"}
 EXPORTS = ("ssm_scan_ckpt_bytes", "ssm_scan_fwd_workspace_bytes", "ssm_scan_bwd_workspace_bytes",
-           "ssm_scan_bwd_ckpt_workspace_bytes", "ssm_scan_fwd", "ssm_scan_bwd", "ssm_scan_step", "ssm_status_str")
+           "ssm_scan_bwd_ckpt_workspace_bytes", "ssm_scan_fwd", "ssm_scan_bwd", "ssm_scan_fwd_fused",
+           "ssm_scan_bwd_fused", "ssm_scan_step", "ssm_status_str")
 
 
 class ssm_scan_desc(ctypes.Structure):
@@ -65,6 +66,10 @@ def lib() -> ctypes.CDLL:
             L.ssm_scan_fwd.restype = ctypes.c_int
             L.ssm_scan_bwd.argtypes = [dp] + [vp] * 15 + [vp, sz, vp]
             L.ssm_scan_bwd.restype = ctypes.c_int
+            L.ssm_scan_fwd_fused.argtypes = [dp] + [vp] * 10 + [vp, sz, vp]
+            L.ssm_scan_fwd_fused.restype = ctypes.c_int
+            L.ssm_scan_bwd_fused.argtypes = [dp] + [vp] * 17 + [vp, sz, vp]
+            L.ssm_scan_bwd_fused.restype = ctypes.c_int
             L.ssm_status_str.argtypes = [ctypes.c_int]
             L.ssm_status_str.restype = ctypes.c_char_p
             _lib = L
@@ -119,9 +124,15 @@ def _workspace(nbytes, device):
     return torch.empty(nbytes, dtype=torch.uint8, device=device), nbytes
 
 
+SSM_SCAN_DELTA_SOFTPLUS = 2
+
+
 def ssm_scan_fwd(x, delta, A, b, c, h0=None, *, ckpt_interval=0, chunk_len=0, y=None, hT=None, ckpt=None,
-                 workspace=None, stream=None):
-    """Forward scan. Returns (y, hT, ckpt); ckpt is None when ckpt_interval == 0."""
+                 workspace=None, D_skip=None, delta_softplus=False, stream=None):
+    """Forward scan. Returns (y, hT, ckpt); ckpt is None when ckpt_interval == 0.
+    delta_softplus=True: delta holds raw values, the scan uses softplus(delta)
+    (SSM_SCAN_DELTA_SOFTPLUS). D_skip (D,) float32: y += D_skip * x, through
+    ssm_scan_fwd_fused."""
     torch = _torch()
     B, T, D = x.shape
     DS = A.shape[1] if A.dim() == 2 else 16
@@ -132,7 +143,8 @@ def ssm_scan_fwd(x, delta, A, b, c, h0=None, *, ckpt_interval=0, chunk_len=0, y=
     _check(b, (B, T, DS), x.dtype, "b", dev)
     _check(c, (B, T, DS), x.dtype, "c", dev)
     _check(h0, (B, D, DS), torch.float32, "h0", dev)
-    desc = make_desc(B, T, D, DS, io, ckpt_interval, chunk_len)
+    _check(D_skip, (D,), torch.float32, "D_skip", dev)
+    desc = make_desc(B, T, D, DS, io, ckpt_interval, chunk_len, SSM_SCAN_DELTA_SOFTPLUS if delta_softplus else 0)
     L = lib()
     if y is None:
         y = torch.empty((B, T, D), dtype=x.dtype, device=dev)
@@ -148,18 +160,24 @@ def ssm_scan_fwd(x, delta, A, b, c, h0=None, *, ckpt_interval=0, chunk_len=0, y=
         workspace, wsb = _workspace(need, dev)
     else:
         wsb = workspace.numel() * workspace.element_size()
-    st = L.ssm_scan_fwd(ctypes.byref(desc), _ptr(x), _ptr(delta), _ptr(A), _ptr(b), _ptr(c), _ptr(h0),
-                        _ptr(y), _ptr(hT), _ptr(ckpt), _ptr(workspace), wsb, _stream(stream))
+    if D_skip is None:
+        st = L.ssm_scan_fwd(ctypes.byref(desc), _ptr(x), _ptr(delta), _ptr(A), _ptr(b), _ptr(c), _ptr(h0),
+                            _ptr(y), _ptr(hT), _ptr(ckpt), _ptr(workspace), wsb, _stream(stream))
+    else:
+        st = L.ssm_scan_fwd_fused(ctypes.byref(desc), _ptr(x), _ptr(delta), _ptr(A), _ptr(b), _ptr(c),
+                                  _ptr(D_skip), _ptr(h0), _ptr(y), _ptr(hT), _ptr(ckpt), _ptr(workspace), wsb,
+                                  _stream(stream))
     if st != 0:
         raise SSMError(st, "ssm_scan_fwd")
     return y, hT, ckpt
 
 
 def ssm_scan_bwd(x, delta, A, b, c, h0, ckpt, dy, ghT=None, *, ckpt_interval=0, grads=None, workspace=None,
-                 deterministic=False, stream=None):
-    """Backward scan. Returns dict(gx, gdelta, gA, gb, gc, gh0), all float32.
-    deterministic=True sets SSM_SCAN_DETERMINISTIC (fixed-order sums, bitwise
-    reproducible gb, gc, gA)."""
+                 deterministic=False, D_skip=None, delta_softplus=False, stream=None):
+    """Backward scan. Returns dict(gx, gdelta, gA, gb, gc, gh0), all float32, plus
+    gD_skip when D_skip is given (ssm_scan_bwd_fused). deterministic=True sets
+    SSM_SCAN_DETERMINISTIC (fixed-order sums, bitwise reproducible gb, gc, gA);
+    delta_softplus=True sets SSM_SCAN_DELTA_SOFTPLUS (gdelta w.r.t. the raw delta)."""
     torch = _torch()
     B, T, D = x.shape
     DS = A.shape[1]
@@ -168,7 +186,9 @@ def ssm_scan_bwd(x, delta, A, b, c, h0, ckpt, dy, ghT=None, *, ckpt_interval=0, 
     _check(dy, (B, T, D), x.dtype, "dy", dev)
     _check(ghT, (B, D, DS), torch.float32, "ghT", dev)
     _check(h0, (B, D, DS), torch.float32, "h0", dev)
-    desc = make_desc(B, T, D, DS, io, ckpt_interval, 0, SSM_SCAN_DETERMINISTIC if deterministic else 0)
+    _check(D_skip, (D,), torch.float32, "D_skip", dev)
+    flags = (SSM_SCAN_DETERMINISTIC if deterministic else 0) | (SSM_SCAN_DELTA_SOFTPLUS if delta_softplus else 0)
+    desc = make_desc(B, T, D, DS, io, ckpt_interval, 0, flags)
     L = lib()
     f32 = dict(dtype=torch.float32, device=dev)
     g = grads or {}
@@ -180,6 +200,8 @@ def ssm_scan_bwd(x, delta, A, b, c, h0, ckpt, dy, ghT=None, *, ckpt_interval=0, 
         "gc": g.get("gc", torch.empty((B, T, DS), **f32)),
         "gh0": g.get("gh0", torch.empty((B, D, DS), **f32)),
     }
+    if D_skip is not None:
+        out["gD_skip"] = g.get("gD_skip", torch.empty((D,), **f32))
     # the library rebuilds checkpoints in the workspace when none are given or
     # when they are further apart than the backward reads directly
     rebuild = ckpt is None or not (0 < ckpt_interval <= MAX_BWD_CKPT_INTERVAL)
@@ -189,17 +211,23 @@ def ssm_scan_bwd(x, delta, A, b, c, h0, ckpt, dy, ghT=None, *, ckpt_interval=0, 
         workspace, wsb = _workspace(need, dev)
     else:
         wsb = workspace.numel() * workspace.element_size()
-    st = L.ssm_scan_bwd(ctypes.byref(desc), _ptr(x), _ptr(delta), _ptr(A), _ptr(b), _ptr(c), _ptr(h0),
-                        _ptr(ckpt), _ptr(dy), _ptr(ghT), _ptr(out["gx"]), _ptr(out["gdelta"]), _ptr(out["gA"]),
-                        _ptr(out["gb"]), _ptr(out["gc"]), _ptr(out["gh0"]), _ptr(workspace), wsb,
-                        _stream(stream))
+    if D_skip is None:
+        st = L.ssm_scan_bwd(ctypes.byref(desc), _ptr(x), _ptr(delta), _ptr(A), _ptr(b), _ptr(c), _ptr(h0),
+                            _ptr(ckpt), _ptr(dy), _ptr(ghT), _ptr(out["gx"]), _ptr(out["gdelta"]), _ptr(out["gA"]),
+                            _ptr(out["gb"]), _ptr(out["gc"]), _ptr(out["gh0"]), _ptr(workspace), wsb,
+                            _stream(stream))
+    else:
+        st = L.ssm_scan_bwd_fused(ctypes.byref(desc), _ptr(x), _ptr(delta), _ptr(A), _ptr(b), _ptr(c),
+                                  _ptr(D_skip), _ptr(h0), _ptr(ckpt), _ptr(dy), _ptr(ghT), _ptr(out["gx"]),
+                                  _ptr(out["gdelta"]), _ptr(out["gA"]), _ptr(out["gb"]), _ptr(out["gc"]),
+                                  _ptr(out["gh0"]), _ptr(out["gD_skip"]), _ptr(workspace), wsb, _stream(stream))
     if st != 0:
         raise SSMError(st, "ssm_scan_bwd")
     return out
 
 
 def ssm_scan_fwd_noalloc(x, delta, A, b, c, h0=None, *, ckpt_interval=0, chunk_len=0, y=None, hT=None, ckpt=None,
-                         stream=None):
+                         delta_softplus=False, stream=None):
     """Forward scan through ssm_scan_fwd_noalloc: the chunked schedule with its
     scratch in the library's fixed device array, for callers that cannot
     allocate scratch memory (outputs can be passed in so nothing is allocated
@@ -216,7 +244,7 @@ def ssm_scan_fwd_noalloc(x, delta, A, b, c, h0=None, *, ckpt_interval=0, chunk_l
                                 (b, (B, T, DS), x.dtype, "b"), (c, (B, T, DS), x.dtype, "c"),
                                 (h0, (B, D, DS), torch.float32, "h0")):
         _check(t_, shape, dt, name, dev)
-    desc = make_desc(B, T, D, DS, _io_of(x), ckpt_interval, chunk_len)
+    desc = make_desc(B, T, D, DS, _io_of(x), ckpt_interval, chunk_len, SSM_SCAN_DELTA_SOFTPLUS if delta_softplus else 0)
     if y is None:
         y = torch.empty((B, T, D), dtype=x.dtype, device=dev)
     if hT is None:
@@ -230,7 +258,7 @@ def ssm_scan_fwd_noalloc(x, delta, A, b, c, h0=None, *, ckpt_interval=0, chunk_l
     return y, hT, ckpt
 
 
-def ssm_scan_step(x, delta, A, b, c, h, *, y=None, stream=None):
+def ssm_scan_step(x, delta, A, b, c, h, *, y=None, delta_softplus=False, stream=None):
     """One decode step through ssm_scan_step: x, delta (B, D), b, c (B, DS) in the I/O
     dtype, A (D, DS) and the state h (B, D, DS) float32, which is updated in place.
     Returns y (B, D)."""
@@ -246,7 +274,7 @@ def ssm_scan_step(x, delta, A, b, c, h, *, y=None, stream=None):
                                 (b, (B, DS), x.dtype, "b"), (c, (B, DS), x.dtype, "c"),
                                 (h, (B, D, DS), torch.float32, "h")):
         _check(t_, shape, dt, name, dev)
-    desc = make_desc(B, 1, D, DS, _io_of(x), 0, 0)
+    desc = make_desc(B, 1, D, DS, _io_of(x), 0, 0, SSM_SCAN_DELTA_SOFTPLUS if delta_softplus else 0)
     if y is None:
         y = torch.empty((B, D), dtype=x.dtype, device=dev)
     st = fn(ctypes.byref(desc), _ptr(x), _ptr(delta), _ptr(A), _ptr(b), _ptr(c), _ptr(h), _ptr(y), _stream(stream))
@@ -298,4 +326,4 @@ _ScanFn = _Lazy()
 
 __all__ = ["lib", "ssm_scan_desc", "make_desc", "ssm_scan_fwd", "ssm_scan_bwd", "ssm_scan_step",
            "ssm_scan_fwd_noalloc", "selective_scan", "SSMError", "EXPORTS", "LIB_PATH", "SSM_IO_F32", "SSM_IO_BF16",
-           "SSM_SCAN_DETERMINISTIC"]
+           "SSM_SCAN_DETERMINISTIC", "SSM_SCAN_DELTA_SOFTPLUS"]

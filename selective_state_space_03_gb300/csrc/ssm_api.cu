@@ -44,7 +44,7 @@ ssm_status check_desc(const ssm_scan_desc* d) {
     if (d == nullptr) return SSM_ERR_INVALID_ARG;
     if (d->B < 0 || d->T < 0 || d->D < 0 || d->DS < 0) return SSM_ERR_INVALID_ARG;
     if (d->io != SSM_IO_F32 && d->io != SSM_IO_BF16) return SSM_ERR_INVALID_ARG;
-    if (d->ckpt_interval < 0 || (d->flags & ~SSM_SCAN_DETERMINISTIC) != 0) return SSM_ERR_INVALID_ARG;
+    if (d->ckpt_interval < 0 || (d->flags & ~(SSM_SCAN_DETERMINISTIC | SSM_SCAN_DELTA_SOFTPLUS)) != 0) return SSM_ERR_INVALID_ARG;
     if (d->B > 65535) return SSM_ERR_INVALID_ARG;
     if (d->DS != kDS) return SSM_ERR_UNSUPPORTED;
     if (d->D > kMaxD) return SSM_ERR_UNSUPPORTED;     // kernels use 32-bit in-tile offsets
@@ -150,9 +150,9 @@ size_t bwd_carry_bytes(const ssm_scan_desc& d) {
 // gb/gc and of gA, rebuilt checkpoints. A call with the forward's checkpoints uses the
 // first three (`with_ckpt`), a call without them all four.
 struct BwdWorkspace {
-    size_t carry = 0, part_gbc = 0, part_gA = 0, rebuild = 0;
+    size_t carry = 0, part_gbc = 0, part_gA = 0, part_gD = 0, rebuild = 0;
     int64_t nblk = 0, nz = 1;      // channel blocks and chunks per (b, block) of the partials
-    size_t with_ckpt() const { return carry + part_gbc + part_gA; }
+    size_t with_ckpt() const { return carry + part_gbc + part_gA + part_gD; }
     size_t total() const { return with_ckpt() + rebuild; }
 };
 
@@ -167,6 +167,7 @@ BwdWorkspace bwd_workspace(const ssm_scan_desc& d) {
     if (d.flags & SSM_SCAN_DETERMINISTIC) {
         w.part_gbc = align_up(size_t(w.nblk) * size_t(d.B) * size_t(d.T) * 2 * kDS * 4);
         w.part_gA = align_up(size_t(d.B) * size_t(w.nz) * size_t(d.D) * kDS * 4);
+        w.part_gD = align_up(size_t(d.B) * size_t(w.nz) * size_t(d.D) * 4);    // skip weights' gradient
     }
     w.rebuild = align_up(size_t(nck) * size_t(d.B) * size_t(d.D) * kDS * 4);
     return w;
@@ -212,16 +213,16 @@ size_t ssm_scan_bwd_workspace_bytes(const ssm_scan_desc* d) {
     return bwd_workspace(*d).total();
 }
 
-ssm_status ssm_scan_fwd(const ssm_scan_desc* desc, const void* x, const void* delta, const float* A,
-                        const void* b, const void* c, const float* h0, void* y, float* hT, float* ckpt,
-                        void* workspace, size_t workspace_bytes, void* stream) {
+ssm_status ssm_scan_fwd_fused(const ssm_scan_desc* desc, const void* x, const void* delta, const float* A,
+                              const void* b, const void* c, const float* D_skip, const float* h0, void* y,
+                              float* hT, float* ckpt, void* workspace, size_t workspace_bytes, void* stream) {
     ssm_status st = check_desc(desc);
     if (st != SSM_OK) return st;
     const ssm_scan_desc& d = *desc;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool work = d.B > 0 && d.T > 0 && d.D > 0;
     if (work && (!x || !delta || !A || !b || !c || !y)) return SSM_ERR_INVALID_ARG;
-    const void* ptrs[] = {x, delta, A, b, c, h0, y, hT, ckpt};
+    const void* ptrs[] = {x, delta, A, b, c, D_skip, h0, y, hT, ckpt};
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return SSM_ERR_MISALIGNED;
     if (!work) {
@@ -246,6 +247,8 @@ ssm_status ssm_scan_fwd(const ssm_scan_desc* desc, const void* x, const void* de
     L.vec = vec_ok(d);
     L.ckpt_only = false;
     L.G = P.G;
+    L.softplus = (d.flags & SSM_SCAN_DELTA_SOFTPLUS) != 0;
+    L.Dskip = D_skip;
     cudaError_t e;
     if (P.mode == 2) {
         L.Lc = P.Lc;
@@ -262,10 +265,18 @@ ssm_status ssm_scan_fwd(const ssm_scan_desc* desc, const void* x, const void* de
     return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
-ssm_status ssm_scan_bwd(const ssm_scan_desc* desc, const void* x, const void* delta, const float* A,
-                        const void* b, const void* c, const float* h0, const float* ckpt, const void* dy,
-                        const float* ghT, float* gx, float* gdelta, float* gA, float* gb, float* gc,
-                        float* gh0, void* workspace, size_t workspace_bytes, void* stream) {
+ssm_status ssm_scan_fwd(const ssm_scan_desc* desc, const void* x, const void* delta, const float* A,
+                        const void* b, const void* c, const float* h0, void* y, float* hT, float* ckpt,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+    return ssm_scan_fwd_fused(desc, x, delta, A, b, c, nullptr, h0, y, hT, ckpt, workspace, workspace_bytes,
+                              stream);
+}
+
+ssm_status ssm_scan_bwd_fused(const ssm_scan_desc* desc, const void* x, const void* delta, const float* A,
+                              const void* b, const void* c, const float* D_skip, const float* h0,
+                              const float* ckpt, const void* dy, const float* ghT, float* gx, float* gdelta,
+                              float* gA, float* gb, float* gc, float* gh0, float* gD_skip, void* workspace,
+                              size_t workspace_bytes, void* stream) {
     ssm_status st = check_desc(desc);
     if (st != SSM_OK) return st;
     const ssm_scan_desc& d = *desc;
@@ -274,13 +285,15 @@ ssm_status ssm_scan_bwd(const ssm_scan_desc* desc, const void* x, const void* de
     if (work && (!x || !delta || !A || !b || !c || !dy || !gx || !gdelta || !gb || !gc)) return SSM_ERR_INVALID_ARG;
     if (d.D > 0 && !gA) return SSM_ERR_INVALID_ARG;
     if (d.B > 0 && d.D > 0 && !gh0) return SSM_ERR_INVALID_ARG;
-    const void* ptrs[] = {x, delta, A, b, c, h0, ckpt, dy, ghT, gx, gdelta, gA, gb, gc, gh0};
+    if (D_skip && d.D > 0 && !gD_skip) return SSM_ERR_INVALID_ARG;
+    const void* ptrs[] = {x, delta, A, b, c, D_skip, h0, ckpt, dy, ghT, gx, gdelta, gA, gb, gc, gh0, gD_skip};
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return SSM_ERR_MISALIGNED;
     if (!work) {
         // no steps: gA = 0, gh0 = ghT (zeros without ghT); gb, gc have no rows unless D == 0
         cudaError_t e = cudaSuccess;
         if (d.D > 0) e = cudaMemsetAsync(gA, 0, size_t(d.D) * kDS * 4, s);
+        if (e == cudaSuccess && D_skip && d.D > 0) e = cudaMemsetAsync(gD_skip, 0, size_t(d.D) * 4, s);
         if (e == cudaSuccess && d.B > 0 && d.D > 0) {
             const size_t bytes = size_t(d.B) * size_t(d.D) * kDS * 4;
             e = ghT ? cudaMemcpyAsync(gh0, ghT, bytes, cudaMemcpyDeviceToDevice, s) : cudaMemsetAsync(gh0, 0, bytes, s);
@@ -319,6 +332,7 @@ ssm_status ssm_scan_bwd(const ssm_scan_desc* desc, const void* x, const void* de
         L.vec = vec_ok(d);
         L.G = 4;
         L.ckpt_only = true;
+        L.softplus = (d.flags & SSM_SCAN_DELTA_SOFTPLUS) != 0;
         if (run_fwd(d, L, 3, s) != cudaSuccess) return SSM_ERR_CUDA;
         ck = L.ckpt;
     }
@@ -328,6 +342,7 @@ ssm_status ssm_scan_bwd(const ssm_scan_desc* desc, const void* x, const void* de
         const size_t bts = size_t(d.B) * size_t(d.T) * kDS * 4;
         if (cudaMemsetAsync(gb, 0, bts, s) != cudaSuccess) return SSM_ERR_CUDA;
         if (cudaMemsetAsync(gc, 0, bts, s) != cudaSuccess) return SSM_ERR_CUDA;
+        if (D_skip && cudaMemsetAsync(gD_skip, 0, size_t(d.D) * 4, s) != cudaSuccess) return SSM_ERR_CUDA;
     }
 
     BwdLaunch L{};
@@ -338,6 +353,7 @@ ssm_status ssm_scan_bwd(const ssm_scan_desc* desc, const void* x, const void* de
     L.vec = vec_ok(d);
     L.kd = bwd_channels_per_lane(d);
     L.tpar = tpar;
+    L.softplus = (d.flags & SSM_SCAN_DELTA_SOFTPLUS) != 0;
     if (tpar) {
         L.kd = 1;
         L.carry_Z = reinterpret_cast<float*>(ws);
@@ -345,14 +361,26 @@ ssm_status ssm_scan_bwd(const ssm_scan_desc* desc, const void* x, const void* de
         const cudaError_t e1 = d.io == SSM_IO_BF16 ? launch_bwd_carry_bf16(L, s) : launch_bwd_carry_f32(L, s);
         if (e1 != cudaSuccess) return SSM_ERR_CUDA;
     }
+    L.softplus = (d.flags & SSM_SCAN_DELTA_SOFTPLUS) != 0;
+    L.Dskip = D_skip;
+    L.gDskip = gD_skip;
     L.det = det;
     if (det) {
         L.part_gbc = reinterpret_cast<float*>(ws + W.carry);
         L.part_gA = reinterpret_cast<float*>(ws + W.carry + W.part_gbc);
+        L.part_gD = reinterpret_cast<float*>(ws + W.carry + W.part_gbc + W.part_gA);
     }
     cudaError_t e = d.io == SSM_IO_BF16 ? launch_bwd_bf16(L, s) : launch_bwd_f32(L, s);
     if (e == cudaSuccess && det) e = launch_bwd_reduce(L, W.nblk, W.nz, s);
     return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+ssm_status ssm_scan_bwd(const ssm_scan_desc* desc, const void* x, const void* delta, const float* A,
+                        const void* b, const void* c, const float* h0, const float* ckpt, const void* dy,
+                        const float* ghT, float* gx, float* gdelta, float* gA, float* gb, float* gc,
+                        float* gh0, void* workspace, size_t workspace_bytes, void* stream) {
+    return ssm_scan_bwd_fused(desc, x, delta, A, b, c, nullptr, h0, ckpt, dy, ghT, gx, gdelta, gA, gb, gc, gh0,
+                              nullptr, workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"

@@ -64,7 +64,7 @@ struct Bwd2Cfg {
 };
 
 
-template <typename TIO, bool VEC>
+template <typename TIO, bool VEC, bool FUSE>
 __global__ void __launch_bounds__(128, 3) bwd2_kernel(const BwdLaunch p) {
     using C = Bwd2Cfg<TIO>;
     constexpr int NT = C::NT, KS = C::KS, NP = C::NP, DT = C::DT, LS = C::LS, EPC = C::EPC;
@@ -106,6 +106,9 @@ __global__ void __launch_bounds__(128, 3) bwd2_kernel(const BwdLaunch p) {
     float* gdg = p.gdelta + b * T * D;
 
     // per channel k and state s of this lane: A*log2(e), the carried adjoint a_{t+1} g_{t+1}, gA
+    float Dk[2], skip_acc[2] = {0.f, 0.f};       // skip weights, sums of dy x (fused variant)
+#pragma unroll
+    for (int k = 0; k < 2; ++k) Dk[k] = (FUSE && valid[k] && p.Dskip != nullptr) ? p.Dskip[dch[k]] : 0.f;
     float A2[2][KS], gcar[2][KS], gAacc[2][KS];
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
@@ -167,13 +170,18 @@ __global__ void __launch_bounds__(128, 3) bwd2_kernel(const BwdLaunch p) {
         cp_async_commit();
     };
     // raw tile -> (d0, d0*x0, d1, d1*x1) and (dy0, dy1, x0, x1) per (step, pair); float32 b, c rows
-    auto convert = [&](bool rev) {
+    // (rows >= rows_valid are padding: with softplus their delta must stay 0, not ln 2)
+    auto convert = [&](bool rev, int64_t rows_valid) {
 #pragma unroll
         for (int q = 0; q < LS * NP / NT; ++q) {
             const int i = tid + NT * q;
             const int r = i / NP, pp = i % NP;
             float dl[2], xv[2];
             load_vals<TIO, 2>(dr + r * DT + 2 * pp, dl);
+            if (FUSE && p.softplus) {
+                dl[0] = r < rows_valid ? softplus_f32(dl[0]) : 0.f;
+                dl[1] = r < rows_valid ? softplus_f32(dl[1]) : 0.f;
+            }
             load_vals<TIO, 2>(xr + r * DT + 2 * pp, xv);
             conv1[i] = make_float4(dl[0], dl[0] * xv[0], dl[1], dl[1] * xv[1]);
             if (rev) {
@@ -227,7 +235,7 @@ __global__ void __launch_bounds__(128, 3) bwd2_kernel(const BwdLaunch p) {
         for (int i = 0; i < nsub; ++i) {
             cp_async_wait<0>();
             __syncthreads();
-            convert(false);
+            convert(false, ce - (cs + int64_t(i) * LS));
             __syncthreads();
             if (i + 1 < nsub) stage(cs + int64_t(i + 1) * LS, ce, false);
             if (i + 1 < nsub) {
@@ -286,7 +294,7 @@ __global__ void __launch_bounds__(128, 3) bwd2_kernel(const BwdLaunch p) {
                 }
             }
             if (pend_t0 >= 0) flush_gbc(pend_t0, pend_lim);
-            convert(true);
+            convert(true, ce - t0);
             __syncthreads();
             if (ii + 1 < nsub) stage(t0 - LS, ce, true);
             pend_t0 = t0;
@@ -376,9 +384,19 @@ __global__ void __launch_bounds__(128, 3) bwd2_kernel(const BwdLaunch p) {
                 const float4 w = conv2[r * NP + pc];
                 const int64_t t = t0 + r;
                 if (t < ce) {
-                    const float gx0 = v.x * qs[0], gx1 = v.z * qs[1];
-                    constexpr float kLn2 = 0.6931471805599453f;                       // A = A2 ln 2
-                    const float gd0 = fmaf(rs[0], kLn2, w.z * qs[0]), gd1 = fmaf(rs[1], kLn2, w.w * qs[1]);
+                    float gx0 = v.x * qs[0], gx1 = v.z * qs[1];
+                    // (A = A2 ln 2)
+                    float gd0 = fmaf(rs[0], kLn2, w.z * qs[0]), gd1 = fmaf(rs[1], kLn2, w.w * qs[1]);
+                    if constexpr (FUSE) {
+                        gx0 = fmaf(Dk[0], w.x, gx0);                   // skip: y += D x
+                        gx1 = fmaf(Dk[1], w.y, gx1);
+                        if (p.softplus) {                              // w.r.t. the raw delta
+                            gd0 *= sigmoid_from_softplus(v.x);
+                            gd1 *= sigmoid_from_softplus(v.z);
+                        }
+                        skip_acc[0] = fmaf(w.x, w.z, skip_acc[0]);
+                        skip_acc[1] = fmaf(w.y, w.w, skip_acc[1]);
+                    }
                     if (VEC && valid[1]) {
                         *reinterpret_cast<float2*>(gxg + t * D + dch[0]) = make_float2(gx0, gx1);
                         *reinterpret_cast<float2*>(gdg + t * D + dch[0]) = make_float2(gd0, gd1);
@@ -395,6 +413,21 @@ __global__ void __launch_bounds__(128, 3) bwd2_kernel(const BwdLaunch p) {
     tmem_fence_after_sync();
     if (pend_t0 >= 0) flush_gbc(pend_t0, pend_lim);
     if (warp == 0) tmem_dealloc(tmem_base, C::TMEM_COLS);
+
+    if constexpr (FUSE) {
+        if (p.Dskip != nullptr) {      // gD[d] += sum over this CTA's steps of dy x (the 4 lanes' steps)
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                float v = skip_acc[k];
+                v += __shfl_xor_sync(0xffffffffu, v, 1);
+                v += __shfl_xor_sync(0xffffffffu, v, 2);
+                if (valid[k] && sg == 0) {
+                    if (p.det) p.part_gD[b * D + dch[k]] = v;
+                    else atomicAdd(p.gDskip + dch[k], v);
+                }
+            }
+        }
+    }
 
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
@@ -413,7 +446,9 @@ __global__ void __launch_bounds__(128, 3) bwd2_kernel(const BwdLaunch p) {
 template <typename TIO>
 cudaError_t launch_bwd2_io(const BwdLaunch& L, cudaStream_t stream) {
     using C = Bwd2Cfg<TIO>;
-    auto kern = L.vec ? bwd2_kernel<TIO, true> : bwd2_kernel<TIO, false>;
+    const bool fuse = L.softplus || L.Dskip != nullptr;
+    auto kern = fuse ? (L.vec ? bwd2_kernel<TIO, true, true> : bwd2_kernel<TIO, false, true>)
+                     : (L.vec ? bwd2_kernel<TIO, true, false> : bwd2_kernel<TIO, false, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::SMEM));
     if (e != cudaSuccess) return e;
     const dim3 grid(unsigned((L.D + C::DT - 1) / C::DT), unsigned(L.B));

@@ -108,7 +108,7 @@ __device__ __forceinline__ float4 operator+(const float4 a, const float4 b) {
     return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
 }
 
-template <typename TIO, bool VEC>
+template <typename TIO, bool VEC, bool FUSE>
 __global__ void __launch_bounds__(128, 4) bwd_kernel(const BwdLaunch p) {
     using C = BwdCfg<TIO>;
     constexpr int NT = C::NT, KS = C::KS, DT = C::DT, LS = C::LS, EPC = C::EPC;
@@ -148,6 +148,8 @@ __global__ void __launch_bounds__(128, 4) bwd_kernel(const BwdLaunch p) {
     float* gxg = p.gx + b * T * D;
     float* gdg = p.gdelta + b * T * D;
 
+    const float Dk = (FUSE && valid && p.Dskip != nullptr) ? p.Dskip[d] : 0.f;   // skip weight
+    float skip_acc = 0.f;                                                         // sum of dy x
     float A2[KS], Af[KS], gcarry[KS], gAacc[KS];
 #pragma unroll
     for (int s = 0; s < KS; ++s) {
@@ -194,11 +196,14 @@ __global__ void __launch_bounds__(128, 4) bwd_kernel(const BwdLaunch p) {
         cp_async_commit();
     };
     // raw tile -> (delta, delta*x, x, dy) per (step, channel) and float32 b, c rows
-    auto convert = [&](bool rev) {
+    // (rows >= rows_valid are padding: with softplus their delta must stay 0, not ln 2)
+    auto convert = [&](bool rev, int64_t rows_valid) {
 #pragma unroll
         for (int k = 0; k < LS * DT / NT; ++k) {
             const int i = tid + NT * k;
-            const float dl = to_f32(dr[i]), xv = to_f32(xr[i]);
+            float dl = to_f32(dr[i]);
+            if (FUSE && p.softplus) dl = (i / DT < rows_valid) ? softplus_f32(dl) : 0.f;
+            const float xv = to_f32(xr[i]);
             conv[i] = make_float4(dl, dl * xv, xv, rev ? to_f32(yr[i]) : 0.f);
         }
 #pragma unroll
@@ -260,7 +265,7 @@ __global__ void __launch_bounds__(128, 4) bwd_kernel(const BwdLaunch p) {
         for (int i = 0; i < nsub; ++i) {
             cp_async_wait<0>();
             __syncthreads();
-            convert(false);
+            convert(false, ce - (cs + int64_t(i) * LS));
             __syncthreads();
             if (i + 1 < nsub) stage(cs + int64_t(i + 1) * LS, ce, false);
             sub[i * NT + tid] = make_float4(h[0], h[1], h[2], h[3]);
@@ -283,7 +288,7 @@ __global__ void __launch_bounds__(128, 4) bwd_kernel(const BwdLaunch p) {
             cp_async_wait<0>();
             __syncthreads();
             if (pend_t0 >= 0) flush_gbc(pend_t0, pend_lim);
-            convert(true);
+            convert(true, ce - t0);
             __syncthreads();
             if (ii + 1 < nsub) stage(t0 - LS, ce, true);
             pend_t0 = t0;
@@ -362,8 +367,15 @@ __global__ void __launch_bounds__(128, 4) bwd_kernel(const BwdLaunch p) {
                 const float dl = vr[0], xv = vr[2];
                 const int64_t t = t0 + r;
                 if (valid && t < ce) {
-                    gxg[t * D + d] = dl * qs;
-                    gdg[t * D + d] = rs + xv * qs;
+                    float gxv = dl * qs, gdv = rs + xv * qs;
+                    if constexpr (FUSE) {
+                        const float dyv = vr[3];
+                        gxv = fmaf(Dk, dyv, gxv);                           // skip: y += D x
+                        if (p.softplus) gdv *= sigmoid_from_softplus(dl);   // w.r.t. the raw delta
+                        skip_acc = fmaf(dyv, xv, skip_acc);
+                    }
+                    gxg[t * D + d] = gxv;
+                    gdg[t * D + d] = gdv;
                 }
             }
         }
@@ -374,6 +386,16 @@ __global__ void __launch_bounds__(128, 4) bwd_kernel(const BwdLaunch p) {
     if (pend_t0 >= 0) flush_gbc(pend_t0, pend_lim);
     if (warp == 0) tmem_dealloc(tmem_base, C::TMEM_COLS);
 
+    if constexpr (FUSE) {
+        if (p.Dskip != nullptr) {      // gD[d] += sum over this CTA's steps of dy x (the 4 lanes' steps)
+            skip_acc += __shfl_xor_sync(0xffffffffu, skip_acc, 1);
+            skip_acc += __shfl_xor_sync(0xffffffffu, skip_acc, 2);
+            if (valid && sg == 0) {
+                if (p.det) p.part_gD[(b * gridDim.z + blockIdx.z) * D + d] = skip_acc;
+                else atomicAdd(p.gDskip + d, skip_acc);
+            }
+        }
+    }
     if (!valid) return;
 #pragma unroll
     for (int s = 0; s < KS; ++s)
@@ -440,8 +462,11 @@ __global__ void __launch_bounds__(128) bwd_carry_kernel(const BwdLaunch p) {
         }
         __syncthreads();
 #pragma unroll 4
+        const int64_t rows = ce - (cs + int64_t(ntile - 1 - ii) * LS);
         for (int r = LS - 1; r >= 0; --r) {      // rows past ce are zero: a = 1, g unchanged
-            const float dl = to_f32(dr[buf][r * DT + c]), dy = to_f32(yr[buf][r * DT + c]);
+            float dl = to_f32(dr[buf][r * DT + c]);
+            if (p.softplus) dl = (r < rows) ? softplus_f32(dl) : 0.f;
+            const float dy = to_f32(yr[buf][r * DT + c]);
             float cc[KS];
             load_vals<TIO, KS>(cr[buf] + r * kDS + s0, cc);
 #pragma unroll
@@ -471,7 +496,9 @@ cudaError_t launch_bwd_carry_io(const BwdLaunch& L, cudaStream_t stream) {
 template <typename TIO>
 cudaError_t launch_bwd_io(const BwdLaunch& L, cudaStream_t stream) {
     using C = BwdCfg<TIO>;
-    auto kern = L.vec ? bwd_kernel<TIO, true> : bwd_kernel<TIO, false>;
+    const bool fuse = L.softplus || L.Dskip != nullptr;
+    auto kern = fuse ? (L.vec ? bwd_kernel<TIO, true, true> : bwd_kernel<TIO, false, true>)
+                     : (L.vec ? bwd_kernel<TIO, true, false> : bwd_kernel<TIO, false, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::SMEM));
     if (e != cudaSuccess) return e;
     const unsigned nz = L.tpar ? unsigned((L.T + L.K - 1) / L.K) : 1u;

@@ -22,6 +22,34 @@ __device__ __forceinline__ float ex2(float v) {
     return r;
 }
 
+// log2(v) on the MUFU; absolute error about 2^-22 for v in [1, 2].
+__device__ __forceinline__ float lg2(float v) {
+    float r;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+    return r;
+}
+
+constexpr float kLn2 = 0.6931471805599453f;
+
+// softplus(v) = log(1 + e^v) = max(v, 0) + log1p(e^-|v|), the activation the trace page's
+// model applies to delta. log1p(e) comes from its Taylor series e - e^2/2 + ... + e^5/5 when
+// e < 1/32 (where 1 + e would round most of e away; truncation below 1e-8 relative), else
+// from log2(1 + e) on the MUFU (relative error below 1e-5 there).
+__device__ __forceinline__ float softplus_f32(float v) {
+    const float e = ex2(-fabsf(v) * kLog2e);                 // in (0, 1]
+    const float l = e < 0.03125f
+        ? e * (1.f - e * (0.5f - e * (0.33333334f - e * (0.25f - e * 0.2f))))
+        : lg2(1.f + e) * kLn2;
+    return fmaxf(v, 0.f) + l;
+}
+
+// sigmoid(v), the derivative of softplus, from sp = softplus(v): sigmoid(v) = 1 - e^-sp.
+// Small sp from the series sp - sp^2/2 + sp^3/6 - sp^4/24 (no cancellation).
+__device__ __forceinline__ float sigmoid_from_softplus(float sp) {
+    return sp < 0.03125f ? sp * (1.f - sp * (0.5f - sp * (0.16666667f - sp * 0.041666668f)))
+                         : 1.f - ex2(-sp * kLog2e);
+}
+
 __device__ __forceinline__ float to_f32(float v) { return v; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
 

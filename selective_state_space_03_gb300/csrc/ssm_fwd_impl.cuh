@@ -65,13 +65,16 @@ struct FwdCfg {
     static constexpr size_t BC_F32 = BF ? size_t(TT) * kDS * 4 : 0;          // widened copy (bf16)
     static constexpr size_t Y_BYTES = size_t(TT) * DT * sizeof(TIO);
     static constexpr size_t SMEM = 2 * X_BYTES + 2 * BC_RAW + 2 * BC_F32 + Y_BYTES;
+    // fused variant: delta of the current tile as float32 (softplus applied when asked)
+    static constexpr size_t DSF_BYTES = size_t(TT) * DT * 4;
+    static constexpr size_t SMEM_FUSE = SMEM + DSF_BYTES;
     // registers: keep enough warps resident for the whole grid of the largest shapes
     static constexpr int MINB = (KD == 2) ? 20 : 1;
     static_assert(KD == 1 || G == 2, "multi-channel lanes are built with 2 lanes per channel");
     static_assert(X_CPR >= 1 && DT % EPC == 0, "tile rows must be whole 16-byte chunks");
 };
 
-template <typename TIO, int G, int KD, bool VEC, int MODE, bool CKT>
+template <typename TIO, int G, int KD, bool VEC, int MODE, bool CKT, bool FUSE>
 __global__ void __launch_bounds__(32, FwdCfg<TIO, G, KD>::MINB) fwd_kernel(const FwdLaunch p) {
     using C = FwdCfg<TIO, G, KD>;
     constexpr int NT = C::NT, KS = C::KS, KP = C::KP, DT = C::DT, TT = C::TT, EPC = C::EPC;
@@ -85,6 +88,7 @@ __global__ void __launch_bounds__(32, FwdCfg<TIO, G, KD>::MINB) fwd_kernel(const
     float* bsf = reinterpret_cast<float*>(smem + 2 * C::X_BYTES + 2 * C::BC_RAW);
     float* csf = bsf + (C::BF ? TT * kDS : 0);
     TIO* ys = reinterpret_cast<TIO*>(smem + 2 * C::X_BYTES + 2 * C::BC_RAW + 2 * C::BC_F32);
+    float* dsf = reinterpret_cast<float*>(smem + C::SMEM);           // FUSE only
 
     const int lane = threadIdx.x;
     const int gl = lane % G;                 // lane within the channel group
@@ -139,6 +143,15 @@ __global__ void __launch_bounds__(32, FwdCfg<TIO, G, KD>::MINB) fwd_kernel(const
     float dsum[KD];
 #pragma unroll
     for (int k = 0; k < KD; ++k) dsum[k] = 0.f;
+    // skip weights of the channels whose y this lane stores (KD == 1: its channel; KD > 1:
+    // channels [gl*KD/2, (gl+1)*KD/2) of its group)
+    constexpr int NKEEP = (KD == 1) ? 1 : KD / 2;
+    float Dkeep[NKEEP];
+#pragma unroll
+    for (int i = 0; i < NKEEP; ++i) {
+        const int cc = (KD == 1) ? c0 : c0 + gl * NKEEP + i;
+        Dkeep[i] = (FUSE && READ && p.Dskip != nullptr && d0 + cc < D) ? p.Dskip[d0 + cc] : 0.f;
+    }
     const int64_t K = p.K;
     const bool want_ckpt = (MODE != kPass1) && p.ckpt != nullptr && K > 0;
     int64_t next_ck = want_ckpt ? ((t_begin + K - 1) / K) * K : INT64_MAX;
@@ -222,6 +235,18 @@ __global__ void __launch_bounds__(32, FwdCfg<TIO, G, KD>::MINB) fwd_kernel(const
         }
         const TIO* xt = xs + buf * TT * DT;
         const TIO* dt = ds + buf * TT * DT;
+        if constexpr (FUSE) {      // delta tile as float32, through softplus when asked
+            if (p.softplus) {
+                // rows past the end stay 0 (zero-filled raw rows would give softplus(0) = ln 2,
+                // and padded steps must leave the state unchanged)
+                const int rows = int(min(int64_t(TT), t_end - (t_begin + tile * TT)));
+                for (int i = lane; i < TT * DT; i += NT)
+                    dsf[i] = (i / DT < rows) ? softplus_f32(to_f32(dt[i])) : 0.f;
+            } else {
+                for (int i = lane; i < TT * DT; i += NT) dsf[i] = to_f32(dt[i]);
+            }
+            __syncwarp();
+        }
         const int64_t t0 = t_begin + tile * TT;
         if (CKT && t0 == next_ck) {               // checkpoints fall on tile starts
             if (next_ck < t_end) store_state(p.ckpt + (next_ck / K) * p.B * D * kDS);
@@ -240,7 +265,8 @@ __global__ void __launch_bounds__(32, FwdCfg<TIO, G, KD>::MINB) fwd_kernel(const
                     next_ck += K;
                 }
                 float dl[KD], xv[KD];
-                load_vals<TIO, KD>(dt + r * DT + c0, dl);
+                if constexpr (FUSE) load_vals<float, KD>(dsf + r * DT + c0, dl);
+                else load_vals<TIO, KD>(dt + r * DT + c0, dl);
                 load_vals<TIO, KD>(xt + r * DT + c0, xv);
                 float2 bb[KP], cc[KP];
 #pragma unroll
@@ -279,7 +305,9 @@ __global__ void __launch_bounds__(32, FwdCfg<TIO, G, KD>::MINB) fwd_kernel(const
                     float v[G];
 #pragma unroll
                     for (int j = 0; j < G; ++j) v[j] = part[j][0];
-                    ys[(tt + gl) * DT + c0] = from_f32<TIO>(reduce_scatter_steps<G>(v, gl));
+                    float yv = reduce_scatter_steps<G>(v, gl);
+                    if constexpr (FUSE) yv = fmaf(Dkeep[0], to_f32(xt[(tt + gl) * DT + c0]), yv);   // skip
+                    ys[(tt + gl) * DT + c0] = from_f32<TIO>(yv);
                 } else {
                     // two lanes per channel group: lane gl keeps channels [gl*KD/2, (gl+1)*KD/2)
                     constexpr int H = KD / 2;
@@ -289,6 +317,8 @@ __global__ void __launch_bounds__(32, FwdCfg<TIO, G, KD>::MINB) fwd_kernel(const
                         const float send = gl ? part[0][i] : part[0][H + i];
                         const float keep = gl ? part[0][H + i] : part[0][i];
                         out[i] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+                        if constexpr (FUSE)                                                // skip
+                            out[i] = fmaf(Dkeep[i], to_f32(xt[tt * DT + c0 + gl * H + i]), out[i]);
                     }
                     store_vals<TIO, H>(ys + tt * DT + c0 + gl * H, out);
                 }
@@ -330,31 +360,32 @@ __global__ void __launch_bounds__(32, FwdCfg<TIO, G, KD>::MINB) fwd_kernel(const
     if (last && p.hT != nullptr) store_state(p.hT);
 }
 
-template <typename TIO, int G, int KD, bool VEC, int MODE, bool CKT>
+template <typename TIO, int G, int KD, bool VEC, int MODE, bool CKT, bool FUSE>
 cudaError_t launch_fwd_t(const FwdLaunch& L, cudaStream_t stream) {
     using C = FwdCfg<TIO, G, KD>;
-    auto kern = fwd_kernel<TIO, G, KD, VEC, MODE, CKT>;
-    if (C::SMEM > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::SMEM));
+    constexpr size_t smem = FUSE ? C::SMEM_FUSE : C::SMEM;
+    auto kern = fwd_kernel<TIO, G, KD, VEC, MODE, CKT, FUSE>;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
         if (e != cudaSuccess) return e;
     }
     unsigned gy = 1;
     if (MODE == kPass1) gy = unsigned(L.nchunk - 1);
     if (MODE == kPass2) gy = unsigned(L.nchunk);
     const dim3 grid(unsigned((L.D + C::DT - 1) / C::DT), gy, unsigned(L.B));
-    kern<<<grid, C::NT, C::SMEM, stream>>>(L);
+    kern<<<grid, C::NT, smem, stream>>>(L);
     return cudaGetLastError();
 }
 
-// All instantiations for one I/O type. Checkpoints are checked once per tile when
-// every checkpoint step is a tile start (K and the chunk length multiples of 16).
-template <typename TIO>
-cudaError_t launch_fwd_io(const FwdLaunch& L, int mode, cudaStream_t stream) {
+// All instantiations for one I/O type and fusion choice. Checkpoints are checked once per
+// tile when every checkpoint step is a tile start (K and the chunk length multiples of 16).
+template <typename TIO, bool FUSE>
+cudaError_t launch_fwd_fuse(const FwdLaunch& L, int mode, cudaStream_t stream) {
     constexpr int TT = FwdCfg<TIO, 4, 1>::TT;
     const bool ckt = L.K == 0 || (L.K % TT == 0 && (mode == kSingle || mode == kCkptOnly || L.Lc % TT == 0));
 #define SSM_FWD_CK(G_, KD_, MODE_, VEC_)                                                   \
-    return ckt ? launch_fwd_t<TIO, G_, KD_, VEC_, MODE_, true>(L, stream)                 \
-               : launch_fwd_t<TIO, G_, KD_, VEC_, MODE_, false>(L, stream)
+    return ckt ? launch_fwd_t<TIO, G_, KD_, VEC_, MODE_, true, FUSE>(L, stream)           \
+               : launch_fwd_t<TIO, G_, KD_, VEC_, MODE_, false, FUSE>(L, stream)
 #define SSM_FWD_VEC(G_, KD_, MODE_)                                                       \
     if (L.vec) { SSM_FWD_CK(G_, KD_, MODE_, true); } else { SSM_FWD_CK(G_, KD_, MODE_, false); }
     switch (mode) {
@@ -362,14 +393,20 @@ cudaError_t launch_fwd_io(const FwdLaunch& L, int mode, cudaStream_t stream) {
             if (L.G == 2) { SSM_FWD_VEC(2, 2, kSingle); }
             SSM_FWD_VEC(4, 1, kSingle);
         case kPass1:
-            if (L.vec) return launch_fwd_t<TIO, 4, 1, true, kPass1, true>(L, stream);
-            return launch_fwd_t<TIO, 4, 1, false, kPass1, true>(L, stream);
+            if (L.vec) return launch_fwd_t<TIO, 4, 1, true, kPass1, true, FUSE>(L, stream);
+            return launch_fwd_t<TIO, 4, 1, false, kPass1, true, FUSE>(L, stream);
         case kPass2: SSM_FWD_VEC(4, 1, kPass2);
         case kCkptOnly: SSM_FWD_VEC(4, 1, kCkptOnly);
         default: return cudaErrorInvalidValue;
     }
 #undef SSM_FWD_VEC
 #undef SSM_FWD_CK
+}
+
+template <typename TIO>
+cudaError_t launch_fwd_io(const FwdLaunch& L, int mode, cudaStream_t stream) {
+    const bool fuse = L.softplus || (L.Dskip != nullptr && (mode == kSingle || mode == kPass2));
+    return fuse ? launch_fwd_fuse<TIO, true>(L, mode, stream) : launch_fwd_fuse<TIO, false>(L, mode, stream);
 }
 
 }  // namespace ssm

@@ -38,6 +38,9 @@ struct FwdLaunch {
     int G;          // lane layout: 2 (2 lanes x 4 channels per lane) or 4 (4 lanes x 1 channel)
     bool vec;       // 16-byte staging allowed
     bool ckpt_only; // mode 0 without readout (checkpoint rebuild for the backward)
+    // fused prologue / epilogue (the fused kernel variants only)
+    bool softplus;       // delta holds raw values; the scan uses softplus(delta)
+    const float* Dskip;  // (D) or null: y += Dskip[d] * x
 };
 
 cudaError_t launch_fwd(const FwdLaunch& L, int mode, cudaStream_t stream);
@@ -71,6 +74,11 @@ struct BwdLaunch {
     bool det;
     float* part_gbc;     // [channel blocks][B][T][2][16]: per-CTA sums over d of gb (0) and gc (1)
     float* part_gA;      // [B * chunks][D][16]: per-CTA sums over t of gA (chunks = gridDim.z)
+    // fused prologue / epilogue (the fused kernel variants only)
+    bool softplus;       // delta holds raw values; gdelta is with respect to them
+    const float* Dskip;  // (D) or null: the forward added Dskip[d] * x to y
+    float* gDskip;       // (D), with Dskip: sum over b, t of dy * x (zeroed by the launcher)
+    float* part_gD;      // deterministic: [B * chunks][D] partials of gDskip
 };
 
 // Deterministic backward: sums of the per-CTA partials in a fixed order into gb, gc and gA.

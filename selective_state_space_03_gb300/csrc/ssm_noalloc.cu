@@ -75,7 +75,7 @@ extern "C" ssm_status ssm_scan_fwd_noalloc(const ssm_scan_desc* desc, const void
     const ssm_scan_desc& d = *desc;
     if (d.B < 0 || d.T < 0 || d.D < 0 || d.DS < 0) return SSM_ERR_INVALID_ARG;
     if (d.io != SSM_IO_F32 && d.io != SSM_IO_BF16) return SSM_ERR_INVALID_ARG;
-    if (d.ckpt_interval < 0 || (d.flags & ~SSM_SCAN_DETERMINISTIC) != 0 || d.B > 65535) return SSM_ERR_INVALID_ARG;
+    if (d.ckpt_interval < 0 || (d.flags & ~(SSM_SCAN_DETERMINISTIC | SSM_SCAN_DELTA_SOFTPLUS)) != 0 || d.B > 65535) return SSM_ERR_INVALID_ARG;
     if (d.DS != kDS) return SSM_ERR_UNSUPPORTED;
     if (d.D > kMaxD) return SSM_ERR_UNSUPPORTED;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -112,6 +112,7 @@ extern "C" ssm_status ssm_scan_fwd_noalloc(const ssm_scan_desc* desc, const void
     L.vec = (d.D * (d.io == SSM_IO_BF16 ? 2 : 4)) % 16 == 0;
     L.ckpt_only = false;
     L.G = 4;
+    L.softplus = (d.flags & SSM_SCAN_DELTA_SOFTPLUS) != 0;
     auto run = [&](int mode) {
         return d.io == SSM_IO_BF16 ? launch_fwd_bf16(L, mode, s) : launch_fwd_f32(L, mode, s);
     };

@@ -3,7 +3,8 @@
 // In deterministic mode every backward CTA writes its partial sums instead of
 // adding them atomically: for gb and gc one row of 2 x 16 values per (channel
 // block, b, t) (its sum over its channels), for gA one row of 16 values per
-// (b, chunk, d) (its sum over its steps). These kernels add the partials in
+// (b, chunk, d) (its sum over its steps), and for the skip weights' gradient one value
+// per (b, chunk, d). These kernels add the partials in
 // increasing block (resp. batch-then-chunk) order, so the result does not
 // depend on which CTA finished first. Each thread sums one 16-byte column of
 // the partials; the partial arrays are read once (HBM-bound).
@@ -43,6 +44,16 @@ __global__ void __launch_bounds__(256) reduce_gA_kernel(const float* __restrict_
     }
 }
 
+// parts [nparts][D] -> gD [D]
+__global__ void __launch_bounds__(256) reduce_gD_kernel(const float* __restrict__ parts, int64_t nparts, int64_t D,
+                                                        float* __restrict__ gD) {
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < D; i += int64_t(gridDim.x) * blockDim.x) {
+        float acc = parts[i];
+        for (int64_t k = 1; k < nparts; ++k) acc += parts[k * D + i];
+        gD[i] = acc;
+    }
+}
+
 unsigned grid_for(int64_t n4) {
     const int64_t want = (n4 + 255) / 256;
     const int64_t cap = int64_t(device_sm_count()) * 8;
@@ -57,6 +68,9 @@ cudaError_t launch_bwd_reduce(const BwdLaunch& L, int64_t nblk, int64_t nz, cuda
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     reduce_gA_kernel<<<grid_for(L.D * 4), 256, 0, stream>>>(L.part_gA, L.B * nz, L.D, L.gA);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || L.Dskip == nullptr) return e;
+    reduce_gD_kernel<<<grid_for(L.D), 256, 0, stream>>>(L.part_gD, L.B * nz, L.D, L.gDskip);
     return cudaGetLastError();
 }
 

@@ -27,6 +27,7 @@ struct StepLaunch {
     float* h;            // (B, D, 16), read and written
     void* y;             // (B, D) io
     int64_t B, D;
+    bool softplus;       // delta holds raw values
 };
 
 template <typename TIO>
@@ -39,7 +40,8 @@ __global__ void __launch_bounds__(128) step_kernel(const StepLaunch p) {
     float4 hv = make_float4(0.f, 0.f, 0.f, 0.f);
     if (valid) {
         const int64_t bb = chain / p.D, d = chain - bb * p.D;
-        const float dl = to_f32(static_cast<const TIO*>(p.delta)[chain]);
+        float dl = to_f32(static_cast<const TIO*>(p.delta)[chain]);
+        if (p.softplus) dl = softplus_f32(dl);
         const float dx = dl * to_f32(static_cast<const TIO*>(p.x)[chain]);
         float bv[4], cv[4];
         load_vals<TIO, 4>(static_cast<const TIO*>(p.b) + bb * kDS + s0, bv);
@@ -72,7 +74,7 @@ extern "C" ssm_status ssm_scan_step(const ssm_scan_desc* desc, const void* x, co
     const ssm_scan_desc& d = *desc;
     if (d.B < 0 || d.D < 0 || d.DS < 0 || d.T != 1) return SSM_ERR_INVALID_ARG;
     if (d.io != SSM_IO_F32 && d.io != SSM_IO_BF16) return SSM_ERR_INVALID_ARG;
-    if (d.ckpt_interval < 0 || (d.flags & ~SSM_SCAN_DETERMINISTIC) != 0 || d.B > 65535) return SSM_ERR_INVALID_ARG;
+    if (d.ckpt_interval < 0 || (d.flags & ~(SSM_SCAN_DETERMINISTIC | SSM_SCAN_DELTA_SOFTPLUS)) != 0 || d.B > 65535) return SSM_ERR_INVALID_ARG;
     if (d.DS != kDS || d.D > kMaxD) return SSM_ERR_UNSUPPORTED;
     if (d.B == 0 || d.D == 0) return SSM_OK;
     if (!x || !delta || !A || !b || !c || !h || !y) return SSM_ERR_INVALID_ARG;
@@ -82,7 +84,7 @@ extern "C" ssm_status ssm_scan_step(const ssm_scan_desc* desc, const void* x, co
     const int64_t threads = d.B * d.D * 4;
     const int64_t blocks = (threads + 127) / 128;
     if (blocks > int64_t(0x7fffffff)) return SSM_ERR_UNSUPPORTED;
-    StepLaunch L{x, delta, A, b, c, h, y, d.B, d.D};
+    StepLaunch L{x, delta, A, b, c, h, y, d.B, d.D, (d.flags & SSM_SCAN_DELTA_SOFTPLUS) != 0};
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (d.io == SSM_IO_BF16) {
         step_kernel<__nv_bfloat16><<<unsigned(blocks), 128, 0, s>>>(L);

@@ -170,5 +170,25 @@ def test_deterministic_flag_workspace(L):
     # without the flag the same shape needs no workspace
     assert L.ssm_scan_bwd_ckpt_workspace_bytes(ctypes.byref(desc(B=2, T=100, D=320, ckpt_interval=100))) == 0
     # unknown flag bits are rejected
-    assert bwd(L, desc(flags=2)) == 1
+    assert bwd(L, desc(flags=4)) == 1
     assert step(L, desc(T=1, flags=4)) == 1
+
+
+def test_fused_entry_point_checks(L):
+    P = ctypes.c_void_p
+    d = desc(flags=2)                                    # softplus on delta is a valid flag
+
+    def fwdf(D_skip=FAKE, y=FAKE, dd=d):
+        return L.ssm_scan_fwd_fused(ctypes.byref(dd), P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(D_skip),
+                                    P(None), P(y), P(None), P(None), P(None), 0, None)
+
+    def bwdf(D_skip=FAKE, gD=FAKE, dd=d):
+        g = [P(FAKE)] * 6
+        return L.ssm_scan_bwd_fused(ctypes.byref(dd), P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(D_skip),
+                                    P(None), P(FAKE), P(FAKE), P(None), *g, P(gD), P(None), 0, None)
+
+    assert fwdf(D_skip=FAKE + 4) == 3
+    assert fwdf(y=None) == 1
+    assert bwdf(gD=None) == 1                            # the skip weights' gradient is required
+    assert bwdf(gD=FAKE + 8) == 3
+    assert bwdf(dd=desc(flags=8)) == 1

@@ -1,0 +1,136 @@
+"""GPU parity of the fused prologue / epilogue against the oracle's fused functions.
+
+SSM_SCAN_DELTA_SOFTPLUS (delta given raw, the scan uses softplus(delta)) and the
+skip y += D_skip * x (ssm_scan_fwd_fused / ssm_scan_bwd_fused, with gD_skip)
+are checked through every schedule that applies them: the one-pass forward in
+both lane layouts, the chunked forward, the checkpoint rebuild, both backward
+layouts, the chunk-parallel backward, the deterministic sums and the decode
+step. Tolerances as for the plain scan: float32 I/O 1e-4 (y, hT) and 1e-3
+(gradients), bf16 I/O 1e-2, as max |got - ref| / (1 + |ref|).
+"""
+import contextlib
+import os
+
+import numpy as np
+import pytest
+
+import gen
+import oracle
+from gpu_util import GRADS, assert_close, dev_inputs, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _setup():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from selective_state_space_03_gb300 import build
+    build.build()
+    torch.cuda.set_device(0)
+
+
+def ssm():
+    import selective_state_space_03_gb300 as m
+    return m
+
+
+@contextlib.contextmanager
+def forced(**env):
+    """Set layout overrides of the library (read at each call) for the block."""
+    old = {k: os.environ.get(k) for k in env}
+    for k, v in env.items():
+        if v is not None:
+            os.environ[k] = str(v)
+    try:
+        yield
+    finally:
+        for k, v in env.items():
+            if v is None:
+                continue
+            if old[k] is None:
+                del os.environ[k]
+            else:
+                os.environ[k] = old[k]
+
+
+def fused_case(w, K, softplus=True, skip=True, chunk_len=0, lanes=None, kd=None, tpar=None, det=False,
+               rebuild=False, seed=0):
+    import torch
+    inp = gen.make_inputs(w, seed=seed, with_grad_inputs=True, with_ghT=True, raw_delta=softplus,
+                          with_skip=skip)
+    t = dev_inputs(inp)
+    Ds = to_dev(inp["D_skip"]) if skip else None
+    with forced(SSM_SCAN_FORCE_LANES=lanes):
+        y, hT, ckpt = ssm().ssm_scan_fwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], ckpt_interval=K,
+                                         chunk_len=chunk_len, D_skip=Ds, delta_softplus=softplus)
+    torch.cuda.synchronize()
+    ref = oracle.fwd_fused(inp["x"], inp["delta"], inp["A"], inp["b"], inp["c"], inp["h0"], inp.get("D_skip"),
+                           delta_softplus=softplus, ckpt_interval=K)
+    assert_close(to_host(y), ref["y"], w.io, "fwd", "y")
+    assert_close(to_host(hT), ref["hT"], w.io, "fwd", "hT")
+    if K > 0:
+        assert_close(to_host(ckpt), ref["ckpt"], w.io, "fwd", "ckpt")
+    with forced(SSM_SCAN_FORCE_BWD_KD=kd, SSM_SCAN_FORCE_BWD_TPAR=tpar):
+        g = ssm().ssm_scan_bwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], None if rebuild else ckpt,
+                               t["dy"], t["ghT"], ckpt_interval=K, D_skip=Ds, delta_softplus=softplus,
+                               deterministic=det)
+    torch.cuda.synchronize()
+    gref = oracle.bwd_fused(inp["x"], inp["delta"], inp["A"], inp["b"], inp["c"], inp["h0"], inp["dy"],
+                            inp["ghT"], inp.get("D_skip"), delta_softplus=softplus)
+    for k in GRADS + (("gD_skip",) if skip else ()):
+        assert_close(to_host(g[k]), gref[k], w.io, "grad", k)
+    return g
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("softplus,skip", [(True, True), (True, False), (False, True)])
+def test_fused_one_pass_and_backward(io, softplus, skip):
+    fused_case(gen.workload(2, B=3, T=200, D=72, io=io, h0_std=0.1), K=64, softplus=softplus, skip=skip)
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_fused_two_lane_forward_and_two_channel_backward(io):
+    fused_case(gen.workload(2, B=2, T=150, D=136, io=io, h0_std=0.1), K=32, lanes=2, kd=2, tpar=0)
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_fused_chunked_forward_chunk_parallel_backward(io):
+    fused_case(gen.workload(2, B=2, T=230, D=40, io=io, h0_std=0.1), K=50, chunk_len=50, kd=1, tpar=1)
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_fused_unaligned_channels_and_rebuild(io):
+    D = 37 if io == "f32" else 20
+    fused_case(gen.workload(2, B=2, T=77, D=D, io=io, h0_std=0.1), K=24, rebuild=True)
+
+
+@pytest.mark.parametrize("layout", [dict(kd=1, tpar=0), dict(kd=2, tpar=0), dict(kd=1, tpar=1)])
+def test_fused_deterministic(layout):
+    import torch
+    w = gen.workload(2, B=3, T=160, D=200, io="bf16", h0_std=0.1)
+    g1 = fused_case(w, K=64, det=True, **layout)
+    g2 = fused_case(w, K=64, det=True, **layout)
+    for k in GRADS + ("gD_skip",):
+        assert torch.equal(g1[k], g2[k]), k
+
+
+def test_fused_workload5_shape_reduced():
+    fused_case(gen.workload(5, B=2, T=600, D=264), K=256)
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_decode_step_with_softplus(io):
+    import torch
+    w = gen.workload(2, B=3, T=12, D=72, io=io, h0_std=0.1)
+    inp = gen.make_inputs(w, seed=4, raw_delta=True)
+    t = dev_inputs(inp)
+    h = t["h0"].clone()
+    ys = [ssm().ssm_scan_step(t["x"][:, k].contiguous(), t["delta"][:, k].contiguous(), t["A"],
+                              t["b"][:, k].contiguous(), t["c"][:, k].contiguous(), h, delta_softplus=True)
+          for k in range(w.T)]
+    torch.cuda.synchronize()
+    ref = oracle.fwd_fused(inp["x"], inp["delta"], inp["A"], inp["b"], inp["c"], inp["h0"], delta_softplus=True)
+    assert_close(np.stack([to_host(v) for v in ys], axis=1), ref["y"], io, "fwd", "y")
+    assert_close(to_host(h), ref["hT"], io, "fwd", "hT")

@@ -75,3 +75,18 @@ def test_noalloc_rejects_problems_beyond_its_scratch(L):
     st = L.ssm_scan_fwd_noalloc(ctypes.byref(desc), fake, fake, fake, fake, fake, None, fake, None, None, None)
     assert st == 4
     assert np.int64(2 * 99 * 8192 * 68) > (8 << 20)
+
+
+def test_noalloc_with_softplus_on_delta(L):
+    import torch
+    import oracle
+    import selective_state_space_03_gb300 as ssm
+    w = gen.workload(2, B=2, T=300, D=48, h0_std=0.1)
+    inp = gen.make_inputs(w, seed=6, with_grad_inputs=False, raw_delta=True)
+    t = dev_inputs(inp)
+    y, hT, _ = ssm.ssm_scan_fwd_noalloc(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], chunk_len=64,
+                                        delta_softplus=True)
+    torch.cuda.synchronize()
+    ref = oracle.fwd_fused(inp["x"], inp["delta"], inp["A"], inp["b"], inp["c"], inp["h0"], delta_softplus=True)
+    assert_close(to_host(y), ref["y"], "f32", "fwd", "y")
+    assert_close(to_host(hT), ref["hT"], "f32", "fwd", "hT")
