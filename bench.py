@@ -266,6 +266,36 @@ def run_ours(args, rank, world, local_rank):
     bwd_det_ms = d0.elapsed_time(d1) / 5
     del det_ws, g_det
 
+    # the fused variant: softplus applied to delta inside the kernels and the skip y += D x
+    # (delta's values are reused as the raw input: the cost does not depend on them)
+    Dsk = torch.ones(w.D, dtype=torch.float32, device=dev)
+    y_f, hT_f, ck_f = torch.empty_like(y), torch.empty_like(hT), torch.empty_like(ckpt)
+    g_f = {k: torch.empty_like(v) for k, v in grads.items()}
+    g_f["gD_skip"] = torch.empty_like(Dsk)
+
+    def fwd_fused():
+        ssm.ssm_scan_fwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], ckpt_interval=K, y=y_f, hT=hT_f,
+                         ckpt=ck_f, D_skip=Dsk, delta_softplus=True)
+
+    def bwd_fused():
+        ssm.ssm_scan_bwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], ck_f, t["dy"], ckpt_interval=K,
+                         grads=g_f, D_skip=Dsk, delta_softplus=True)
+
+    fwd_fused()
+    bwd_fused()
+    torch.cuda.synchronize()
+    f0, f1, f2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    f0.record(stream)
+    for _ in range(5):
+        fwd_fused()
+    f1.record(stream)
+    for _ in range(5):
+        bwd_fused()
+    f2.record(stream)
+    torch.cuda.synchronize()
+    fused_fwd_ms, fused_bwd_ms = f0.elapsed_time(f1) / 5, f1.elapsed_time(f2) / 5
+    del y_f, hT_f, ck_f, g_f
+
     # ---- end to end through the public API with host buffers. Every step copies its inputs
     # from pinned host memory and all its outputs (y, hT and the six gradients) back; the steps
     # are pipelined over three streams (copy in, compute, copy out) with two device buffer sets,
@@ -363,6 +393,7 @@ def run_ours(args, rank, world, local_rank):
                    "state_and_grads": "f32", "ckpt_interval": K, "l2": "inputs larger than L2 (no flush)",
                    "parallelism": f"replicas x{world}"},
         "kernels": {"fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "bwd_deterministic_ms": bwd_det_ms,
+                    "fused_softplus_skip_fwd_ms": fused_fwd_ms, "fused_softplus_skip_bwd_ms": fused_bwd_ms,
                     "fwd_elem_per_s": el / (fwd_ms / 1e3), "bwd_elem_per_s": el / (bwd_ms / 1e3),
                     "fwd_hbm_gbs": fwd_bytes / (fwd_ms / 1e3) / 1e9, "bwd_hbm_gbs": bwd_bytes / (bwd_ms / 1e3) / 1e9,
                     "fwd_hbm_frac": fwd_bytes / (fwd_ms / 1e3) / 1e9 / hbm_peak,
