@@ -51,6 +51,13 @@ def load_peaks():
         return 6800.0, "fallback"
 
 
+# DRAM bytes (read + write) of one bwd2_kernel launch at workload 5, from the ncu capture
+# summarised in profiles/bwd2_kernel_B16_T512_D5120.md: 683.5 MB at T = 512, and traffic
+# grows with the number of steps, so 4 x that at T = 2048. Reset to None whenever the
+# kernel changes until it is captured again.
+BWD2_TRAFFIC = {"bytes_per_launch": 4 * 683.456e6,
+                "source": "ncu dram__bytes_read+write of bwd2_kernel at T=512 (683.5 MB) x 4 steps ratio"}
+
 # ---------------------------------------------------------------- algorithmic work per element
 
 def compulsory_bytes(w, direction):
@@ -245,6 +252,12 @@ def run_ours(args, rank, world, local_rank):
     ms_per_step = total_ms / args.steps
     value = job_throughput(el, args.steps, world, total_ms)
 
+    if args.step_only:
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "value": value, "unit": UNIT, "ms_per_step": ms_per_step,
+                              "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "step_only": True}), flush=True)
+        return
+
     # the same backward with fixed-order (bitwise reproducible) gb, gc, gA sums
     ddesc = ssm.make_desc(w.B, w.T, w.D, w.DS, ssm.SSM_IO_BF16, K, 0, ssm.SSM_SCAN_DETERMINISTIC)
     det_ws = torch.empty(ssm.lib().ssm_scan_bwd_ckpt_workspace_bytes(ctypes.byref(ddesc)), dtype=torch.uint8,
@@ -399,9 +412,10 @@ def run_ours(args, rank, world, local_rank):
                     "fwd_hbm_frac": fwd_bytes / (fwd_ms / 1e3) / 1e9 / hbm_peak,
                     "bwd_hbm_frac": bwd_bytes / (bwd_ms / 1e3) / 1e9 / hbm_peak,
                     "fwd_ex2_frac": fwd_ex2 / ex2_peak},
-        "roofline": {"kernel": "bwd_kernel (reverse sweep with recompute)", "bound": "alu",
+        "roofline": {"kernel": "bwd2_kernel (reverse sweep with recompute, two channels per lane)", "bound": "alu",
                      "achieved": bwd_ops / 1e12, "peak": fp32_peak / 1e12, "unit": "TFLOP/s",
-                     "frac": bwd_ops / fp32_peak, "traffic": None,
+                     "frac": bwd_ops / fp32_peak, "traffic": BWD2_TRAFFIC["bytes_per_launch"],
+                     "traffic_source": BWD2_TRAFFIC["source"],
                      "basis": f"{BWD_OPS_PER_ELEM} FP32-pipe ops/element x {el} elements per launch; peak = "
                               f"{FP32_PER_SM_CLK} lanes x SMs x median SM clock {sm_mhz:.0f} MHz",
                      "hbm": {"achieved": bwd_bytes / (bwd_ms / 1e3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
@@ -611,6 +625,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extra", action="store_true", help="skip the other two workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle timing")
+    ap.add_argument("--step-only", action="store_true",
+                    help="time only the forward+backward steps (no other measurements), e.g. under a profiler")
     ap.add_argument("--profile", action="store_true",
                     help="run one warm-up and one forward+backward for a profiler, no timing")
     ap.add_argument("--workload", type=int, default=0, help="with --profile: workload 1-5 instead of 5")
