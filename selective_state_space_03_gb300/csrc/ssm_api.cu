@@ -1,4 +1,5 @@
 // C ABI of libssm_scan.so: argument checks, schedule choice and launches.
+#include <algorithm>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -75,7 +76,10 @@ FwdPlan plan_fwd(const ssm_scan_desc& d) {
         Lc = d.chunk_len;
     } else if (d.chunk_len == 0 && chains * 4 * 2 < want && d.T >= 256) {
         chunked = true;
-        const int64_t nch = cdiv(want, chains * 4);
+        // chunks for about 14 resident warps per SM in pass 2 (rounded down: on workload 4's
+        // 4096-step calls 8 chunks of 512 ran 9 % faster than 10 of 416, and 16 of 256
+        // 3 % slower: fewer chunks also shorten pass 1)
+        const int64_t nch = std::max<int64_t>(2, int64_t(device_sm_count()) * 448 / (chains * 4));
         Lc = cdiv(cdiv(d.T, nch), 32) * 32;
         if (Lc < 64) Lc = 64;
     }

@@ -21,6 +21,7 @@
 //    GPU (other streams, other host threads) race on it and must be ordered by
 //    the caller. Pass 1 overwrites every entry pass 2 reads, so nothing in the
 //    array needs clearing between calls.
+#include <algorithm>
 #include <mutex>
 
 #include "ssm_internal.h"
@@ -94,11 +95,11 @@ extern "C" ssm_status ssm_scan_fwd_noalloc(const ssm_scan_desc* desc, const void
         return SSM_OK;
     }
 
-    // chunk length: the caller's, else enough chunks for ~16 resident warps per SM
+    // chunk length: the caller's, else chunks for about 14 resident warps per SM (the rule
+    // ssm_scan_fwd uses for its chunked schedule)
     int64_t Lc = d.chunk_len;
     if (Lc <= 0) {
-        const int64_t want = int64_t(device_sm_count()) * 512;
-        const int64_t nch = cdiv64(want, d.B * d.D * 4);
+        const int64_t nch = std::max<int64_t>(2, int64_t(device_sm_count()) * 448 / (d.B * d.D * 4));
         Lc = cdiv64(cdiv64(d.T, nch), 32) * 32;
         if (Lc < 64) Lc = 64;
     }
