@@ -60,13 +60,14 @@ bool vec_ok(const ssm_scan_desc& d) { return (d.D * io_size(d)) % 16 == 0; }
 struct FwdPlan {
     int mode;        // kSingle (0) or chunked (2, meaning pass 1 + pass 2)
     int G;
+    int kd;          // channels per lane of the G = 4 layout (1 or 2)
     int64_t Lc;
     int64_t nchunk;
     size_t ws_S, ws_Sd;   // byte sizes of the two workspace arrays
 };
 
 FwdPlan plan_fwd(const ssm_scan_desc& d) {
-    FwdPlan P{0, 4, d.T, 1, 0, 0};
+    FwdPlan P{0, 4, 1, d.T, 1, 0, 0};
     const int64_t chains = d.B * d.D;
     const int64_t want = int64_t(device_sm_count()) * 512;   // ~16 resident warps per SM
     bool chunked = false;
@@ -92,13 +93,23 @@ FwdPlan plan_fwd(const ssm_scan_desc& d) {
         P.ws_S = align_up(size_t(d.B) * size_t(P.nchunk - 1) * size_t(d.D) * kDS * 4);
         P.ws_Sd = align_up(size_t(d.B) * size_t(P.nchunk - 1) * size_t(d.D) * 4);
     } else {
-        // 2 lanes x 4 channels per lane (64 channels per warp) when that still gives
-        // ~6 warps per SM; otherwise 4 lanes x 1 channel (8 channels per warp)
-        P.G = chains >= int64_t(device_sm_count()) * 6 * 64 ? 2 : 4;
-        // testing aid: force the lane layout of the one-pass schedule (2 or 4)
+        // Lane layout: the most channels per warp (fewest lanes re-reading each b, c value
+        // from shared memory) that still keeps enough warps resident: 2 lanes per chain x 2
+        // channels per lane (32 channels per warp) from about 12 warps per SM, 4 lanes x 2
+        // channels (16 per warp) from about 4 warps per SM, else 4 lanes x 1 channel (8).
+        const int64_t sms = device_sm_count();
+        P.G = chains >= sms * 12 * 32 ? 2 : 4;
+        P.kd = (P.G == 4 && chains >= sms * 4 * 16) ? 2 : 1;
+        // testing aids: force the layout ("2x2", "4x2", "4x1"; the older SSM_SCAN_FORCE_LANES
+        // takes 2 for 2x2 and 4 for 4x1)
         if (const char* env = std::getenv("SSM_SCAN_FORCE_LANES")) {
             const int g = std::atoi(env);
-            if (g == 2 || g == 4) P.G = g;
+            if (g == 2 || g == 4) { P.G = g; P.kd = g == 2 ? 2 : 1; }
+        }
+        if (const char* env = std::getenv("SSM_SCAN_FORCE_FWD_LAYOUT")) {
+            if (std::strcmp(env, "2x2") == 0) { P.G = 2; P.kd = 2; }
+            if (std::strcmp(env, "4x2") == 0) { P.G = 4; P.kd = 2; }
+            if (std::strcmp(env, "4x1") == 0) { P.G = 4; P.kd = 1; }
         }
     }
     return P;
@@ -251,6 +262,7 @@ ssm_status ssm_scan_fwd_fused(const ssm_scan_desc* desc, const void* x, const vo
     L.vec = vec_ok(d);
     L.ckpt_only = false;
     L.G = P.G;
+    L.kd = P.kd;
     L.softplus = (d.flags & SSM_SCAN_DELTA_SOFTPLUS) != 0;
     L.Dskip = D_skip;
     cudaError_t e;

@@ -201,4 +201,26 @@ __device__ __forceinline__ float reduce_scatter_steps(const float (&v)[G], int g
     }
 }
 
+// Eight values per lane summed over the 4 lanes of a group (gl = lane & 3): lane gl
+// returns the totals of entries 2 gl and 2 gl + 1 (two reduce-scatter stages).
+__device__ __forceinline__ float2 reduce_scatter8_over4(const float (&v)[8], int gl) {
+    const bool hi2 = gl & 2;
+    float w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float send = hi2 ? v[i] : v[i + 4];
+        const float keep = hi2 ? v[i + 4] : v[i];
+        w[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+    }
+    const bool hi1 = gl & 1;
+    float u[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const float send = hi1 ? w[i] : w[i + 2];
+        const float keep = hi1 ? w[i + 2] : w[i];
+        u[i] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+    }
+    return make_float2(u[0], u[1]);
+}
+
 }  // namespace ssm

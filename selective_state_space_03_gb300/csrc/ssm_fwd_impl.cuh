@@ -70,7 +70,7 @@ struct FwdCfg {
     static constexpr size_t SMEM_FUSE = SMEM + DSF_BYTES;
     // registers: keep enough warps resident for the whole grid of the largest shapes
     static constexpr int MINB = (KD == 2) ? 20 : 1;
-    static_assert(KD == 1 || G == 2, "multi-channel lanes are built with 2 lanes per channel");
+    static_assert(KD == 1 || (KD == 2 && (G == 2 || G == 4)), "layouts: (4,1), (4,2), (2,2)");
     static_assert(X_CPR >= 1 && DT % EPC == 0, "tile rows must be whole 16-byte chunks");
 };
 
@@ -143,13 +143,15 @@ __global__ void __launch_bounds__(32, FwdCfg<TIO, G, KD>::MINB) fwd_kernel(const
     float dsum[KD];
 #pragma unroll
     for (int k = 0; k < KD; ++k) dsum[k] = 0.f;
-    // skip weights of the channels whose y this lane stores (KD == 1: its channel; KD > 1:
-    // channels [gl*KD/2, (gl+1)*KD/2) of its group)
-    constexpr int NKEEP = (KD == 1) ? 1 : KD / 2;
+    // Readout: with G = 4 the lanes of a chain group each finish one step of every G steps,
+    // for all KD channels; with G = 2 each finishes KD / 2 of the channels, every step.
+    constexpr bool BY_STEP = (G == 4);
+    // skip weights of the channels whose y this lane stores
+    constexpr int NKEEP = BY_STEP ? KD : KD / 2;
     float Dkeep[NKEEP];
 #pragma unroll
     for (int i = 0; i < NKEEP; ++i) {
-        const int cc = (KD == 1) ? c0 : c0 + gl * NKEEP + i;
+        const int cc = BY_STEP ? c0 + i : c0 + gl * NKEEP + i;
         Dkeep[i] = (FUSE && READ && p.Dskip != nullptr && d0 + cc < D) ? p.Dskip[d0 + cc] : 0.f;
     }
     const int64_t K = p.K;
@@ -252,7 +254,7 @@ __global__ void __launch_bounds__(32, FwdCfg<TIO, G, KD>::MINB) fwd_kernel(const
             if (next_ck < t_end) store_state(p.ckpt + (next_ck / K) * p.B * D * kDS);
             next_ck += K;
         }
-        constexpr int RG = (KD == 1) ? G : 1;   // steps per readout group
+        constexpr int RG = BY_STEP ? G : 1;     // steps per readout group
 
 #pragma unroll
         for (int tt = 0; tt < TT; tt += RG) {
@@ -301,13 +303,26 @@ __global__ void __launch_bounds__(32, FwdCfg<TIO, G, KD>::MINB) fwd_kernel(const
                 }
             }
             if (READ) {
-                if constexpr (KD == 1) {
+                if constexpr (BY_STEP && KD == 1) {
                     float v[G];
 #pragma unroll
                     for (int j = 0; j < G; ++j) v[j] = part[j][0];
                     float yv = reduce_scatter_steps<G>(v, gl);
                     if constexpr (FUSE) yv = fmaf(Dkeep[0], to_f32(xt[(tt + gl) * DT + c0]), yv);   // skip
                     ys[(tt + gl) * DT + c0] = from_f32<TIO>(yv);
+                } else if constexpr (BY_STEP) {
+                    // 4 steps x 2 channels over the 4 lanes: lane gl takes step tt + gl of both
+                    float v[8];
+#pragma unroll
+                    for (int j = 0; j < G; ++j) { v[2 * j] = part[j][0]; v[2 * j + 1] = part[j][1]; }
+                    const float2 r2 = reduce_scatter8_over4(v, gl);
+                    float out[2] = {r2.x, r2.y};
+                    if constexpr (FUSE) {                                                  // skip
+#pragma unroll
+                        for (int k = 0; k < 2; ++k)
+                            out[k] = fmaf(Dkeep[k], to_f32(xt[(tt + gl) * DT + c0 + k]), out[k]);
+                    }
+                    store_vals<TIO, 2>(ys + (tt + gl) * DT + c0, out);
                 } else {
                     // two lanes per channel group: lane gl keeps channels [gl*KD/2, (gl+1)*KD/2)
                     constexpr int H = KD / 2;
@@ -391,6 +406,7 @@ cudaError_t launch_fwd_fuse(const FwdLaunch& L, int mode, cudaStream_t stream) {
     switch (mode) {
         case kSingle:
             if (L.G == 2) { SSM_FWD_VEC(2, 2, kSingle); }
+            if (L.kd == 2) { SSM_FWD_VEC(4, 2, kSingle); }
             SSM_FWD_VEC(4, 1, kSingle);
         case kPass1:
             if (L.vec) return launch_fwd_t<TIO, 4, 1, true, kPass1, true, FUSE>(L, stream);

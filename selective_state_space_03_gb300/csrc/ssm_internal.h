@@ -35,7 +35,8 @@ struct FwdLaunch {
     int64_t Lc;     // chunk length (chunked modes; T in mode 0)
     int64_t nchunk; // number of chunks (1 in mode 0)
     IO io;
-    int G;          // lane layout: 2 (2 lanes x 4 channels per lane) or 4 (4 lanes x 1 channel)
+    int G;          // lane layout: 2 (2 lanes per chain x 2 channels per lane) or 4 (4 lanes per chain)
+    int kd;         // with G = 4: channels per lane, 1 or 2 (one-pass schedule only)
     bool vec;       // 16-byte staging allowed
     bool ckpt_only; // mode 0 without readout (checkpoint rebuild for the backward)
     // fused prologue / epilogue (the fused kernel variants only)

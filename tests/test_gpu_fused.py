@@ -96,6 +96,12 @@ def test_fused_two_lane_forward_and_two_channel_backward(io):
 
 
 @pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_fused_four_lane_two_channel_forward(io):
+    with forced(SSM_SCAN_FORCE_FWD_LAYOUT="4x2"):
+        fused_case(gen.workload(2, B=2, T=150, D=72, io=io, h0_std=0.1), K=32)
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
 def test_fused_chunked_forward_chunk_parallel_backward(io):
     fused_case(gen.workload(2, B=2, T=230, D=40, io=io, h0_std=0.1), K=50, chunk_len=50, kd=1, tpar=1)
 

@@ -52,11 +52,11 @@ def forced(var, value):
 
 
 def run_case(w, K, chunk_len=0, seed=0, ghT=False, bwd=True, lanes=None, ckpt_to_bwd=True, bwd_kd=None,
-             bwd_tpar=None, bwd_workspace=None, deterministic=False):
+             bwd_tpar=None, bwd_workspace=None, deterministic=False, fwd_layout=None):
     import torch
     inp = gen.make_inputs(w, seed=seed, with_grad_inputs=bwd, with_ghT=ghT)
     t = dev_inputs(inp)
-    with forced("SSM_SCAN_FORCE_LANES", lanes):
+    with forced("SSM_SCAN_FORCE_LANES", lanes), forced("SSM_SCAN_FORCE_FWD_LAYOUT", fwd_layout):
         y, hT, ckpt = ssm().ssm_scan_fwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], ckpt_interval=K,
                                          chunk_len=chunk_len)
     torch.cuda.synchronize()
@@ -97,6 +97,7 @@ def test_workload2_one_pass_schedule():
 
 def test_workload3_shape_reduced_bf16():
     run_case(gen.workload(3, B=2, T=300, D=200), K=64)
+    run_case(gen.workload(3, B=2, T=300, D=200), K=64, fwd_layout="4x2", bwd=False)
 
 
 def test_workload5_shape_reduced_bf16():
@@ -104,9 +105,11 @@ def test_workload5_shape_reduced_bf16():
 
 
 @pytest.mark.parametrize("io", ["f32", "bf16"])
-@pytest.mark.parametrize("lanes", [2, 4])
-def test_lanes_per_chain_variants(io, lanes):
-    run_case(gen.workload(1, B=3, T=100, D=72, io=io), K=32, chunk_len=-1, lanes=lanes, bwd=False)
+@pytest.mark.parametrize("layout", ["2x2", "4x2", "4x1"])
+def test_forward_lane_layouts(io, layout):
+    # D = 72 leaves a partial last CTA in every layout (32, 16, 8 channels per warp)
+    run_case(gen.workload(1, B=3, T=100, D=72, io=io), K=32, chunk_len=-1, fwd_layout=layout, bwd=False)
+    run_case(gen.workload(1, B=2, T=37, D=50, io=io), K=16, chunk_len=-1, fwd_layout=layout, bwd=False)
 
 
 @pytest.mark.parametrize("io", ["f32", "bf16"])
@@ -170,6 +173,8 @@ def test_unaligned_channel_count(io, bwd_kd):
     D = 37 if io == "f32" else 20
     run_case(gen.workload(2, B=2, T=77, D=D, io=io, h0_std=0.1), K=24, ghT=True, bwd_kd=bwd_kd)
     if bwd_kd == 2:
+        run_case(gen.workload(2, B=2, T=77, D=D, io=io, h0_std=0.1), K=24, chunk_len=-1, fwd_layout="4x2",
+                 bwd=False)
         return
     run_case(gen.workload(2, B=2, T=77, D=D, io=io, h0_std=0.1), K=24, chunk_len=20, bwd=False)
     run_case(gen.workload(2, B=2, T=77, D=D, io=io, h0_std=0.1), K=24, chunk_len=-1, lanes=2, bwd=False)
