@@ -68,6 +68,7 @@ template <typename TIO, bool VEC, bool FUSE>
 __global__ void __launch_bounds__(128, 3) bwd2_kernel(const BwdLaunch p) {
     using C = Bwd2Cfg<TIO>;
     constexpr int NT = C::NT, KS = C::KS, NP = C::NP, DT = C::DT, LS = C::LS, EPC = C::EPC;
+    constexpr int KP = KS / 2;                  // state pairs per lane and channel
     constexpr int HS = int(C::TMEM_H_STEP);
 
     extern __shared__ __align__(16) unsigned char smem[];
@@ -109,7 +110,10 @@ __global__ void __launch_bounds__(128, 3) bwd2_kernel(const BwdLaunch p) {
     float Dk[2], skip_acc[2] = {0.f, 0.f};       // skip weights, sums of dy x (fused variant)
 #pragma unroll
     for (int k = 0; k < 2; ++k) Dk[k] = (FUSE && valid[k] && p.Dskip != nullptr) ? p.Dskip[dch[k]] : 0.f;
-    float A2[2][KS], gcar[2][KS], gAacc[2][KS];
+    // Per-state values are kept as pairs of neighbouring states (float2), so that the
+    // arithmetic runs as packed f32x2 operations: on sm_103a these issue fewer instructions
+    // per element than scalar ones (measured on the forward: 7 % faster).
+    float2 A2[2][KP], gcar[2][KP], gAacc[2][KP];
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
         float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f), g4 = a4;
@@ -117,13 +121,11 @@ __global__ void __launch_bounds__(128, 3) bwd2_kernel(const BwdLaunch p) {
             a4 = *reinterpret_cast<const float4*>(p.A + dch[k] * kDS + s0);
             if (p.ghT != nullptr) g4 = *reinterpret_cast<const float4*>(p.ghT + (b * D + dch[k]) * kDS + s0);
         }
-        const float av[4] = {a4.x, a4.y, a4.z, a4.w}, gv[4] = {g4.x, g4.y, g4.z, g4.w};
-#pragma unroll
-        for (int s = 0; s < KS; ++s) {
-            A2[k][s] = av[s] * kLog2e;
-            gcar[k][s] = gv[s];
-            gAacc[k][s] = 0.f;
-        }
+        A2[k][0] = make_float2(a4.x * kLog2e, a4.y * kLog2e);
+        A2[k][1] = make_float2(a4.z * kLog2e, a4.w * kLog2e);
+        gcar[k][0] = make_float2(g4.x, g4.y);
+        gcar[k][1] = make_float2(g4.z, g4.w);
+        gAacc[k][0] = gAacc[k][1] = make_float2(0.f, 0.f);
     }
 
     // level-3 window in tensor memory: this warp's 32 lanes x 128 columns
@@ -254,17 +256,30 @@ __global__ void __launch_bounds__(128, 3) bwd2_kernel(const BwdLaunch p) {
 #pragma unroll
                 for (int s = 0; s < KS; ++s) { hlast[s] = h[0][s]; hlast[KS + s] = h[1][s]; }
             }
+            float2 hp2[2][KP];
+#pragma unroll
+            for (int k = 0; k < 2; ++k)
+#pragma unroll
+                for (int q = 0; q < KP; ++q) hp2[k][q] = make_float2(h[k][2 * q], h[k][2 * q + 1]);
 #pragma unroll 4
             for (int r = 0; r < LS; ++r) {
                 const float4 v = conv1[r * NP + pc];                                   // d0, d0 x0, d1, d1 x1
                 const float4 b4 = *reinterpret_cast<const float4*>(bf + r * kDS + s0);
-                const float bb[4] = {b4.x, b4.y, b4.z, b4.w};
+                const float2 bp[KP] = {make_float2(b4.x, b4.y), make_float2(b4.z, b4.w)};
+                const float2 dl2[2] = {make_float2(v.x, v.x), make_float2(v.z, v.z)};
+                const float2 dx2[2] = {make_float2(v.y, v.y), make_float2(v.w, v.w)};
 #pragma unroll
-                for (int s = 0; s < KS; ++s) {
-                    h[0][s] = fmaf(ex2(v.x * A2[0][s]), h[0][s], v.y * bb[s]);
-                    h[1][s] = fmaf(ex2(v.z * A2[1][s]), h[1][s], v.w * bb[s]);
-                }
+                for (int k = 0; k < 2; ++k)
+#pragma unroll
+                    for (int q = 0; q < KP; ++q) {
+                        const float2 e = __fmul2_rn(dl2[k], A2[k][q]);
+                        hp2[k][q] = __ffma2_rn(make_float2(ex2(e.x), ex2(e.y)), hp2[k][q], __fmul2_rn(dx2[k], bp[q]));
+                    }
             }
+#pragma unroll
+            for (int k = 0; k < 2; ++k)
+#pragma unroll
+                for (int q = 0; q < KP; ++q) { h[k][2 * q] = hp2[k][q].x; h[k][2 * q + 1] = hp2[k][q].y; }
         }
 
         // ---- reverse over the sub-chunks
@@ -302,20 +317,28 @@ __global__ void __launch_bounds__(128, 3) bwd2_kernel(const BwdLaunch p) {
 
             // level 3: states of this sub-chunk into the window (8 columns per step)
             {
-                float hc[2 * KS];
+                float2 hc[2][KP];
 #pragma unroll
-                for (int e = 0; e < 2 * KS; ++e) hc[e] = hs[e];
+                for (int k = 0; k < 2; ++k)
+#pragma unroll
+                    for (int q = 0; q < KP; ++q) hc[k][q] = make_float2(hs[k * KS + 2 * q], hs[k * KS + 2 * q + 1]);
 #pragma unroll
                 for (int r = 0; r < LS; ++r) {
                     const float4 v = conv1[r * NP + pc];
                     const float4 b4 = *reinterpret_cast<const float4*>(bf + r * kDS + s0);
-                    const float bb[4] = {b4.x, b4.y, b4.z, b4.w};
+                    const float2 bp[KP] = {make_float2(b4.x, b4.y), make_float2(b4.z, b4.w)};
+                    const float2 dl2[2] = {make_float2(v.x, v.x), make_float2(v.z, v.z)};
+                    const float2 dx2[2] = {make_float2(v.y, v.y), make_float2(v.w, v.w)};
 #pragma unroll
-                    for (int s = 0; s < KS; ++s) {
-                        hc[s] = fmaf(ex2(v.x * A2[0][s]), hc[s], v.y * bb[s]);
-                        hc[KS + s] = fmaf(ex2(v.z * A2[1][s]), hc[KS + s], v.w * bb[s]);
-                    }
-                    tmem_st8(tw + uint32_t(r * HS), hc);
+                    for (int k = 0; k < 2; ++k)
+#pragma unroll
+                        for (int q = 0; q < KP; ++q) {
+                            const float2 e = __fmul2_rn(dl2[k], A2[k][q]);
+                            hc[k][q] = __ffma2_rn(make_float2(ex2(e.x), ex2(e.y)), hc[k][q], __fmul2_rn(dx2[k], bp[q]));
+                        }
+                    const float hv[8] = {hc[0][0].x, hc[0][0].y, hc[0][1].x, hc[0][1].y,
+                                         hc[1][0].x, hc[1][0].y, hc[1][1].x, hc[1][1].y};
+                    tmem_st8(tw + uint32_t(r * HS), hv);
                 }
                 tmem_wait_st();
             }
@@ -341,34 +364,42 @@ __global__ void __launch_bounds__(128, 3) bwd2_kernel(const BwdLaunch p) {
                     const float2 dyv = *reinterpret_cast<const float2*>(conv2 + r * NP + pc);      // dy0, dy1
                     const float4 c4 = *reinterpret_cast<const float4*>(cf + r * kDS + s0);
                     const float4 b4 = *reinterpret_cast<const float4*>(bf + r * kDS + s0);
-                    const float cc[4] = {c4.x, c4.y, c4.z, c4.w}, bb[4] = {b4.x, b4.y, b4.z, b4.w};
-                    const float dl[2] = {v.x, v.z}, dx[2] = {v.y, v.w}, dyk[2] = {dyv.x, dyv.y};
-                    float part[8];
+                    const float2 cp[KP] = {make_float2(c4.x, c4.y), make_float2(c4.z, c4.w)};
+                    const float2 bp[KP] = {make_float2(b4.x, b4.y), make_float2(b4.z, b4.w)};
+                    const float2 dl2[2] = {make_float2(v.x, v.x), make_float2(v.z, v.z)};
+                    const float2 dx2[2] = {make_float2(v.y, v.y), make_float2(v.w, v.w)};
+                    const float2 dy2[2] = {make_float2(dyv.x, dyv.x), make_float2(dyv.y, dyv.y)};
+                    float2 pgb[KP], pgc[KP];                  // gb, gc terms of the lane's two channels
 #pragma unroll
                     for (int k = 0; k < 2; ++k) {
-                        float racc = 0.f, qacc = 0.f;
+                        float2 racc = make_float2(0.f, 0.f), qacc = racc;
 #pragma unroll
-                        for (int s = 0; s < KS; ++s) {
-                            const float a = ex2(dl[k] * A2[k][s]);
-                            const float g = fmaf(dyk[k], cc[s], gcar[k][s]);
-                            gcar[k][s] = a * g;
-                            const float hp = (jj == 0) ? hprev[k * KS + s] : hg[(jj - 1) * HS + k * KS + s];
-                            const float pp = gcar[k][s] * hp;
-                            gAacc[k][s] = fmaf(pp, dl[k], gAacc[k][s]);
-                            racc = fmaf(pp, A2[k][s], racc);      // times ln 2 below
-                            qacc = fmaf(g, bb[s], qacc);
-                            const float ht = hg[jj * HS + k * KS + s];
+                        for (int q = 0; q < KP; ++q) {
+                            const int e0 = k * KS + 2 * q;
+                            const float2 e = __fmul2_rn(dl2[k], A2[k][q]);
+                            const float2 a = make_float2(ex2(e.x), ex2(e.y));
+                            const float2 g = __ffma2_rn(dy2[k], cp[q], gcar[k][q]);
+                            gcar[k][q] = __fmul2_rn(a, g);
+                            const float2 hp = (jj == 0) ? make_float2(hprev[e0], hprev[e0 + 1])
+                                                        : make_float2(hg[(jj - 1) * HS + e0], hg[(jj - 1) * HS + e0 + 1]);
+                            const float2 pp = __fmul2_rn(gcar[k][q], hp);
+                            gAacc[k][q] = __ffma2_rn(pp, dl2[k], gAacc[k][q]);
+                            racc = __ffma2_rn(pp, A2[k][q], racc);      // times ln 2 below
+                            qacc = __ffma2_rn(g, bp[q], qacc);
+                            const float2 ht = make_float2(hg[jj * HS + e0], hg[jj * HS + e0 + 1]);
                             if (k == 0) {
-                                part[s] = g * dx[0];                      // gb terms of the lane's channels
-                                part[KS + s] = dyk[0] * ht;               // gc terms
+                                pgb[q] = __fmul2_rn(g, dx2[0]);
+                                pgc[q] = __fmul2_rn(dy2[0], ht);
                             } else {
-                                part[s] = fmaf(g, dx[1], part[s]);
-                                part[KS + s] = fmaf(dyk[1], ht, part[KS + s]);
+                                pgb[q] = __ffma2_rn(g, dx2[1], pgb[q]);
+                                pgc[q] = __ffma2_rn(dy2[1], ht, pgc[q]);
                             }
                         }
-                        rr[k][jj] = racc;
-                        qq[k][jj] = qacc;
+                        rr[k][jj] = racc.x + racc.y;
+                        qq[k][jj] = qacc.x + qacc.y;
                     }
+                    const float part[8] = {pgb[0].x, pgb[0].y, pgb[1].x, pgb[1].y,
+                                           pgc[0].x, pgc[0].y, pgc[1].x, pgc[1].y};
                     // sum over the warp's 8 channel pairs; this lane keeps entry (cw >> 2, cw & 3)
                     gw[r * 2 * kDS + (cw >> 2) * kDS + s0 + (cw & 3)] = warp_reduce_scatter8(part, lane);
                 }
@@ -433,12 +464,12 @@ __global__ void __launch_bounds__(128, 3) bwd2_kernel(const BwdLaunch p) {
     for (int k = 0; k < 2; ++k) {
         if (!valid[k]) continue;
         *reinterpret_cast<float4*>(p.gh0 + (b * D + dch[k]) * kDS + s0) =
-            make_float4(gcar[k][0], gcar[k][1], gcar[k][2], gcar[k][3]);
+            make_float4(gcar[k][0].x, gcar[k][0].y, gcar[k][1].x, gcar[k][1].y);
         if (p.det) {
             *reinterpret_cast<float4*>(p.part_gA + (b * D + dch[k]) * kDS + s0) =
-                make_float4(gAacc[k][0], gAacc[k][1], gAacc[k][2], gAacc[k][3]);
+                make_float4(gAacc[k][0].x, gAacc[k][0].y, gAacc[k][1].x, gAacc[k][1].y);
         } else {
-            red_add_v4(p.gA + dch[k] * kDS + s0, gAacc[k][0], gAacc[k][1], gAacc[k][2], gAacc[k][3]);
+            red_add_v4(p.gA + dch[k] * kDS + s0, gAacc[k][0].x, gAacc[k][0].y, gAacc[k][1].x, gAacc[k][1].y);
         }
     }
 }
