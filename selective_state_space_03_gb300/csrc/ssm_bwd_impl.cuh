@@ -150,13 +150,16 @@ __global__ void __launch_bounds__(128, 4) bwd_kernel(const BwdLaunch p) {
 
     const float Dk = (FUSE && valid && p.Dskip != nullptr) ? p.Dskip[d] : 0.f;   // skip weight
     float skip_acc = 0.f;                                                         // sum of dy x
-    float A2[KS], Af[KS], gcarry[KS], gAacc[KS];
+    // per-state values as pairs of neighbouring states, for packed f32x2 arithmetic
+    float2 A2[2], Af[2], gcarry[2], gAacc[2];
 #pragma unroll
-    for (int s = 0; s < KS; ++s) {
-        Af[s] = valid ? p.A[d * kDS + s0 + s] : 0.f;
-        A2[s] = Af[s] * kLog2e;
-        gcarry[s] = (valid && p.ghT != nullptr) ? p.ghT[(b * D + d) * kDS + s0 + s] : 0.f;
-        gAacc[s] = 0.f;
+    for (int q = 0; q < 2; ++q) {
+        const int s = s0 + 2 * q;
+        Af[q] = valid ? make_float2(p.A[d * kDS + s], p.A[d * kDS + s + 1]) : make_float2(0.f, 0.f);
+        A2[q] = make_float2(Af[q].x * kLog2e, Af[q].y * kLog2e);
+        gcarry[q] = (valid && p.ghT != nullptr)
+            ? make_float2(p.ghT[(b * D + d) * kDS + s], p.ghT[(b * D + d) * kDS + s + 1]) : make_float2(0.f, 0.f);
+        gAacc[q] = make_float2(0.f, 0.f);
     }
 
     // level-3 window in tensor memory: this warp's 32 lanes x LS*4 columns
@@ -241,10 +244,8 @@ __global__ void __launch_bounds__(128, 4) bwd_kernel(const BwdLaunch p) {
             for (int64_t jj = nck - 1; jj > jlo; --jj) {
                 const float4 z = *reinterpret_cast<const float4*>(p.carry_Z + ((jj * p.B + b) * D + d) * kDS + s0);
                 const float sd = p.carry_S[(jj * p.B + b) * D + d];
-                gcarry[0] = fmaf(ex2(A2[0] * sd), gcarry[0], z.x);
-                gcarry[1] = fmaf(ex2(A2[1] * sd), gcarry[1], z.y);
-                gcarry[2] = fmaf(ex2(A2[2] * sd), gcarry[2], z.z);
-                gcarry[3] = fmaf(ex2(A2[3] * sd), gcarry[3], z.w);
+                gcarry[0] = make_float2(fmaf(ex2(A2[0].x * sd), gcarry[0].x, z.x), fmaf(ex2(A2[0].y * sd), gcarry[0].y, z.y));
+                gcarry[1] = make_float2(fmaf(ex2(A2[1].x * sd), gcarry[1].x, z.z), fmaf(ex2(A2[1].y * sd), gcarry[1].y, z.w));
             }
         }
     }
@@ -269,15 +270,20 @@ __global__ void __launch_bounds__(128, 4) bwd_kernel(const BwdLaunch p) {
             __syncthreads();
             if (i + 1 < nsub) stage(cs + int64_t(i + 1) * LS, ce, false);
             sub[i * NT + tid] = make_float4(h[0], h[1], h[2], h[3]);
+            float2 h2[2] = {make_float2(h[0], h[1]), make_float2(h[2], h[3])};
 #pragma unroll 4
             for (int r = 0; r < LS; ++r) {
                 const float2 v = *reinterpret_cast<const float2*>(conv + r * DT + c);   // delta, delta*x
                 const float4 b4 = *reinterpret_cast<const float4*>(bf + r * kDS + s0);
-                h[0] = fmaf(ex2(v.x * A2[0]), h[0], v.y * b4.x);
-                h[1] = fmaf(ex2(v.x * A2[1]), h[1], v.y * b4.y);
-                h[2] = fmaf(ex2(v.x * A2[2]), h[2], v.y * b4.z);
-                h[3] = fmaf(ex2(v.x * A2[3]), h[3], v.y * b4.w);
+                const float2 bp[2] = {make_float2(b4.x, b4.y), make_float2(b4.z, b4.w)};
+                const float2 dl2 = make_float2(v.x, v.x), dx2 = make_float2(v.y, v.y);
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const float2 e = __fmul2_rn(dl2, A2[q]);
+                    h2[q] = __ffma2_rn(make_float2(ex2(e.x), ex2(e.y)), h2[q], __fmul2_rn(dx2, bp[q]));
+                }
             }
+            h[0] = h2[0].x; h[1] = h2[0].y; h[2] = h2[1].x; h[3] = h2[1].y;
         }
 
         // ---- reverse over the sub-chunks
@@ -301,15 +307,19 @@ __global__ void __launch_bounds__(128, 4) bwd_kernel(const BwdLaunch p) {
                 hs[0] = v.x; hs[1] = v.y; hs[2] = v.z; hs[3] = v.w;
             }
             {
-                float hc[KS] = {hs[0], hs[1], hs[2], hs[3]};
+                float2 hc[2] = {make_float2(hs[0], hs[1]), make_float2(hs[2], hs[3])};
 #pragma unroll
                 for (int r = 0; r < LS; ++r) {
                     const float2 v = *reinterpret_cast<const float2*>(conv + r * DT + c);
                     const float4 b4 = *reinterpret_cast<const float4*>(bf + r * kDS + s0);
-                    const float bb[4] = {b4.x, b4.y, b4.z, b4.w};
+                    const float2 bp[2] = {make_float2(b4.x, b4.y), make_float2(b4.z, b4.w)};
+                    const float2 dl2 = make_float2(v.x, v.x), dx2 = make_float2(v.y, v.y);
 #pragma unroll
-                    for (int s = 0; s < KS; ++s) hc[s] = fmaf(ex2(v.x * A2[s]), hc[s], v.y * bb[s]);
-                    tmem_st4(tw + uint32_t(r * KS), hc[0], hc[1], hc[2], hc[3]);
+                    for (int q = 0; q < 2; ++q) {
+                        const float2 e = __fmul2_rn(dl2, A2[q]);
+                        hc[q] = __ffma2_rn(make_float2(ex2(e.x), ex2(e.y)), hc[q], __fmul2_rn(dx2, bp[q]));
+                    }
+                    tmem_st4(tw + uint32_t(r * KS), hc[0].x, hc[0].y, hc[1].x, hc[1].y);
                     tmem_st4(tw + C::TMEM_B + uint32_t(r * KS), b4.x, b4.y, b4.z, b4.w);
                 }
                 tmem_wait_st();
@@ -338,24 +348,28 @@ __global__ void __launch_bounds__(128, 4) bwd_kernel(const BwdLaunch p) {
                     const float dyv = reinterpret_cast<const float*>(conv + r * DT + c)[3];
                     const float4 v = make_float4(v2.x, v2.y, 0.f, dyv);
                     const float4 c4 = *reinterpret_cast<const float4*>(cf + r * kDS + s0);
-                    const float bb[4] = {bgr[jj * KS], bgr[jj * KS + 1], bgr[jj * KS + 2], bgr[jj * KS + 3]};
-                    const float cc[4] = {c4.x, c4.y, c4.z, c4.w};
-                    float racc = 0.f, qacc = 0.f, part[8];
+                    const float2 cp[2] = {make_float2(c4.x, c4.y), make_float2(c4.z, c4.w)};
+                    const float2 dl2 = make_float2(v.x, v.x), dx2 = make_float2(v.y, v.y), dy2 = make_float2(v.w, v.w);
+                    float2 racc = make_float2(0.f, 0.f), qacc = racc, pgb[2], pgc[2];
 #pragma unroll
-                    for (int s = 0; s < KS; ++s) {
-                        const float a = ex2(v.x * A2[s]);
-                        const float g = fmaf(v.w, cc[s], gcarry[s]);
-                        gcarry[s] = a * g;
-                        const float hp = (jj == 0) ? hprev[s] : hg[(jj - 1) * KS + s];
-                        const float pp = gcarry[s] * hp;
-                        gAacc[s] = fmaf(pp, v.x, gAacc[s]);
-                        racc = fmaf(pp, Af[s], racc);
-                        qacc = fmaf(g, bb[s], qacc);
-                        part[s] = g * v.y;                      // gb term of this channel
-                        part[4 + s] = v.w * hg[jj * KS + s];    // gc term of this channel
+                    for (int q = 0; q < 2; ++q) {
+                        const int e0 = 2 * q;
+                        const float2 e = __fmul2_rn(dl2, A2[q]);
+                        const float2 a = make_float2(ex2(e.x), ex2(e.y));
+                        const float2 g = __ffma2_rn(dy2, cp[q], gcarry[q]);
+                        gcarry[q] = __fmul2_rn(a, g);
+                        const float2 hp = (jj == 0) ? make_float2(hprev[e0], hprev[e0 + 1])
+                                                    : make_float2(hg[(jj - 1) * KS + e0], hg[(jj - 1) * KS + e0 + 1]);
+                        const float2 pp = __fmul2_rn(gcarry[q], hp);
+                        gAacc[q] = __ffma2_rn(pp, dl2, gAacc[q]);
+                        racc = __ffma2_rn(pp, Af[q], racc);
+                        qacc = __ffma2_rn(g, make_float2(bgr[jj * KS + e0], bgr[jj * KS + e0 + 1]), qacc);
+                        pgb[q] = __fmul2_rn(g, dx2);                                            // gb terms
+                        pgc[q] = __fmul2_rn(dy2, make_float2(hg[jj * KS + e0], hg[jj * KS + e0 + 1]));   // gc terms
                     }
-                    rr[jj] = racc;
-                    qq[jj] = qacc;
+                    const float part[8] = {pgb[0].x, pgb[0].y, pgb[1].x, pgb[1].y, pgc[0].x, pgc[0].y, pgc[1].x, pgc[1].y};
+                    rr[jj] = racc.x + racc.y;
+                    qq[jj] = qacc.x + qacc.y;
                     // sum over the warp's 8 channels; this lane keeps entry (cw >> 2, cw & 3)
                     gw[r * 2 * kDS + (cw >> 2) * kDS + s0 + (cw & 3)] = warp_reduce_scatter8(part, lane);
                 }
@@ -399,12 +413,12 @@ __global__ void __launch_bounds__(128, 4) bwd_kernel(const BwdLaunch p) {
     if (!valid) return;
 #pragma unroll
     for (int s = 0; s < KS; ++s)
-        if (jlo == 0) p.gh0[(b * D + d) * kDS + s0 + s] = gcarry[s];
+        if (jlo == 0) p.gh0[(b * D + d) * kDS + s0 + s] = (s & 1) ? gcarry[s >> 1].y : gcarry[s >> 1].x;
     if (p.det) {
         *reinterpret_cast<float4*>(p.part_gA + ((b * gridDim.z + blockIdx.z) * D + d) * kDS + s0) =
-            make_float4(gAacc[0], gAacc[1], gAacc[2], gAacc[3]);
+            make_float4(gAacc[0].x, gAacc[0].y, gAacc[1].x, gAacc[1].y);
     } else {
-        red_add_v4(p.gA + d * kDS + s0, gAacc[0], gAacc[1], gAacc[2], gAacc[3]);
+        red_add_v4(p.gA + d * kDS + s0, gAacc[0].x, gAacc[0].y, gAacc[1].x, gAacc[1].y);
     }
 }
 
