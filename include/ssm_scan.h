@@ -41,8 +41,8 @@
  * that buffers do not overlap. Numbers outside these preconditions give
  * unspecified (but memory-safe) results.
  *
- * Supported: DS == 16; B, T, D >= 0; B <= 65535; D <= 2^27 (SSM_ERR_UNSUPPORTED
- * beyond). T == 0 or B == 0 or D == 0
+ * Supported: DS == 16; B, T, D >= 0; B <= 65535; D <= 2^27; at most 65535
+ * chunks of a chunked forward, ceil(T / chunk_len) (SSM_ERR_UNSUPPORTED beyond). T == 0 or B == 0 or D == 0
  * launches no kernel: hT <- h0 (zeros if h0 is NULL), gh0 <- ghT (zeros if
  * NULL), gA <- 0, as the ruDNN page's `chunk_kda` returns the initial state for
  * an empty sequence.
@@ -63,7 +63,7 @@ typedef enum { SSM_IO_F32 = 0, SSM_IO_BF16 = 1 } ssm_io_dtype;
 typedef enum {
     SSM_OK = 0,
     SSM_ERR_INVALID_ARG = 1,  /* NULL required pointer, negative size, bad enum or flag, B > 65535 */
-    SSM_ERR_UNSUPPORTED = 2,  /* DS != 16, or D > 2^27 */
+    SSM_ERR_UNSUPPORTED = 2,  /* DS != 16, D > 2^27, or more than 65535 forward chunks */
     SSM_ERR_MISALIGNED = 3,   /* a data pointer is not 16-byte aligned */
     SSM_ERR_WORKSPACE = 4,    /* workspace NULL or smaller than the query returned */
     SSM_ERR_CUDA = 5          /* a CUDA runtime call or a launch failed */

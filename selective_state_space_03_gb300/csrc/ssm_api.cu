@@ -251,6 +251,7 @@ ssm_status ssm_scan_fwd_fused(const ssm_scan_desc* desc, const void* x, const vo
         return SSM_OK;
     }
     const FwdPlan P = plan_fwd(d);
+    if (P.mode == 2 && P.nchunk > kMaxChunks) return SSM_ERR_UNSUPPORTED;   // one grid dimension per chunk
     if (P.mode == 2 && (workspace == nullptr || workspace_bytes < P.ws_S + P.ws_Sd)) return SSM_ERR_WORKSPACE;
     if (workspace && !aligned16(workspace)) return SSM_ERR_MISALIGNED;
 

@@ -9,6 +9,7 @@ namespace ssm {
 
 constexpr int kDS = 16;                  // state size the kernels are built for
 constexpr int64_t kMaxD = int64_t(1) << 27;   // channels: in-tile offsets (16 rows x D) stay in 32 bits
+constexpr int64_t kMaxChunks = 65535;         // chunks of the chunked forward (a grid dimension)
 
 enum class IO { F32 = 0, BF16 = 1 };
 

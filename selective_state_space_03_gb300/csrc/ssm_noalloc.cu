@@ -104,6 +104,7 @@ extern "C" ssm_status ssm_scan_fwd_noalloc(const ssm_scan_desc* desc, const void
         if (Lc < 64) Lc = 64;
     }
     const int64_t nchunk = cdiv64(d.T, Lc);
+    if (nchunk > kMaxChunks) return SSM_ERR_UNSUPPORTED;      // one grid dimension per chunk
 
     FwdLaunch L{};
     L.x = x; L.delta = delta; L.A = A; L.b = b; L.c = c; L.h0 = h0;

@@ -192,3 +192,10 @@ def test_fused_entry_point_checks(L):
     assert bwdf(gD=None) == 1                            # the skip weights' gradient is required
     assert bwdf(gD=FAKE + 8) == 3
     assert bwdf(dd=desc(flags=8)) == 1
+
+
+def test_too_many_chunks_is_unsupported(L):
+    # a chunk length that would need more than 65535 chunks is rejected before any launch
+    d = desc(T=70000 * 16, chunk_len=16)
+    need = L.ssm_scan_fwd_workspace_bytes(ctypes.byref(d))
+    assert fwd(L, d, ws=FAKE, wsb=need) == 2
