@@ -199,7 +199,7 @@ const char* ssm_status_str(ssm_status s) {
     switch (s) {
         case SSM_OK: return "ok";
         case SSM_ERR_INVALID_ARG: return "invalid argument";
-        case SSM_ERR_UNSUPPORTED: return "unsupported shape (DS must be 16)";
+        case SSM_ERR_UNSUPPORTED: return "unsupported shape (DS must be 16, D at most 2^27, at most 65535 chunks)";
         case SSM_ERR_MISALIGNED: return "pointer not 16-byte aligned";
         case SSM_ERR_WORKSPACE: return "workspace missing or too small";
         case SSM_ERR_CUDA: return "CUDA error";
