@@ -1,5 +1,6 @@
 // C ABI of libssm_scan.so: argument checks, schedule choice and launches.
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -9,27 +10,20 @@
 
 namespace ssm {
 
-cudaError_t launch_fwd_f32(const FwdLaunch& L, int mode, cudaStream_t stream);
-cudaError_t launch_fwd_bf16(const FwdLaunch& L, int mode, cudaStream_t stream);
-cudaError_t launch_bwd_f32(const BwdLaunch& L, cudaStream_t stream);
-cudaError_t launch_bwd_bf16(const BwdLaunch& L, cudaStream_t stream);
-cudaError_t launch_bwd_carry_f32(const BwdLaunch& L, cudaStream_t stream);
-cudaError_t launch_bwd_carry_bf16(const BwdLaunch& L, cudaStream_t stream);
-
 int device_sm_count() {
-    static int cache[64] = {0};
+    static std::atomic<int> cache[64];      // per device, filled on first use (0 = not yet)
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) {
         cudaGetLastError();
         return 152;
     }
-    if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+    if (dev >= 0 && dev < 64 && cache[dev].load() > 0) return cache[dev].load();
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
         cudaGetLastError();
         n = 152;
     }
-    if (dev >= 0 && dev < 64) cache[dev] = n;
+    if (dev >= 0 && dev < 64) cache[dev].store(n);
     return n;
 }
 

@@ -45,7 +45,8 @@ struct FwdLaunch {
     const float* Dskip;  // (D) or null: y += Dskip[d] * x
 };
 
-cudaError_t launch_fwd(const FwdLaunch& L, int mode, cudaStream_t stream);
+cudaError_t launch_fwd_f32(const FwdLaunch& L, int mode, cudaStream_t stream);
+cudaError_t launch_fwd_bf16(const FwdLaunch& L, int mode, cudaStream_t stream);
 
 struct BwdLaunch {
     const void* x;
@@ -88,7 +89,8 @@ cudaError_t launch_bwd_reduce(const BwdLaunch& L, int64_t nblk, int64_t nz, cuda
 
 constexpr int64_t kMaxBwdK = 256;   // largest checkpoint interval the backward reads directly
 
-cudaError_t launch_bwd(const BwdLaunch& L, cudaStream_t stream);
+cudaError_t launch_bwd_f32(const BwdLaunch& L, cudaStream_t stream);
+cudaError_t launch_bwd_bf16(const BwdLaunch& L, cudaStream_t stream);
 cudaError_t launch_bwd_carry_f32(const BwdLaunch& L, cudaStream_t stream);
 cudaError_t launch_bwd_carry_bf16(const BwdLaunch& L, cudaStream_t stream);
 

@@ -29,9 +29,6 @@
 
 namespace ssm {
 
-cudaError_t launch_fwd_f32(const FwdLaunch& L, int mode, cudaStream_t stream);
-cudaError_t launch_fwd_bf16(const FwdLaunch& L, int mode, cudaStream_t stream);
-
 namespace {
 
 constexpr size_t kNoallocScratchBytes = SSM_SCAN_NOALLOC_SCRATCH_BYTES;
