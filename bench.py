@@ -402,9 +402,7 @@ def run_ours(args, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded Philox normals, gen.make_inputs)",
-        "config": {"workload": w.name, "B": w.B, "T": w.T, "D": w.D, "DS": w.DS, "io": w.io,
-                   "state_and_grads": "f32", "ckpt_interval": K, "l2": "inputs larger than L2 (no flush)",
-                   "parallelism": f"replicas x{world}"},
+        "config": workload_config(w, world),
         "kernels": {"fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "bwd_deterministic_ms": bwd_det_ms,
                     "fused_softplus_skip_fwd_ms": fused_fwd_ms, "fused_softplus_skip_bwd_ms": fused_bwd_ms,
                     "fwd_elem_per_s": el / (fwd_ms / 1e3), "bwd_elem_per_s": el / (bwd_ms / 1e3),
@@ -566,6 +564,13 @@ def other_workloads(torch, ssm, dev):
 
 # ---------------------------------------------------------------- reference arm (the oracle)
 
+def workload_config(w, world):
+    """The `config` object of both arms' JSON lines (the same workload, named by its shape)."""
+    return {"workload": w.name, "B": w.B, "T": w.T, "D": w.D, "DS": w.DS, "io": w.io,
+            "state_and_grads": "f32", "ckpt_interval": w.ckpt_interval,
+            "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"}
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
@@ -594,7 +599,7 @@ def run_reference(args, rank, world):
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded Philox normals, gen.make_inputs)",
-            "config": {"workload": w.name, "sample": f"B={B1} T={w.T} D={w.D} DS={w.DS} per step (fwd+bwd)"},
+            "config": workload_config(w, world),
             "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": f"B={B1} T={w.T} D={w.D} DS={w.DS} per step (fwd+bwd)"},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
