@@ -261,7 +261,7 @@ __global__ void __launch_bounds__(128, 3) bwd2_kernel(const BwdLaunch p) {
             for (int k = 0; k < 2; ++k)
 #pragma unroll
                 for (int q = 0; q < KP; ++q) hp2[k][q] = make_float2(h[k][2 * q], h[k][2 * q + 1]);
-#pragma unroll 4
+#pragma unroll 8
             for (int r = 0; r < LS; ++r) {
                 const float4 v = conv1[r * NP + pc];                                   // d0, d0 x0, d1, d1 x1
                 const float4 b4 = *reinterpret_cast<const float4*>(bf + r * kDS + s0);
