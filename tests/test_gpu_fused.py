@@ -140,3 +140,48 @@ def test_decode_step_with_softplus(io):
     ref = oracle.fwd_fused(inp["x"], inp["delta"], inp["A"], inp["b"], inp["c"], inp["h0"], delta_softplus=True)
     assert_close(np.stack([to_host(v) for v in ys], axis=1), ref["y"], io, "fwd", "y")
     assert_close(to_host(h), ref["hT"], io, "fwd", "hT")
+
+
+def test_fused_and_deterministic_workload5_full_size_sampled():
+    """Workload 5 at full size with softplus on delta, the skip and fixed-order sums:
+    sampled chains against the oracle, gD_skip and gA on sampled channels over all
+    batches, gb and gc on one whole batch, and a second run bitwise equal."""
+    import torch
+    from gpu_util import sample_indices, sub_inputs
+    w = gen.workload(5)
+    inp = gen.make_inputs(w, raw_delta=True, with_skip=True)
+    t = dev_inputs(inp)
+    Ds = to_dev(inp["D_skip"])
+    K = w.ckpt_interval
+    y, hT, ck = ssm().ssm_scan_fwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], ckpt_interval=K, D_skip=Ds,
+                                   delta_softplus=True)
+    g = ssm().ssm_scan_bwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], ck, t["dy"], ckpt_interval=K,
+                           D_skip=Ds, delta_softplus=True, deterministic=True)
+    g2 = ssm().ssm_scan_bwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], ck, t["dy"], ckpt_interval=K,
+                            D_skip=Ds, delta_softplus=True, deterministic=True)
+    torch.cuda.synchronize()
+    for k in GRADS + ("gD_skip",):
+        assert torch.equal(g[k], g2[k]), k
+    del g2
+    bsel, dsel = sample_indices(w.B, 3, 7), sample_indices(w.D, 8, 8)
+    sub = sub_inputs(inp, bsel, dsel)
+    ref = oracle.fwd_fused(sub["x"], sub["delta"], sub["A"], sub["b"], sub["c"], sub["h0"], inp["D_skip"][dsel],
+                           delta_softplus=True)
+    gref = oracle.bwd_fused(sub["x"], sub["delta"], sub["A"], sub["b"], sub["c"], sub["h0"], sub["dy"], None,
+                            inp["D_skip"][dsel], delta_softplus=True)
+    bi, di = torch.as_tensor(bsel), torch.as_tensor(dsel)
+    assert_close(to_host(y[bi][:, :, di]), ref["y"], "bf16", "fwd", "y")
+    assert_close(to_host(hT[bi][:, di]), ref["hT"], "bf16", "fwd", "hT")
+    for k in ("gx", "gdelta"):
+        assert_close(to_host(g[k][bi][:, :, di]), gref[k], "bf16", "grad", k)
+    assert_close(to_host(g["gh0"][bi][:, di]), gref["gh0"], "bf16", "grad", "gh0")
+    sub = sub_inputs(inp, np.arange(w.B), dsel[:3])
+    gref = oracle.bwd_fused(sub["x"], sub["delta"], sub["A"], sub["b"], sub["c"], sub["h0"], sub["dy"], None,
+                            inp["D_skip"][dsel[:3]], delta_softplus=True)
+    for k in ("gA", "gD_skip"):
+        assert_close(to_host(g[k][torch.as_tensor(dsel[:3])]), gref[k], "bf16", "grad", k)
+    sub = sub_inputs(inp, np.array([bsel[2]]), np.arange(w.D))
+    gref = oracle.bwd_fused(sub["x"], sub["delta"], sub["A"], sub["b"], sub["c"], sub["h0"], sub["dy"], None,
+                            inp["D_skip"], delta_softplus=True)
+    for k in ("gb", "gc"):
+        assert_close(to_host(g[k][int(bsel[2])][None]), gref[k], "bf16", "grad", k)
