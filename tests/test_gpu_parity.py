@@ -180,7 +180,7 @@ def test_unaligned_channel_count(io, bwd_kd):
     run_case(gen.workload(2, B=2, T=77, D=D, io=io, h0_std=0.1), K=24, chunk_len=-1, lanes=2, bwd=False)
 
 
-@pytest.mark.parametrize("T,K", [(1, 1), (33, 16), (20, 64), (230, 50), (257, 256)])
+@pytest.mark.parametrize("T,K", [(1, 1), (15, 16), (33, 16), (20, 64), (230, 50), (255, 256), (257, 256)])
 @pytest.mark.parametrize("bwd_kd", [1, 2])
 def test_ragged_lengths_and_intervals(T, K, bwd_kd):
     run_case(gen.workload(2, B=2, T=T, D=40, h0_std=0.1), K=K, ghT=True, bwd_kd=bwd_kd)
