@@ -181,8 +181,9 @@ __global__ void __launch_bounds__(128, 3) bwd2_kernel(const BwdLaunch p) {
             float dl[2], xv[2];
             load_vals<TIO, 2>(dr + r * DT + 2 * pp, dl);
             if (FUSE && p.softplus) {
-                dl[0] = r < rows_valid ? softplus_f32(dl[0]) : 0.f;
-                dl[1] = r < rows_valid ? softplus_f32(dl[1]) : 0.f;
+                const float2 sp = softplus2_f32(make_float2(dl[0], dl[1]));
+                dl[0] = r < rows_valid ? sp.x : 0.f;
+                dl[1] = r < rows_valid ? sp.y : 0.f;
             }
             load_vals<TIO, 2>(xr + r * DT + 2 * pp, xv);
             conv1[i] = make_float4(dl[0], dl[0] * xv[0], dl[1], dl[1] * xv[1]);

@@ -43,6 +43,25 @@ __device__ __forceinline__ float softplus_f32(float v) {
     return fmaxf(v, 0.f) + l;
 }
 
+// softplus of two values with packed f32x2 arithmetic (same formula and accuracy as
+// softplus_f32): the exponent arguments, the series, 1 + e and the ln 2 scaling run as
+// f32x2 operations, the two exponentials and logarithms on the MUFU.
+__device__ __forceinline__ float2 softplus2_f32(float2 v) {
+    const float2 m = __fmul2_rn(make_float2(fabsf(v.x), fabsf(v.y)), make_float2(-kLog2e, -kLog2e));
+    const float2 e = make_float2(ex2(m.x), ex2(m.y));                       // in (0, 1]
+    const float2 ne = make_float2(-e.x, -e.y);
+    // e (1 - e (1/2 - e (1/3 - e (1/4 - e/5)))), nested from the inside
+    float2 p = __ffma2_rn(ne, make_float2(0.2f, 0.2f), make_float2(0.25f, 0.25f));
+    p = __ffma2_rn(ne, p, make_float2(0.33333334f, 0.33333334f));
+    p = __ffma2_rn(ne, p, make_float2(0.5f, 0.5f));
+    p = __ffma2_rn(ne, p, make_float2(1.f, 1.f));
+    const float2 series = __fmul2_rn(e, p);
+    const float2 ope = __fadd2_rn(e, make_float2(1.f, 1.f));
+    const float2 lg = __fmul2_rn(make_float2(lg2(ope.x), lg2(ope.y)), make_float2(kLn2, kLn2));
+    return make_float2(fmaxf(v.x, 0.f) + (e.x < 0.03125f ? series.x : lg.x),
+                       fmaxf(v.y, 0.f) + (e.y < 0.03125f ? series.y : lg.y));
+}
+
 // sigmoid(v), the derivative of softplus, from sp = softplus(v): sigmoid(v) = 1 - e^-sp.
 // Small sp from the series sp - sp^2/2 + sp^3/6 - sp^4/24 (no cancellation).
 __device__ __forceinline__ float sigmoid_from_softplus(float sp) {

@@ -242,8 +242,13 @@ __global__ void __launch_bounds__(32, FwdCfg<TIO, G, KD>::MINB) fwd_kernel(const
                 // rows past the end stay 0 (zero-filled raw rows would give softplus(0) = ln 2,
                 // and padded steps must leave the state unchanged)
                 const int rows = int(min(int64_t(TT), t_end - (t_begin + tile * TT)));
-                for (int i = lane; i < TT * DT; i += NT)
-                    dsf[i] = (i / DT < rows) ? softplus_f32(to_f32(dt[i])) : 0.f;
+                static_assert(DT % 2 == 0, "softplus pairs stay within a tile row");
+                for (int i = 2 * lane; i < TT * DT; i += 2 * NT) {      // two neighbouring channels
+                    float raw[2];
+                    load_vals<TIO, 2>(dt + i, raw);
+                    const float2 sp = softplus2_f32(make_float2(raw[0], raw[1]));
+                    *reinterpret_cast<float2*>(dsf + i) = (i / DT < rows) ? sp : make_float2(0.f, 0.f);
+                }
             } else {
                 for (int i = lane; i < TT * DT; i += NT) dsf[i] = to_f32(dt[i]);
             }
