@@ -24,7 +24,8 @@
 // level-3 window (h_t of both channels, 16 steps, 128 columns) is in tensor
 // memory and b_t comes from shared memory, so shared memory per CTA is ~35 KB
 // and three CTAs (12 warps) are resident per SM, each thread with up to 168
-// registers.
+// registers. As in `bwd_kernel`, the per-state arithmetic is packed f32x2 on
+// pairs of neighbouring states.
 #pragma once
 
 #include "ssm_bwd_impl.cuh"

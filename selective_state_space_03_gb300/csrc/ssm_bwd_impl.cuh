@@ -34,6 +34,13 @@
 // clock per SM, and a 16-byte broadcast load takes 4 of its cycles, so the
 // reductions are built to spend as few of those cycles as possible.) gA is
 // accumulated in registers over the CTA's whole sweep and added atomically once.
+// The per-state arithmetic runs on pairs of neighbouring states as packed f32x2
+// operations (FMUL2 / FFMA2: one issue slot for two operations), the MUFU
+// exponentials and the reductions stay scalar.
+//
+// The same file holds the chunk-parallel pass (bwd_carry_kernel), and the
+// kernels' deterministic (partials instead of atomics) and fused (softplus on
+// delta, skip connection) variants.
 #pragma once
 
 #include <type_traits>
