@@ -221,7 +221,12 @@ ssm_status ssm_scan_fwd_noalloc(const ssm_scan_desc* desc,
  *   b, c          (B, DS)     io dtype
  *   A             (D, DS)     float32
  *   h             (B, D, DS)  float32, read and overwritten (not NULL)
- * No workspace; B == 0 or D == 0 launches nothing. Errors as ssm_scan_fwd. */
+ * No workspace; B == 0 or D == 0 launches nothing. Errors as ssm_scan_fwd.
+ * Steps are launched as programmatic dependents of the preceding kernel on the
+ * stream: after an earlier ssm_scan_step, a step may already read its own x,
+ * delta, A, b and c while that step finishes (it waits for it before reading h),
+ * so these five must not be the h or y written by the preceding step call.
+ * After any other kernel or copy the step starts only when that one is done. */
 ssm_status ssm_scan_step(const ssm_scan_desc* desc,
                          const void* x, const void* delta, const float* A,
                          const void* b, const void* c, float* h, void* y, void* stream);

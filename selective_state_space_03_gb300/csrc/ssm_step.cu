@@ -10,7 +10,9 @@
 // The step moves 128 bytes of state per chain in and out and does 16 exp per
 // chain, so it is bound by HBM (or by launch latency for small B*D). Layout: 4
 // lanes per chain, 4 states per lane in one 16-byte load and store, the readout
-// finished with two shuffles; 32 chains per 128-thread CTA.
+// finished with two shuffles; 32 chains per 128-thread CTA. Steps are launched
+// with programmatic stream serialization: a step's loads of its own inputs
+// overlap the end of the previous step, and only the state load waits for it.
 #include "ssm_common.cuh"
 #include "ssm_internal.h"
 #include "ssm_scan.h"
@@ -36,17 +38,26 @@ __global__ void __launch_bounds__(128) step_kernel(const StepLaunch p) {
     const int64_t chain = gid >> 2;
     const int sg = int(gid & 3), s0 = sg * 4;
     const bool valid = chain < p.B * p.D;       // whole 4-lane groups are valid or not
+    // Consecutive steps on a stream are launched as programmatic dependents: let the next
+    // step's CTAs start now; they run up to their wait below while this grid finishes.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     float acc = 0.f;
     float4 hv = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (valid) {
+    float dl = 0.f, dx = 0.f, bv[4] = {0.f, 0.f, 0.f, 0.f}, cv[4] = {0.f, 0.f, 0.f, 0.f};
+    float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (valid) {      // this step's inputs, which no earlier step writes
         const int64_t bb = chain / p.D, d = chain - bb * p.D;
-        float dl = to_f32(static_cast<const TIO*>(p.delta)[chain]);
+        dl = to_f32(static_cast<const TIO*>(p.delta)[chain]);
         if (p.softplus) dl = softplus_f32(dl);
-        const float dx = dl * to_f32(static_cast<const TIO*>(p.x)[chain]);
-        float bv[4], cv[4];
+        dx = dl * to_f32(static_cast<const TIO*>(p.x)[chain]);
         load_vals<TIO, 4>(static_cast<const TIO*>(p.b) + bb * kDS + s0, bv);
         load_vals<TIO, 4>(static_cast<const TIO*>(p.c) + bb * kDS + s0, cv);
-        const float4 a4 = *reinterpret_cast<const float4*>(p.A + d * kDS + s0);
+        a4 = *reinterpret_cast<const float4*>(p.A + d * kDS + s0);
+    }
+    // the state (and y) belong to the previous step: wait until the grid before this one has
+    // completed and its writes are visible (returns at once without such a grid)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (valid) {
         hv = *reinterpret_cast<const float4*>(p.h + chain * kDS + s0);
         hv.x = fmaf(ex2(dl * (a4.x * kLog2e)), hv.x, dx * bv[0]);
         hv.y = fmaf(ex2(dl * (a4.y * kLog2e)), hv.y, dx * bv[1]);
@@ -85,11 +96,16 @@ extern "C" ssm_status ssm_scan_step(const ssm_scan_desc* desc, const void* x, co
     const int64_t blocks = (threads + 127) / 128;
     if (blocks > int64_t(0x7fffffff)) return SSM_ERR_UNSUPPORTED;
     StepLaunch L{x, delta, A, b, c, h, y, d.B, d.D, (d.flags & SSM_SCAN_DELTA_SOFTPLUS) != 0};
-    const cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (d.io == SSM_IO_BF16) {
-        step_kernel<__nv_bfloat16><<<unsigned(blocks), 128, 0, s>>>(L);
-    } else {
-        step_kernel<float><<<unsigned(blocks), 128, 0, s>>>(L);
-    }
-    return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(blocks));
+    cfg.blockDim = dim3(128);
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // overlap with the previous step
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = d.io == SSM_IO_BF16 ? cudaLaunchKernelEx(&cfg, step_kernel<__nv_bfloat16>, L)
+                                              : cudaLaunchKernelEx(&cfg, step_kernel<float>, L);
+    return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
