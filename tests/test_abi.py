@@ -199,3 +199,22 @@ def test_too_many_chunks_is_unsupported(L):
     d = desc(T=70000 * 16, chunk_len=16)
     need = L.ssm_scan_fwd_workspace_bytes(ctypes.byref(d))
     assert fwd(L, d, ws=FAKE, wsb=need) == 2
+
+
+def test_product_path_does_not_import_the_oracle():
+    # a fresh interpreter: importing the package and loading the library pulls in no oracle module
+    import subprocess
+    import sys
+    code = ("import sys; sys.path.insert(0, %r); import selective_state_space_03_gb300 as m; m.lib(); "
+            "bad = [k for k in sys.modules if k == 'oracle' or k.startswith('oracle.')]; "
+            "print('ORACLE' if bad else 'CLEAN')") % ROOT
+    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=120)
+    assert out.stdout.strip().endswith("CLEAN"), out.stdout + out.stderr
+
+
+def test_missing_library_raises_instead_of_falling_back(monkeypatch):
+    import selective_state_space_03_gb300 as m
+    monkeypatch.setattr(m, "_lib", None)
+    monkeypatch.setattr(m, "LIB_PATH", os.path.join(ROOT, "no_such_dir", "libssm_scan.so"))
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        m.lib()
