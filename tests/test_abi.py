@@ -201,7 +201,7 @@ def test_too_many_chunks_is_unsupported(L):
     assert fwd(L, d, ws=FAKE, wsb=need) == 2
 
 
-def test_product_path_does_not_import_the_oracle():
+def test_product_path_does_not_import_the_oracle(L):
     # a fresh interpreter: importing the package and loading the library pulls in no oracle module
     import subprocess
     import sys
