@@ -54,7 +54,7 @@ struct Bwd2Cfg {
     static constexpr size_t CONV1 = size_t(LS) * NP * 16;                   // (d0, d0*x0, d1, d1*x1)
     static constexpr size_t CONV2 = size_t(LS) * NP * 16;                   // (dy0, dy1, x0, x1)
     static constexpr size_t BCF = size_t(LS) * kDS * 4;                     // one of b, c as float32
-    static constexpr size_t GBC = size_t(NW) * LS * 2 * kDS * 4;            // per-warp gb, gc sums of a tile
+    static constexpr size_t GBC = size_t(2 * NW) * LS * 2 * kDS * 4;        // per-half-warp gb, gc sums of a tile
     static constexpr size_t SMEM = 3 * RAW_X + 2 * RAW_BC + CONV1 + CONV2 + 2 * BCF + GBC + 16;
     // tensor memory columns per lane: h of both channels per step
     static constexpr uint32_t TMEM_H_STEP = KD * KS;                        // 8
@@ -83,7 +83,7 @@ __global__ void __launch_bounds__(128, 3) bwd2_kernel(const BwdLaunch p) {
     float4* conv2 = reinterpret_cast<float4*>(ptr); ptr += C::CONV2;   // [LS][NP]
     float* bf = reinterpret_cast<float*>(ptr);      ptr += C::BCF;     // [LS][16]
     float* cf = reinterpret_cast<float*>(ptr);      ptr += C::BCF;
-    float* gbc = reinterpret_cast<float*>(ptr);     ptr += C::GBC;     // [NW][LS][2][16]
+    float* gbc = reinterpret_cast<float*>(ptr);     ptr += C::GBC;     // [2 NW][LS][2][16]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ptr);
 
     const int tid = threadIdx.x;
@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(128, 3) bwd2_kernel(const BwdLaunch p) {
         const int off = r * 2 * kDS + tau * kDS + q * 4;
         float4 v = *reinterpret_cast<const float4*>(gbc + off);
 #pragma unroll
-        for (int w = 1; w < C::NW; ++w) v = v + *reinterpret_cast<const float4*>(gbc + w * LS * 2 * kDS + off);
+        for (int w = 1; w < 2 * C::NW; ++w) v = v + *reinterpret_cast<const float4*>(gbc + w * LS * 2 * kDS + off);
         if (t0 + r < t_lim) {
             if (p.det) {
                 *reinterpret_cast<float4*>(p.part_gbc + ((int64_t(blockIdx.x) * p.B + b) * T + t0 + r) * (2 * kDS) +
@@ -345,7 +345,8 @@ __global__ void __launch_bounds__(128, 3) bwd2_kernel(const BwdLaunch p) {
                 tmem_wait_st();
             }
 
-            float* gw = gbc + warp * LS * 2 * kDS;   // this warp's gb, gc sums for the tile
+            // this lane's slot set: sums over the 4 channel pairs {cw, cw^2, cw^4, cw^6} of its warp
+            float* gw = gbc + (warp * 2 + (cw & 1)) * LS * 2 * kDS;
             // reverse sweep over the sub-chunk, 4 steps per lane reduce-scatter group
 #pragma unroll 2
             for (int rg = LS - 4; rg >= 0; rg -= 4) {
@@ -403,7 +404,11 @@ __global__ void __launch_bounds__(128, 3) bwd2_kernel(const BwdLaunch p) {
                     const float part[8] = {pgb[0].x, pgb[0].y, pgb[1].x, pgb[1].y,
                                            pgc[0].x, pgc[0].y, pgc[1].x, pgc[1].y};
                     // sum over the warp's 8 channel pairs; this lane keeps entry (cw >> 2, cw & 3)
-                    gw[r * 2 * kDS + (cw >> 2) * kDS + s0 + (cw & 3)] = warp_reduce_scatter8(part, lane);
+                    {   // sum over 4 of the warp's 8 channel pairs; this lane keeps entries 2 (cw>>1) + {0, 1}
+                        const int e0 = 2 * (cw >> 1);
+                        const float2 v2 = warp_reduce_scatter8_half(part, lane);
+                        *reinterpret_cast<float2*>(gw + r * 2 * kDS + (e0 >> 2) * kDS + s0 + (e0 & 3)) = v2;
+                    }
                 }
                 // sums over the pair's 4 lanes: this lane takes step rg + sg of both channels
                 float rs[2], qs[2];

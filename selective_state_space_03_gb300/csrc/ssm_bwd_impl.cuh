@@ -111,6 +111,29 @@ __device__ __forceinline__ float warp_reduce_scatter8(const float (&v)[8], int l
     return keep + __shfl_xor_sync(0xffffffffu, send, 4);
 }
 
+// The first two stages of warp_reduce_scatter8: sums over the 4 lanes {cw, cw^2, cw^4, cw^6}
+// (cw = lane >> 2); lane returns entries 2 (cw >> 1) and 2 (cw >> 1) + 1.
+__device__ __forceinline__ float2 warp_reduce_scatter8_half(const float (&v)[8], int lane) {
+    const int cw = lane >> 2;
+    float a[4];
+    const bool b2 = cw & 4;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float send = b2 ? v[k] : v[k + 4];
+        const float keep = b2 ? v[k + 4] : v[k];
+        a[k] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+    float c2[2];
+    const bool b1 = cw & 2;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const float send = b1 ? a[k] : a[k + 2];
+        const float keep = b1 ? a[k + 2] : a[k];
+        c2[k] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+    return make_float2(c2[0], c2[1]);
+}
+
 __device__ __forceinline__ float4 operator+(const float4 a, const float4 b) {
     return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
 }
