@@ -9,8 +9,9 @@
 //
 // What the second channel buys, per element: the b and c values a lane reads
 // from shared memory serve 8 chains instead of 4; the per-step sums over d of
-// gb and gc first add the lane's two channels in registers, so the 8-lane
-// reduce-scatter (shuffles and selects) is paid once per 8 elements instead of
+// gb and gc first add the lane's two channels in registers, so the lane
+// reduce-scatter (shuffles and selects; two stages here, into per-half-warp
+// slots that the per-tile flush adds) is paid once per 8 elements instead of
 // once per 4; the (delta, delta*x) pair of both channels arrives in one 16-byte
 // shared load. The instruction count per element drops by about a quarter.
 //
