@@ -52,11 +52,11 @@ def load_peaks():
 
 
 # DRAM bytes (read + write) of one bwd2_kernel launch at workload 5, from the ncu capture
-# summarised in profiles/bwd2_kernel_B16_T512_D5120.md: 693.7 MB at T = 512, and traffic
+# summarised in profiles/bwd2_kernel_B16_T512_D5120.md: 691.4 MB at T = 512, and traffic
 # grows with the number of steps, so 4 x that at T = 2048. Reset to None whenever the
 # kernel changes until it is captured again.
-BWD2_TRAFFIC = {"bytes_per_launch": 4 * 693.696e6,
-                "source": "ncu dram__bytes_read+write of bwd2_kernel at T=512 (693.7 MB) x 4 steps ratio"}
+BWD2_TRAFFIC = {"bytes_per_launch": 4 * 691.428608e6,
+                "source": "ncu dram__bytes_read+write of bwd2_kernel at T=512 (691.4 MB) x 4 steps ratio"}
 
 # ---------------------------------------------------------------- algorithmic work per element
 
