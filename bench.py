@@ -77,6 +77,7 @@ def compulsory_bytes(w, direction):
 # dy*c, g update, a*g, p = (a g) h_{t-1}, gA, gdelta, <g,b>, gb term, gc term (9).
 BWD_OPS_PER_ELEM = 12
 FWD_EX2_PER_ELEM = 1    # one exp per element (MUFU)
+BWD_EX2_PER_ELEM = 3    # exps the backward executes per element: two recompute levels and the reverse sweep
 EX2_PER_SM_CLK = 32     # GB300 MUFU ex2 throughput, measured on the box
 FP32_PER_SM_CLK = 128   # FP32 FMA lanes per SM
 
@@ -397,6 +398,7 @@ def run_ours(args, rank, world, local_rank):
     ex2_peak = EX2_PER_SM_CLK * torch.cuda.get_device_properties(dev).multi_processor_count * sm_mhz * 1e6
     bwd_ops = el * BWD_OPS_PER_ELEM / (bwd_ms / 1e3)
     fwd_ex2 = el * FWD_EX2_PER_ELEM / (fwd_ms / 1e3)
+    bwd_ex2 = el * BWD_EX2_PER_ELEM / (bwd_ms / 1e3)
     fwd_bytes, bwd_bytes = compulsory_bytes(w, "fwd"), compulsory_bytes(w, "bwd")
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -409,7 +411,9 @@ def run_ours(args, rank, world, local_rank):
                     "fwd_hbm_gbs": fwd_bytes / (fwd_ms / 1e3) / 1e9, "bwd_hbm_gbs": bwd_bytes / (bwd_ms / 1e3) / 1e9,
                     "fwd_hbm_frac": fwd_bytes / (fwd_ms / 1e3) / 1e9 / hbm_peak,
                     "bwd_hbm_frac": bwd_bytes / (bwd_ms / 1e3) / 1e9 / hbm_peak,
-                    "fwd_ex2_frac": fwd_ex2 / ex2_peak},
+                    "fwd_ex2_frac": fwd_ex2 / ex2_peak, "bwd_ex2_frac": bwd_ex2 / ex2_peak,
+                    "ex2_basis": f"MUFU ex2 executed ({FWD_EX2_PER_ELEM}/element forward, {BWD_EX2_PER_ELEM}/element "
+                                 f"backward) vs {EX2_PER_SM_CLK}/clk/SM x SMs x median SM clock"},
         "roofline": {"kernel": "bwd2_kernel (reverse sweep with recompute, two channels per lane)", "bound": "alu",
                      "achieved": bwd_ops / 1e12, "peak": fp32_peak / 1e12, "unit": "TFLOP/s",
                      "frac": bwd_ops / fp32_peak, "traffic": BWD2_TRAFFIC["bytes_per_launch"],
