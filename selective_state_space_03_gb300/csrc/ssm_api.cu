@@ -65,25 +65,19 @@ FwdPlan plan_fwd(const ssm_scan_desc& d) {
     const int64_t chains = d.B * d.D;
     const int64_t want = int64_t(device_sm_count()) * 512;   // ~16 resident warps per SM
     bool chunked = false;
-    int64_t Lc = 0;
-    if (d.chunk_len > 0) {
-        chunked = true;
-        Lc = d.chunk_len;
-    } else if (d.chunk_len == 0 && chains * 4 * 2 < want && d.T >= 256) {
-        chunked = true;
-        // chunks for about 14 resident warps per SM in pass 2 (rounded down: on workload 4's
-        // 4096-step calls 8 chunks of 512 ran 9 % faster than 10 of 416, and 16 of 256
-        // 3 % slower: fewer chunks also shorten pass 1)
-        const int64_t nch = std::max<int64_t>(2, int64_t(device_sm_count()) * 448 / (chains * 4));
-        Lc = cdiv(cdiv(d.T, nch), 32) * 32;
-        if (Lc < 64) Lc = 64;
+    ChunkSchedule cs{0, 1};
+    if (d.chunk_len > 0 || (d.chunk_len == 0 && chains * 4 * 2 < want && d.T >= 256)) {
+        cs = chunk_schedule(d.T, chains, d.chunk_len, device_sm_count());
+        chunked = cdiv(d.T, cs.Lc) >= 2;
     }
-    if (chunked && cdiv(d.T, Lc) < 2) chunked = false;
     if (chunked) {
         P.mode = 2;
         P.G = 4;
-        P.Lc = Lc;
-        P.nchunk = cdiv(d.T, Lc);
+        P.kd = cs.kd;
+        // testing aid: channels per lane of both chunk passes (1 or 2)
+        if (const char* env = std::getenv("SSM_SCAN_FORCE_CHUNK_KD")) P.kd = std::atoi(env) == 2 ? 2 : 1;
+        P.Lc = cs.Lc;
+        P.nchunk = cdiv(d.T, cs.Lc);
         P.ws_S = align_up(size_t(d.B) * size_t(P.nchunk - 1) * size_t(d.D) * kDS * 4);
         P.ws_Sd = align_up(size_t(d.B) * size_t(P.nchunk - 1) * size_t(d.D) * 4);
     } else {

@@ -418,9 +418,15 @@ cudaError_t launch_fwd_fuse(const FwdLaunch& L, int mode, cudaStream_t stream) {
             if (L.kd == 2) { SSM_FWD_VEC(4, 2, kSingle); }
             SSM_FWD_VEC(4, 1, kSingle);
         case kPass1:
+            if (L.kd == 2) {
+                if (L.vec) return launch_fwd_t<TIO, 4, 2, true, kPass1, true, FUSE>(L, stream);
+                return launch_fwd_t<TIO, 4, 2, false, kPass1, true, FUSE>(L, stream);
+            }
             if (L.vec) return launch_fwd_t<TIO, 4, 1, true, kPass1, true, FUSE>(L, stream);
             return launch_fwd_t<TIO, 4, 1, false, kPass1, true, FUSE>(L, stream);
-        case kPass2: SSM_FWD_VEC(4, 1, kPass2);
+        case kPass2:
+            if (L.kd == 2) { SSM_FWD_VEC(4, 2, kPass2); }
+            SSM_FWD_VEC(4, 1, kPass2);
         case kCkptOnly: SSM_FWD_VEC(4, 1, kCkptOnly);
         default: return cudaErrorInvalidValue;
     }

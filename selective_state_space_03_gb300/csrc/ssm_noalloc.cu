@@ -92,14 +92,10 @@ extern "C" ssm_status ssm_scan_fwd_noalloc(const ssm_scan_desc* desc, const void
         return SSM_OK;
     }
 
-    // chunk length: the caller's, else chunks for about 14 resident warps per SM (the rule
-    // ssm_scan_fwd uses for its chunked schedule)
-    int64_t Lc = d.chunk_len;
-    if (Lc <= 0) {
-        const int64_t nch = std::max<int64_t>(2, int64_t(device_sm_count()) * 448 / (d.B * d.D * 4));
-        Lc = cdiv64(cdiv64(d.T, nch), 32) * 32;
-        if (Lc < 64) Lc = 64;
-    }
+    // chunk length and lanes: the schedule ssm_scan_fwd uses for its chunked scan (with the
+    // caller's chunk length when given)
+    const ChunkSchedule cs = chunk_schedule(d.T, d.B * d.D, d.chunk_len > 0 ? d.chunk_len : 0, device_sm_count());
+    const int64_t Lc = cs.Lc;
     const int64_t nchunk = cdiv64(d.T, Lc);
     if (nchunk > kMaxChunks) return SSM_ERR_UNSUPPORTED;      // one grid dimension per chunk
 
@@ -111,6 +107,7 @@ extern "C" ssm_status ssm_scan_fwd_noalloc(const ssm_scan_desc* desc, const void
     L.vec = (d.D * (d.io == SSM_IO_BF16 ? 2 : 4)) % 16 == 0;
     L.ckpt_only = false;
     L.G = 4;
+    L.kd = cs.kd;
     L.softplus = (d.flags & SSM_SCAN_DELTA_SOFTPLUS) != 0;
     auto run = [&](int mode) {
         return d.io == SSM_IO_BF16 ? launch_fwd_bf16(L, mode, s) : launch_fwd_f32(L, mode, s);

@@ -107,6 +107,12 @@ def test_fused_chunked_forward_chunk_parallel_backward(io):
 
 
 @pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_fused_chunked_forward_two_channels_per_lane(io):
+    with forced(SSM_SCAN_FORCE_CHUNK_KD=2):
+        fused_case(gen.workload(2, B=2, T=230, D=40, io=io, h0_std=0.1), K=50, chunk_len=50, kd=2, tpar=0)
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
 def test_fused_unaligned_channels_and_rebuild(io):
     D = 37 if io == "f32" else 20
     fused_case(gen.workload(2, B=2, T=77, D=D, io=io, h0_std=0.1), K=24, rebuild=True)

@@ -52,11 +52,12 @@ def forced(var, value):
 
 
 def run_case(w, K, chunk_len=0, seed=0, ghT=False, bwd=True, lanes=None, ckpt_to_bwd=True, bwd_kd=None,
-             bwd_tpar=None, bwd_workspace=None, deterministic=False, fwd_layout=None):
+             bwd_tpar=None, bwd_workspace=None, deterministic=False, fwd_layout=None, chunk_kd=None):
     import torch
     inp = gen.make_inputs(w, seed=seed, with_grad_inputs=bwd, with_ghT=ghT)
     t = dev_inputs(inp)
-    with forced("SSM_SCAN_FORCE_LANES", lanes), forced("SSM_SCAN_FORCE_FWD_LAYOUT", fwd_layout):
+    with forced("SSM_SCAN_FORCE_LANES", lanes), forced("SSM_SCAN_FORCE_FWD_LAYOUT", fwd_layout), \
+            forced("SSM_SCAN_FORCE_CHUNK_KD", chunk_kd):
         y, hT, ckpt = ssm().ssm_scan_fwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], ckpt_interval=K,
                                          chunk_len=chunk_len)
     torch.cuda.synchronize()
@@ -186,9 +187,18 @@ def test_ragged_lengths_and_intervals(T, K, bwd_kd):
     run_case(gen.workload(2, B=2, T=T, D=40, h0_std=0.1), K=K, ghT=True, bwd_kd=bwd_kd)
 
 
+@pytest.mark.parametrize("chunk_kd", [1, 2])
 @pytest.mark.parametrize("chunk_len", [32, 50, 129])
-def test_chunked_ragged_chunks(chunk_len):
-    run_case(gen.workload(2, B=2, T=230, D=48, h0_std=0.1), K=64, chunk_len=chunk_len, bwd=False)
+def test_chunked_ragged_chunks(chunk_len, chunk_kd):
+    run_case(gen.workload(2, B=2, T=230, D=48, h0_std=0.1), K=64, chunk_len=chunk_len, bwd=False, chunk_kd=chunk_kd)
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_chunked_two_channels_per_lane_unaligned(io):
+    # an odd channel count leaves the last lane's second channel empty; bf16 rows of 20
+    # channels are not whole 16-byte chunks
+    D = 37 if io == "f32" else 20
+    run_case(gen.workload(2, B=3, T=300, D=D, io=io, h0_std=0.1), K=32, chunk_len=64, bwd=False, chunk_kd=2)
 
 
 def test_backward_rebuilds_checkpoints():

@@ -62,6 +62,7 @@ def draw_case(seed):
     }
     if case["io"] == "bf16" and case["D"] % 8 and r.integers(0, 2):
         case["D"] += 8 - case["D"] % 8           # both aligned and unaligned rows for bf16
+    case["chunk_kd"] = r.choice([None, 1, 2])    # channels per lane of the chunked forward
     return case
 
 
@@ -78,7 +79,7 @@ def test_random_case(seed):
     K = cs["K"]
     layout = cs["fwd"] if cs["fwd"] in ("2x2", "4x2", "4x1") else None
     chunk_len = cs["chunk_len"] if cs["fwd"] == "chunked" else (-1 if layout else 0)
-    with forced(SSM_SCAN_FORCE_FWD_LAYOUT=layout):
+    with forced(SSM_SCAN_FORCE_FWD_LAYOUT=layout, SSM_SCAN_FORCE_CHUNK_KD=cs["chunk_kd"]):
         y, hT, ck = ssm.ssm_scan_fwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], ckpt_interval=K,
                                      chunk_len=chunk_len, D_skip=Ds, delta_softplus=cs["softplus"])
     with forced(SSM_SCAN_FORCE_BWD_KD=cs["kd"], SSM_SCAN_FORCE_BWD_TPAR=cs["tpar"]):
