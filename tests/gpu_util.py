@@ -30,6 +30,8 @@ def maxrel(got, want):
     assert got.shape == want.shape, (got.shape, want.shape)
     if want.size == 0:
         return 0.0
+    if not np.all(np.isfinite(got)):
+        return float("inf")              # a NaN would compare as 'not greater' and pass silently
     return float(np.max(np.abs(got - want) / (1.0 + np.abs(want))))
 
 
