@@ -472,8 +472,11 @@ def other_workloads(torch, ssm, dev):
                           ckpt_interval=K2)
     ms_b = timed(lambda: ssm.ssm_scan_bwd(t2["x"], t2["delta"], t2["A"], t2["b"], t2["c"], t2["h0"], ck2,
                                           t2["dy"], ckpt_interval=K2, grads=g2))
+    ms_f_lb = timed(lambda: ssm.ssm_scan_fwd(t2["x"], t2["delta"], t2["A"], t2["b"], t2["c"], t2["h0"],
+                                             ckpt_interval=K2, y=y2, hT=h2, ckpt=ck2, lookback=True))
+    ssm.lookback_status()
     out[w2.name] = {"fwd_ms": ms_f, "bwd_ms": ms_b, "elem_per_s": gen.elements(w2) / ((ms_f + ms_b) / 1e3),
-                    "l2": "flushed"}
+                    "fwd_ms_lookback": ms_f_lb, "l2": "flushed"}
     del t2, y2, h2, ck2, g2, i2
     w3 = gen.workload(3)
     i3 = gen.make_inputs(w3)
@@ -508,10 +511,27 @@ def other_workloads(torch, ssm, dev):
     with torch.cuda.graph(g4, stream=sg4):
         f4()
     ms_graph = timed(g4.replay, reps=5)
+
+    def f4_lookback():
+        h = h04
+        for (x, d, b, c), yk in zip(parts, ys):
+            _, h, _ = ssm.ssm_scan_fwd(x, d, A4, b, c, h, y=yk, lookback=True)
+
+    ms_lb = timed(f4_lookback, reps=3)
+    with torch.cuda.stream(sg4):
+        f4_lookback()
+    torch.cuda.current_stream().wait_stream(sg4)
+    g4lb = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g4lb, stream=sg4):
+        f4_lookback()
+    ms_lb_graph = timed(g4lb.replay, reps=5)
+    ssm.lookback_status()
     out[w4.name] = {"fwd_ms": ms_graph, "elem_per_s": gen.elements(w4) / (ms_graph / 1e3), "calls": w4.T // L,
-                    "fwd_ms_eager_calls": ms, "launch": "16 chained calls replayed from one CUDA graph",
+                    "fwd_ms_eager_calls": ms, "fwd_ms_lookback": ms_lb_graph,
+                    "fwd_ms_lookback_eager_calls": ms_lb,
+                    "launch": "16 chained calls replayed from one CUDA graph; lookback: one launch per call",
                     "l2": "flushed before the 16 calls"}
-    del g4
+    del g4, g4lb
     # single-step decode at workload 5's width: one step per call, state in place; L2 flushed
     # before every step (the 5 MB state would otherwise stay in L2)
     wd = gen.workload(5, T=1)

@@ -66,7 +66,8 @@ typedef enum {
     SSM_ERR_UNSUPPORTED = 2,  /* DS != 16, D > 2^27, or more than 65535 forward chunks */
     SSM_ERR_MISALIGNED = 3,   /* a data pointer is not 16-byte aligned */
     SSM_ERR_WORKSPACE = 4,    /* workspace NULL or smaller than the query returned */
-    SSM_ERR_CUDA = 5          /* a CUDA runtime call or a launch failed */
+    SSM_ERR_CUDA = 5,         /* a CUDA runtime call or a launch failed */
+    SSM_ERR_TIMEOUT = 6       /* ssm_scan_fwd_lookback_status: a look-back wait ran out */
 } ssm_status;
 
 typedef struct {
@@ -77,7 +78,8 @@ typedef struct {
     int32_t chunk_len;      /* forward schedule: 0 = chosen by the library; > 0 = chunked
                                two-pass scan with chunks of this many steps; < 0 = one
                                pass over T. Every schedule computes the same function. */
-    int32_t flags;          /* SSM_SCAN_DETERMINISTIC | SSM_SCAN_DELTA_SOFTPLUS or 0;
+    int32_t flags;          /* SSM_SCAN_DETERMINISTIC | SSM_SCAN_DELTA_SOFTPLUS |
+                               SSM_SCAN_LOOKBACK or 0;
                                other bits must be 0 */
 } ssm_scan_desc;
 
@@ -95,6 +97,23 @@ typedef struct {
  * activation the model on the POPCORNBENCH trace page ("FW-GLM-5-1__l2_p30",
  * its forward() op list) applies to its delta projection before the scan. */
 #define SSM_SCAN_DELTA_SOFTPLUS 2
+
+/* ssm_scan_desc.flags: when the forward's schedule is chunked (chunk_len > 0,
+ * or chosen by the library for shapes with few (b, d) chains), run it as ONE
+ * launch with decoupled look-back (Merrill and Garland, "Single-pass Parallel
+ * Prefix Scan with Decoupled Look-back", 2016) instead of two: each chunk's CTA
+ * first publishes its affine map h -> exp(A sum(delta)) h + S (chunk 0: its
+ * end state from h0), then reads its predecessors' maps back to the nearest
+ * published end state, publishes its own end state and rescans its chunk with
+ * readout. CTAs take their order from a counter, so a CTA only ever waits for
+ * CTAs that started before it. Every wait is bounded (about a second of
+ * polling per CTA); a wait that runs out does not hang the GPU: the launch
+ * finishes, that chunk's outputs are wrong, and ssm_scan_fwd_lookback_status
+ * returns SSM_ERR_TIMEOUT. The workspace (ssm_scan_fwd_workspace_bytes with
+ * this flag set) holds the maps, end states and flags; the call zeroes the
+ * flags with cudaMemsetAsync before the launch. The one-pass schedule, the
+ * backward, ssm_scan_fwd_noalloc and ssm_scan_step ignore the flag. */
+#define SSM_SCAN_LOOKBACK 4
 
 /* Bytes of the checkpoint buffer: ceil(T/K)*B*D*DS*4, 0 when K == 0. */
 size_t ssm_scan_ckpt_bytes(const ssm_scan_desc* desc);
@@ -138,6 +157,17 @@ ssm_status ssm_scan_fwd(const ssm_scan_desc* desc,
                         const void* b, const void* c, const float* h0,
                         void* y, float* hT, float* ckpt,
                         void* workspace, size_t workspace_bytes, void* stream);
+
+/* After a forward call with SSM_SCAN_LOOKBACK whose schedule was chunked:
+ * waits for `stream` (cudaStreamSynchronize) and reads the count of look-back
+ * waits that ran out from `workspace` (the same workspace and desc as that
+ * call). SSM_OK when none ran out, or when desc's schedule is not the
+ * one-launch chunked scan (nothing waited); SSM_ERR_TIMEOUT otherwise (that
+ * call's y, hT and checkpoints are then not valid); SSM_ERR_WORKSPACE /
+ * SSM_ERR_MISALIGNED for a bad workspace; SSM_ERR_CUDA if the copy or the
+ * synchronisation failed. The count is reset by the next forward call. */
+ssm_status ssm_scan_fwd_lookback_status(const ssm_scan_desc* desc, const void* workspace,
+                                        size_t workspace_bytes, void* stream);
 
 /* Backward scan: gx, gdelta, gA, gb, gc, gh0 (all float32) for
  * L = sum dy*y + sum ghT*hT.

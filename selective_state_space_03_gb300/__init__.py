@@ -26,10 +26,10 @@ LIB_PATH = os.path.join(_PKG, "_lib", "libssm_scan.so")
 SSM_IO_F32, SSM_IO_BF16 = 0, 1
 MAX_BWD_CKPT_INTERVAL = 256   # longest checkpoint interval ssm_scan_bwd reads without a rebuild
 STATUS = {0: "SSM_OK", 1: "SSM_ERR_INVALID_ARG", 2: "SSM_ERR_UNSUPPORTED", 3: "SSM_ERR_MISALIGNED",
-          4: "SSM_ERR_WORKSPACE", 5: "SSM_ERR_CUDA"}
+          4: "SSM_ERR_WORKSPACE", 5: "SSM_ERR_CUDA", 6: "SSM_ERR_TIMEOUT"}
 EXPORTS = ("ssm_scan_ckpt_bytes", "ssm_scan_fwd_workspace_bytes", "ssm_scan_bwd_workspace_bytes",
            "ssm_scan_bwd_ckpt_workspace_bytes", "ssm_scan_fwd", "ssm_scan_bwd", "ssm_scan_fwd_fused",
-           "ssm_scan_bwd_fused", "ssm_scan_step", "ssm_status_str")
+           "ssm_scan_bwd_fused", "ssm_scan_step", "ssm_scan_fwd_lookback_status", "ssm_status_str")
 
 
 class ssm_scan_desc(ctypes.Structure):
@@ -70,6 +70,8 @@ def lib() -> ctypes.CDLL:
             L.ssm_scan_fwd_fused.restype = ctypes.c_int
             L.ssm_scan_bwd_fused.argtypes = [dp] + [vp] * 17 + [vp, sz, vp]
             L.ssm_scan_bwd_fused.restype = ctypes.c_int
+            L.ssm_scan_fwd_lookback_status.argtypes = [dp, vp, sz, vp]
+            L.ssm_scan_fwd_lookback_status.restype = ctypes.c_int
             L.ssm_status_str.argtypes = [ctypes.c_int]
             L.ssm_status_str.restype = ctypes.c_char_p
             _lib = L
@@ -125,14 +127,20 @@ def _workspace(nbytes, device):
 
 
 SSM_SCAN_DELTA_SOFTPLUS = 2
+SSM_SCAN_LOOKBACK = 4
+SSM_ERR_TIMEOUT = 6
+
+_last_lookback = {}     # device -> (desc, workspace) of the last forward call with lookback=True
 
 
 def ssm_scan_fwd(x, delta, A, b, c, h0=None, *, ckpt_interval=0, chunk_len=0, y=None, hT=None, ckpt=None,
-                 workspace=None, D_skip=None, delta_softplus=False, stream=None):
+                 workspace=None, D_skip=None, delta_softplus=False, lookback=False, stream=None):
     """Forward scan. Returns (y, hT, ckpt); ckpt is None when ckpt_interval == 0.
     delta_softplus=True: delta holds raw values, the scan uses softplus(delta)
     (SSM_SCAN_DELTA_SOFTPLUS). D_skip (D,) float32: y += D_skip * x, through
-    ssm_scan_fwd_fused."""
+    ssm_scan_fwd_fused. lookback=True sets SSM_SCAN_LOOKBACK (a chunked schedule
+    runs as one launch with decoupled look-back); lookback_status() then reports
+    whether any of its bounded waits ran out."""
     torch = _torch()
     B, T, D = x.shape
     DS = A.shape[1] if A.dim() == 2 else 16
@@ -144,7 +152,8 @@ def ssm_scan_fwd(x, delta, A, b, c, h0=None, *, ckpt_interval=0, chunk_len=0, y=
     _check(c, (B, T, DS), x.dtype, "c", dev)
     _check(h0, (B, D, DS), torch.float32, "h0", dev)
     _check(D_skip, (D,), torch.float32, "D_skip", dev)
-    desc = make_desc(B, T, D, DS, io, ckpt_interval, chunk_len, SSM_SCAN_DELTA_SOFTPLUS if delta_softplus else 0)
+    flags = (SSM_SCAN_DELTA_SOFTPLUS if delta_softplus else 0) | (SSM_SCAN_LOOKBACK if lookback else 0)
+    desc = make_desc(B, T, D, DS, io, ckpt_interval, chunk_len, flags)
     L = lib()
     if y is None:
         y = torch.empty((B, T, D), dtype=x.dtype, device=dev)
@@ -169,7 +178,24 @@ def ssm_scan_fwd(x, delta, A, b, c, h0=None, *, ckpt_interval=0, chunk_len=0, y=
                                   _stream(stream))
     if st != 0:
         raise SSMError(st, "ssm_scan_fwd")
+    if lookback:
+        _last_lookback[dev] = (desc, workspace, wsb, stream)
     return y, hT, ckpt
+
+
+def lookback_status(device=None):
+    """Waits for the last ssm_scan_fwd(..., lookback=True) call on `device` and
+    raises SSMError(SSM_ERR_TIMEOUT) if one of its look-back waits ran out
+    (ssm_scan_fwd_lookback_status). Returns None otherwise."""
+    torch = _torch()
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    if dev not in _last_lookback:
+        return None
+    desc, ws, wsb, stream = _last_lookback[dev]
+    st = lib().ssm_scan_fwd_lookback_status(ctypes.byref(desc), _ptr(ws), wsb, _stream(stream))
+    if st != 0:
+        raise SSMError(st, "ssm_scan_fwd_lookback_status")
+    return None
 
 
 def ssm_scan_bwd(x, delta, A, b, c, h0, ckpt, dy, ghT=None, *, ckpt_interval=0, grads=None, workspace=None,
@@ -326,4 +352,5 @@ _ScanFn = _Lazy()
 
 __all__ = ["lib", "ssm_scan_desc", "make_desc", "ssm_scan_fwd", "ssm_scan_bwd", "ssm_scan_step",
            "ssm_scan_fwd_noalloc", "selective_scan", "SSMError", "EXPORTS", "LIB_PATH", "SSM_IO_F32", "SSM_IO_BF16",
-           "SSM_SCAN_DETERMINISTIC", "SSM_SCAN_DELTA_SOFTPLUS"]
+           "SSM_SCAN_DETERMINISTIC", "SSM_SCAN_DELTA_SOFTPLUS", "SSM_SCAN_LOOKBACK", "SSM_ERR_TIMEOUT",
+           "lookback_status"]

@@ -39,7 +39,8 @@ ssm_status check_desc(const ssm_scan_desc* d) {
     if (d == nullptr) return SSM_ERR_INVALID_ARG;
     if (d->B < 0 || d->T < 0 || d->D < 0 || d->DS < 0) return SSM_ERR_INVALID_ARG;
     if (d->io != SSM_IO_F32 && d->io != SSM_IO_BF16) return SSM_ERR_INVALID_ARG;
-    if (d->ckpt_interval < 0 || (d->flags & ~(SSM_SCAN_DETERMINISTIC | SSM_SCAN_DELTA_SOFTPLUS)) != 0) return SSM_ERR_INVALID_ARG;
+    constexpr int32_t kFlags = SSM_SCAN_DETERMINISTIC | SSM_SCAN_DELTA_SOFTPLUS | SSM_SCAN_LOOKBACK;
+    if (d->ckpt_interval < 0 || (d->flags & ~kFlags) != 0) return SSM_ERR_INVALID_ARG;
     if (d->B > 65535) return SSM_ERR_INVALID_ARG;
     if (d->DS != kDS) return SSM_ERR_UNSUPPORTED;
     if (d->D > kMaxD) return SSM_ERR_UNSUPPORTED;     // kernels use 32-bit in-tile offsets
@@ -52,16 +53,28 @@ int64_t io_size(const ssm_scan_desc& d) { return d.io == SSM_IO_BF16 ? 2 : 4; }
 bool vec_ok(const ssm_scan_desc& d) { return (d.D * io_size(d)) % 16 == 0; }
 
 struct FwdPlan {
-    int mode;        // kSingle (0) or chunked (2, meaning pass 1 + pass 2)
+    int mode;        // kSingle (0), chunked (2, meaning pass 1 + pass 2) or chunked in one launch (4)
     int G;
     int kd;          // channels per lane of the G = 4 layout (1 or 2)
     int64_t Lc;
     int64_t nchunk;
-    size_t ws_S, ws_Sd;   // byte sizes of the two workspace arrays
+    size_t ws_S, ws_Sd;   // byte sizes of the two workspace arrays (mode 2)
+    // mode 4: maps, inclusive states, delta sums, then the zeroed block (flags, ticket, status)
+    size_t lb_S, lb_X, lb_Sd, lb_zero;
+    size_t ws_total() const { return mode == 4 ? lb_S + lb_X + lb_Sd + lb_zero : ws_S + ws_Sd; }
 };
 
+// polls of a predecessor's flag before a look-back wait gives up (about a second)
+int64_t lookback_polls() {
+    if (const char* env = std::getenv("SSM_SCAN_LOOKBACK_POLLS")) {     // testing aid
+        const long long v = std::atoll(env);
+        if (v > 0) return v;
+    }
+    return int64_t(1) << 20;
+}
+
 FwdPlan plan_fwd(const ssm_scan_desc& d) {
-    FwdPlan P{0, 4, 1, d.T, 1, 0, 0};
+    FwdPlan P{0, 4, 1, d.T, 1, 0, 0, 0, 0, 0, 0};
     const int64_t chains = d.B * d.D;
     const int64_t want = int64_t(device_sm_count()) * 512;   // ~16 resident warps per SM
     bool chunked = false;
@@ -80,6 +93,15 @@ FwdPlan plan_fwd(const ssm_scan_desc& d) {
         P.nchunk = cdiv(d.T, cs.Lc);
         P.ws_S = align_up(size_t(d.B) * size_t(P.nchunk - 1) * size_t(d.D) * kDS * 4);
         P.ws_Sd = align_up(size_t(d.B) * size_t(P.nchunk - 1) * size_t(d.D) * 4);
+        if (d.flags & SSM_SCAN_LOOKBACK) {
+            P.mode = 4;
+            const size_t rows = size_t(d.B) * size_t(P.nchunk) * size_t(d.D);
+            const size_t nblk = size_t(cdiv(d.D, 8 * P.kd));
+            P.lb_S = align_up(rows * kDS * 4);
+            P.lb_X = align_up(rows * kDS * 4);
+            P.lb_Sd = align_up(rows * 4);
+            P.lb_zero = align_up((size_t(P.nchunk) + 1) * size_t(d.B) * nblk * 4 + 16);
+        }
     } else {
         // Lane layout: the most channels per warp (fewest lanes re-reading each b, c value
         // from shared memory) that still keeps enough warps resident: 2 lanes per chain x 2
@@ -191,6 +213,7 @@ const char* ssm_status_str(ssm_status s) {
         case SSM_ERR_MISALIGNED: return "pointer not 16-byte aligned";
         case SSM_ERR_WORKSPACE: return "workspace missing or too small";
         case SSM_ERR_CUDA: return "CUDA error";
+        case SSM_ERR_TIMEOUT: return "a look-back wait of the one-launch chunked scan ran out";
     }
     return "unknown status";
 }
@@ -203,7 +226,7 @@ size_t ssm_scan_ckpt_bytes(const ssm_scan_desc* d) {
 size_t ssm_scan_fwd_workspace_bytes(const ssm_scan_desc* d) {
     if (check_desc(d) != SSM_OK || d->B == 0 || d->T == 0 || d->D == 0) return 0;
     const FwdPlan P = plan_fwd(*d);
-    return P.mode == 2 ? P.ws_S + P.ws_Sd : 0;
+    return P.mode == 0 ? 0 : P.ws_total();
 }
 
 size_t ssm_scan_bwd_ckpt_workspace_bytes(const ssm_scan_desc* d) {
@@ -239,8 +262,8 @@ ssm_status ssm_scan_fwd_fused(const ssm_scan_desc* desc, const void* x, const vo
         return SSM_OK;
     }
     const FwdPlan P = plan_fwd(d);
-    if (P.mode == 2 && P.nchunk > kMaxChunks) return SSM_ERR_UNSUPPORTED;   // one grid dimension per chunk
-    if (P.mode == 2 && (workspace == nullptr || workspace_bytes < P.ws_S + P.ws_Sd)) return SSM_ERR_WORKSPACE;
+    if (P.mode != 0 && P.nchunk > kMaxChunks) return SSM_ERR_UNSUPPORTED;   // one grid dimension per chunk
+    if (P.mode != 0 && (workspace == nullptr || workspace_bytes < P.ws_total())) return SSM_ERR_WORKSPACE;
     if (workspace && !aligned16(workspace)) return SSM_ERR_MISALIGNED;
 
     FwdLaunch L{};
@@ -262,12 +285,45 @@ ssm_status ssm_scan_fwd_fused(const ssm_scan_desc* desc, const void* x, const vo
         L.ws_Sd = reinterpret_cast<float*>(static_cast<char*>(workspace) + P.ws_S);
         e = run_fwd(d, L, 1, s);
         if (e == cudaSuccess) e = run_fwd(d, L, 2, s);
+    } else if (P.mode == 4) {
+        char* w = static_cast<char*>(workspace);
+        L.Lc = P.Lc;
+        L.nchunk = P.nchunk;
+        L.lb_S = reinterpret_cast<float*>(w);
+        L.lb_X = reinterpret_cast<float*>(w + P.lb_S);
+        L.lb_Sd = reinterpret_cast<float*>(w + P.lb_S + P.lb_X);
+        char* z = w + P.lb_S + P.lb_X + P.lb_Sd;      // status (4 B), pad, flags, tickets
+        const size_t nblk = size_t(cdiv(d.D, 8 * P.kd));
+        L.lb_status = reinterpret_cast<unsigned int*>(z + 8);
+        L.lb_flags = reinterpret_cast<int*>(z + 16);
+        L.lb_ticket = reinterpret_cast<int*>(z + 16 + size_t(P.nchunk) * size_t(d.B) * nblk * 4);
+        L.lb_polls = lookback_polls();
+        L.lb_test_drop = std::getenv("SSM_SCAN_TEST_LOOKBACK_DROP") != nullptr;   // testing aid
+        e = cudaMemsetAsync(z, 0, P.lb_zero, s);
+        if (e == cudaSuccess) e = run_fwd(d, L, 4, s);
     } else {
         L.Lc = d.T;
         L.nchunk = 1;
         e = run_fwd(d, L, 0, s);
     }
     return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+ssm_status ssm_scan_fwd_lookback_status(const ssm_scan_desc* desc, const void* workspace, size_t workspace_bytes,
+                                         void* stream) {
+    ssm_status st = check_desc(desc);
+    if (st != SSM_OK) return st;
+    const FwdPlan P = plan_fwd(*desc);
+    if (P.mode != 4 || desc->B == 0 || desc->T == 0 || desc->D == 0) return SSM_OK;    // nothing waited
+    // the status word's place does not depend on the lane layout (which sizes the flags)
+    if (workspace == nullptr || workspace_bytes < P.lb_S + P.lb_X + P.lb_Sd + 16) return SSM_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return SSM_ERR_MISALIGNED;
+    unsigned int n = 0;
+    const char* z = static_cast<const char*>(workspace) + P.lb_S + P.lb_X + P.lb_Sd;
+    if (cudaMemcpyAsync(&n, z + 8, sizeof(n), cudaMemcpyDeviceToHost, static_cast<cudaStream_t>(stream)) != cudaSuccess ||
+        cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return SSM_ERR_CUDA;
+    return n == 0 ? SSM_OK : SSM_ERR_TIMEOUT;
 }
 
 ssm_status ssm_scan_fwd(const ssm_scan_desc* desc, const void* x, const void* delta, const float* A,

@@ -41,7 +41,7 @@
 
 namespace ssm {
 
-enum FwdMode { kSingle = 0, kPass1 = 1, kPass2 = 2, kCkptOnly = 3 };
+enum FwdMode { kSingle = 0, kPass1 = 1, kPass2 = 2, kCkptOnly = 3, kLookback = 4 };
 
 template <typename TIO, int G, int KD>
 struct FwdCfg {
@@ -74,8 +74,28 @@ struct FwdCfg {
     static_assert(X_CPR >= 1 && DT % EPC == 0, "tile rows must be whole 16-byte chunks");
 };
 
+// The lane's KD x KS states into a (.., D, 16) array (rows of chains b * D + d).
+template <int G, int KD>
+__device__ __forceinline__ void store_lane_states(float* base, int64_t b, int64_t D, int64_t dfirst, int s0,
+                                                  const bool (&valid)[KD], const float2 (&h)[KD][kDS / G / 2]) {
+#pragma unroll
+    for (int k = 0; k < KD; ++k) {
+        if (!valid[k]) continue;
+        float4* dst = reinterpret_cast<float4*>(base + (b * D + dfirst + k) * kDS + s0);
+#pragma unroll
+        for (int q = 0; q < kDS / G / 2; q += 2)
+            dst[q / 2] = make_float4(h[k][q].x, h[k][q].y, h[k][q + 1].x, h[k][q + 1].y);
+    }
+}
+
+// One sweep of one warp over steps [t_begin, t_end) of batch b, channels d0 .. d0 + DT - 1,
+// starting from the state in h and leaving the end state there. MODE selects the work:
+// kSingle / kPass2 read out y (and write checkpoints), kPass1 adds up delta per channel into
+// dsum (no readout, no checkpoints), kCkptOnly writes checkpoints only.
 template <typename TIO, int G, int KD, bool VEC, int MODE, bool CKT, bool FUSE>
-__global__ void __launch_bounds__(32, FwdCfg<TIO, G, KD>::MINB) fwd_kernel(const FwdLaunch p) {
+__device__ __forceinline__ void fwd_sweep(const FwdLaunch& p, int64_t b, int64_t d0, int64_t t_begin, int64_t t_end,
+                                          const float2 (&A2)[KD][FwdCfg<TIO, G, KD>::KP], const bool (&valid)[KD],
+                                          float2 (&h)[KD][FwdCfg<TIO, G, KD>::KP], float (&dsum)[KD]) {
     using C = FwdCfg<TIO, G, KD>;
     constexpr int NT = C::NT, KS = C::KS, KP = C::KP, DT = C::DT, TT = C::TT, EPC = C::EPC;
     constexpr bool READ = (MODE == kSingle || MODE == kPass2);
@@ -95,12 +115,6 @@ __global__ void __launch_bounds__(32, FwdCfg<TIO, G, KD>::MINB) fwd_kernel(const
     const int c0 = (lane / G) * KD;          // first channel of this lane within the CTA
     const int s0 = gl * KS;
     const int64_t T = p.T, D = p.D;
-    const int64_t b = blockIdx.z;
-    const int64_t d0 = int64_t(blockIdx.x) * DT;
-    const int64_t nprev = p.nchunk - 1;      // chunks with a stored carry
-    const int64_t chunk = (MODE == kPass1 || MODE == kPass2) ? int64_t(blockIdx.y) : 0;
-    const int64_t t_begin = chunk * p.Lc;
-    const int64_t t_end = (MODE == kPass1 || MODE == kPass2) ? min(T, t_begin + p.Lc) : T;
     const bool full_d = d0 + DT <= D;
 
     const TIO* xg = static_cast<const TIO*>(p.x) + b * T * D;
@@ -109,40 +123,6 @@ __global__ void __launch_bounds__(32, FwdCfg<TIO, G, KD>::MINB) fwd_kernel(const
     const TIO* cgl = static_cast<const TIO*>(p.c) + b * T * kDS;
     TIO* yg = static_cast<TIO*>(p.y) + b * T * D;
 
-    bool valid[KD];
-    float2 A2[KD][KP], h[KD][KP];
-#pragma unroll
-    for (int k = 0; k < KD; ++k) {
-        const int64_t d = d0 + c0 + k;
-        valid[k] = d < D;
-#pragma unroll
-        for (int q = 0; q < KP; ++q) {
-            A2[k][q] = valid[k] ? make_float2(p.A[d * kDS + s0 + 2 * q] * kLog2e, p.A[d * kDS + s0 + 2 * q + 1] * kLog2e)
-                                : make_float2(0.f, 0.f);
-            h[k][q] = make_float2(0.f, 0.f);
-        }
-        if (MODE != kPass1 && valid[k] && p.h0 != nullptr) {
-            const float* src = p.h0 + (b * D + d) * kDS + s0;
-#pragma unroll
-            for (int q = 0; q < KP; ++q) h[k][q] = make_float2(src[2 * q], src[2 * q + 1]);
-        }
-        if (MODE == kPass2 && valid[k]) {
-            // start state of this chunk: fold the carries of the chunks before it
-            for (int64_t j = 0; j < chunk; ++j) {
-                const int64_t row = (b * nprev + j) * D + d;
-                const float sd = p.ws_Sd[row];
-                const float* S = p.ws_S + row * kDS + s0;
-#pragma unroll
-                for (int q = 0; q < KP; ++q) {
-                    const float2 P = make_float2(ex2(A2[k][q].x * sd), ex2(A2[k][q].y * sd));
-                    h[k][q] = __ffma2_rn(P, h[k][q], make_float2(S[2 * q], S[2 * q + 1]));
-                }
-            }
-        }
-    }
-    float dsum[KD];
-#pragma unroll
-    for (int k = 0; k < KD; ++k) dsum[k] = 0.f;
     // Readout: with G = 4 the lanes of a chain group each finish one step of every G steps,
     // for all KD channels; with G = 2 each finishes KD / 2 of the channels, every step.
     constexpr bool BY_STEP = (G == 4);
@@ -198,16 +178,7 @@ __global__ void __launch_bounds__(32, FwdCfg<TIO, G, KD>::MINB) fwd_kernel(const
             if (READ) stage_tile<TIO, TT, kDS, NT, true>(csr + buf * TT * kDS, cgl, kDS, t0, t_end, 0);
         }
     };
-    auto store_state = [&](float* base) {     // the lane's KD x KS states into a (.., D, 16) array
-#pragma unroll
-        for (int k = 0; k < KD; ++k) {
-            if (!valid[k]) continue;
-            float4* dst = reinterpret_cast<float4*>(base + (b * D + d0 + c0 + k) * kDS + s0);
-#pragma unroll
-            for (int q = 0; q < KP; q += 2)
-                dst[q / 2] = make_float4(h[k][q].x, h[k][q].y, h[k][q + 1].x, h[k][q + 1].y);
-        }
-    };
+    auto store_state = [&](float* base) { store_lane_states<G, KD>(base, b, D, d0 + c0, s0, valid, h); };
 
     if (ntiles > 0) {
         stage(0, 0);
@@ -368,6 +339,74 @@ __global__ void __launch_bounds__(32, FwdCfg<TIO, G, KD>::MINB) fwd_kernel(const
         }
     }
 
+}
+
+// Lane layout, A * log2(e) and the start state of the lane's chains (channels d0 + c0 + k).
+template <typename TIO, int G, int KD>
+__device__ __forceinline__ void fwd_lane_setup(const FwdLaunch& p, int64_t b, int64_t d0, bool with_h0,
+                                               bool (&valid)[KD], float2 (&A2)[KD][FwdCfg<TIO, G, KD>::KP],
+                                               float2 (&h)[KD][FwdCfg<TIO, G, KD>::KP]) {
+    constexpr int KP = FwdCfg<TIO, G, KD>::KP, KS = FwdCfg<TIO, G, KD>::KS;
+    const int lane = threadIdx.x;
+    const int c0 = (lane / G) * KD, s0 = (lane % G) * KS;
+#pragma unroll
+    for (int k = 0; k < KD; ++k) {
+        const int64_t d = d0 + c0 + k;
+        valid[k] = d < p.D;
+#pragma unroll
+        for (int q = 0; q < KP; ++q) {
+            A2[k][q] = valid[k] ? make_float2(p.A[d * kDS + s0 + 2 * q] * kLog2e, p.A[d * kDS + s0 + 2 * q + 1] * kLog2e)
+                                : make_float2(0.f, 0.f);
+            h[k][q] = make_float2(0.f, 0.f);
+        }
+        if (with_h0 && valid[k] && p.h0 != nullptr) {
+            const float* src = p.h0 + (b * p.D + d) * kDS + s0;
+#pragma unroll
+            for (int q = 0; q < KP; ++q) h[k][q] = make_float2(src[2 * q], src[2 * q + 1]);
+        }
+    }
+}
+
+template <typename TIO, int G, int KD, bool VEC, int MODE, bool CKT, bool FUSE>
+__global__ void __launch_bounds__(32, FwdCfg<TIO, G, KD>::MINB) fwd_kernel(const FwdLaunch p) {
+    using C = FwdCfg<TIO, G, KD>;
+    constexpr int KP = C::KP, KS = C::KS;
+    const int lane = threadIdx.x;
+    const int gl = lane % G, c0 = (lane / G) * KD, s0 = gl * KS;
+    const int64_t D = p.D;
+    const int64_t b = blockIdx.z;
+    const int64_t d0 = int64_t(blockIdx.x) * C::DT;
+    const int64_t nprev = p.nchunk - 1;      // chunks with a stored carry
+    const int64_t chunk = (MODE == kPass1 || MODE == kPass2) ? int64_t(blockIdx.y) : 0;
+    const int64_t t_begin = chunk * p.Lc;
+    const int64_t t_end = (MODE == kPass1 || MODE == kPass2) ? min(p.T, t_begin + p.Lc) : p.T;
+
+    bool valid[KD];
+    float2 A2[KD][KP], h[KD][KP];
+    fwd_lane_setup<TIO, G, KD>(p, b, d0, MODE != kPass1, valid, A2, h);
+    if (MODE == kPass2) {
+        // start state of this chunk: fold the carries of the chunks before it
+#pragma unroll
+        for (int k = 0; k < KD; ++k) {
+            if (!valid[k]) continue;
+            for (int64_t j = 0; j < chunk; ++j) {
+                const int64_t row = (b * nprev + j) * D + d0 + c0 + k;
+                const float sd = p.ws_Sd[row];
+                const float* S = p.ws_S + row * kDS + s0;
+#pragma unroll
+                for (int q = 0; q < KP; ++q) {
+                    const float2 P = make_float2(ex2(A2[k][q].x * sd), ex2(A2[k][q].y * sd));
+                    h[k][q] = __ffma2_rn(P, h[k][q], make_float2(S[2 * q], S[2 * q + 1]));
+                }
+            }
+        }
+    }
+    float dsum[KD];
+#pragma unroll
+    for (int k = 0; k < KD; ++k) dsum[k] = 0.f;
+
+    fwd_sweep<TIO, G, KD, VEC, MODE, CKT, FUSE>(p, b, d0, t_begin, t_end, A2, valid, h, dsum);
+
     if (MODE == kPass1) {
 #pragma unroll
         for (int k = 0; k < KD; ++k) {
@@ -381,7 +420,205 @@ __global__ void __launch_bounds__(32, FwdCfg<TIO, G, KD>::MINB) fwd_kernel(const
         return;
     }
     const bool last = (MODE != kPass2) || (chunk == p.nchunk - 1);
-    if (last && p.hT != nullptr) store_state(p.hT);
+    if (last && p.hT != nullptr) store_lane_states<G, KD>(p.hT, b, D, d0 + c0, s0, valid, h);
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* ptr) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_gpu(int* ptr, int v) {
+    asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
+}
+
+// The chunked scan in one launch, with decoupled look-back (the single-pass prefix scan of
+// Merrill and Garland, 2016, applied to the affine chunk maps h -> exp(A sum(delta)) h + S):
+//  1. a CTA of chain block (b, d-block) takes the next ticket of that block's counter as its
+//     chunk, so every CTA it will wait for took an earlier ticket and is already running;
+//  2. chunks before the last sweep once without readout: chunk 0 from h0 (its end state is
+//     the inclusive state, published with flag 2), the others from 0 (their map: end state S
+//     and delta sum, published with flag 1);
+//  3. a chunk k > 0 walks back over k-1, k-2, ...: it folds in each map published there until
+//     it reaches an inclusive state, which gives its start state; it then publishes its own
+//     inclusive state (flag 2);
+//  4. every chunk rescans from its start state with readout, as pass 2 of the two-launch
+//     schedule does.
+// Each wait polls a flag at most lb_polls times per CTA; a wait that runs out adds 1 to
+// lb_status and the chunk carries on with the part of the prefix it has, so the launch always
+// finishes (with wrong values for that chunk) and the host can report the failure.
+template <typename TIO, int KD, bool VEC, bool CKT, bool FUSE>
+__global__ void __launch_bounds__(32, FwdCfg<TIO, 4, KD>::MINB) fwd_lookback_kernel(const FwdLaunch p) {
+    constexpr int G = 4;
+    using C = FwdCfg<TIO, G, KD>;
+    constexpr int KP = C::KP, KS = C::KS;
+    const int lane = threadIdx.x;
+    const int c0 = (lane / G) * KD, s0 = (lane % G) * KS;
+    const int64_t D = p.D, B = p.B, nch = p.nchunk;
+    const int64_t nblk = (D + C::DT - 1) / C::DT;
+
+    // the chain block is the CTA's; its chunk is a ticket from the block's own counter
+    const int64_t b = blockIdx.y, dblk = blockIdx.x, d0 = dblk * C::DT;
+    int tk = 0;
+    if (lane == 0) tk = atomicAdd(p.lb_ticket + b * nblk + dblk, 1);
+    const int64_t chunk = __shfl_sync(0xffffffffu, tk, 0);
+    const int64_t rem = dblk;
+    const int64_t t_begin = chunk * p.Lc, t_end = min(p.T, t_begin + p.Lc);
+    const bool last = chunk == nch - 1;
+    int* my_flag = p.lb_flags + (chunk * B + b) * nblk + rem % nblk;
+    auto row = [&](int64_t j, int k) { return (b * nch + j) * D + d0 + c0 + k; };
+
+    bool valid[KD];
+    float2 A2[KD][KP], h[KD][KP], hin[KD][KP];
+    fwd_lane_setup<TIO, G, KD>(p, b, d0, chunk == 0, valid, A2, hin);   // hin = h0 for chunk 0, else 0
+    float dsum[KD];
+#pragma unroll
+    for (int k = 0; k < KD; ++k) {
+        dsum[k] = 0.f;
+#pragma unroll
+        for (int q = 0; q < KP; ++q) h[k][q] = hin[k][q];
+    }
+
+    // 2. the chunk's map (or, for chunk 0, its inclusive state)
+    if (!last) {
+        fwd_sweep<TIO, G, KD, VEC, kPass1, CKT, FUSE>(p, b, d0, t_begin, t_end, A2, valid, h, dsum);
+        float* dst = chunk == 0 ? p.lb_X : p.lb_S;
+#pragma unroll
+        for (int k = 0; k < KD; ++k) {
+            if (!valid[k]) continue;
+            float4* o = reinterpret_cast<float4*>(dst + row(chunk, k) * kDS + s0);
+#pragma unroll
+            for (int q = 0; q < KP; q += 2) o[q / 2] = make_float4(h[k][q].x, h[k][q].y, h[k][q + 1].x, h[k][q + 1].y);
+            if (lane % G == 0) p.lb_Sd[row(chunk, k)] = dsum[k];
+        }
+        __threadfence();
+        __syncwarp();
+        if (lane == 0 && !(p.lb_test_drop && chunk == 0)) st_release_gpu(my_flag, chunk == 0 ? 2 : 1);
+    }
+
+    // 3. look back for the start state
+    if (chunk > 0) {
+        float sdacc[KD];
+        float2 sacc[KD][KP];
+#pragma unroll
+        for (int k = 0; k < KD; ++k) {
+            sdacc[k] = 0.f;
+#pragma unroll
+            for (int q = 0; q < KP; ++q) sacc[k][q] = make_float2(0.f, 0.f);
+        }
+        // Windowed look-back: lane i probes the flag of predecessor j - i, so one round trip
+        // sees 32 predecessors; the maps up to the nearest unpublished one or the nearest
+        // inclusive state are then folded, their loads issued NB predecessors at a time.
+        constexpr int NB = 4;
+        int64_t polls = 0;
+        bool timed_out = false;
+        int64_t j = chunk - 1;                   // nearest predecessor not yet folded
+        while (true) {
+            const int64_t jl = j - lane;
+            int f = 0;
+            if (jl >= 0) f = ld_acquire_gpu(p.lb_flags + (jl * B + b) * nblk + rem % nblk);
+            const unsigned zero = __ballot_sync(0xffffffffu, jl >= 0 && f == 0);
+            const unsigned incl = __ballot_sync(0xffffffffu, jl >= 0 && f == 2);
+            // (chunk 0 publishes flag 2 only, so a window reaching it always stops there)
+            const unsigned stop = zero | incl;
+            const int first = stop ? __ffs(int(stop)) - 1 : 32;
+            const bool done = first < 32 && ((incl >> first) & 1u);
+            const int n = first + (done ? 1 : 0);          // predecessors to fold now (warp-uniform)
+            for (int i0 = 0; i0 < n; i0 += NB) {
+                float2 v[NB][KD][KP];
+                float sdv[NB][KD];
+#pragma unroll
+                for (int u = 0; u < NB; ++u) {
+                    const int i = i0 + u;
+                    const int fi = __shfl_sync(0xffffffffu, f, i & 31);
+#pragma unroll
+                    for (int k = 0; k < KD; ++k) {
+                        sdv[u][k] = 0.f;
+#pragma unroll
+                        for (int q = 0; q < KP; ++q) v[u][k][q] = make_float2(0.f, 0.f);
+                        if (i >= n || !valid[k]) continue;
+                        const float* src = (fi == 2 ? p.lb_X : p.lb_S) + row(j - i, k) * kDS + s0;
+#pragma unroll
+                        for (int q = 0; q < KP; ++q) v[u][k][q] = __ldcg(reinterpret_cast<const float2*>(src) + q);
+                        if (fi == 1) sdv[u][k] = __ldcg(p.lb_Sd + row(j - i, k));
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < NB; ++u) {
+                    if (i0 + u >= n) break;
+#pragma unroll
+                    for (int k = 0; k < KD; ++k) {
+#pragma unroll
+                        for (int q = 0; q < KP; ++q) {
+                            // fold predecessor j - i in front of the later ones
+                            const float2 P = make_float2(ex2(A2[k][q].x * sdacc[k]), ex2(A2[k][q].y * sdacc[k]));
+                            sacc[k][q] = __ffma2_rn(P, v[u][k][q], sacc[k][q]);
+                        }
+                        sdacc[k] += sdv[u][k];
+                    }
+                }
+            }
+            if (done) break;
+            j -= n;
+            if (n == 0) {                                  // the nearest predecessor has not published yet
+                if (polls >= p.lb_polls) {
+                    timed_out = true;
+                    break;
+                }
+                ++polls;
+                __nanosleep(128);
+            }
+        }
+        if (timed_out && lane == 0) atomicAdd(p.lb_status, 1u);
+#pragma unroll
+        for (int k = 0; k < KD; ++k)
+#pragma unroll
+            for (int q = 0; q < KP; ++q) hin[k][q] = sacc[k][q];
+        if (!last) {
+            // inclusive state of this chunk: exp(A dsum) hin + S (h holds S)
+#pragma unroll
+            for (int k = 0; k < KD; ++k) {
+                if (!valid[k]) continue;
+                float4* o = reinterpret_cast<float4*>(p.lb_X + row(chunk, k) * kDS + s0);
+#pragma unroll
+                for (int q = 0; q < KP; q += 2) {
+                    float2 x2[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const float2 P = make_float2(ex2(A2[k][q + u].x * dsum[k]), ex2(A2[k][q + u].y * dsum[k]));
+                        x2[u] = __ffma2_rn(P, hin[k][q + u], h[k][q + u]);
+                    }
+                    o[q / 2] = make_float4(x2[0].x, x2[0].y, x2[1].x, x2[1].y);
+                }
+            }
+            __threadfence();
+            __syncwarp();
+            if (lane == 0) st_release_gpu(my_flag, 2);
+        }
+    }
+
+    // 4. rescan with readout from the start state
+    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < KD; ++k)
+#pragma unroll
+        for (int q = 0; q < KP; ++q) h[k][q] = hin[k][q];
+    fwd_sweep<TIO, G, KD, VEC, kPass2, CKT, FUSE>(p, b, d0, t_begin, t_end, A2, valid, h, dsum);
+    if (last && p.hT != nullptr) store_lane_states<G, KD>(p.hT, b, D, d0 + c0, s0, valid, h);
+}
+
+template <typename TIO, int KD, bool VEC, bool CKT, bool FUSE>
+cudaError_t launch_fwd_lookback_t(const FwdLaunch& L, cudaStream_t stream) {
+    using C = FwdCfg<TIO, 4, KD>;
+    constexpr size_t smem = FUSE ? C::SMEM_FUSE : C::SMEM;
+    auto kern = fwd_lookback_kernel<TIO, KD, VEC, CKT, FUSE>;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        if (e != cudaSuccess) return e;
+    }
+    const dim3 grid(unsigned((L.D + C::DT - 1) / C::DT), unsigned(L.B), unsigned(L.nchunk));
+    kern<<<grid, C::NT, smem, stream>>>(L);
+    return cudaGetLastError();
 }
 
 template <typename TIO, int G, int KD, bool VEC, int MODE, bool CKT, bool FUSE>
@@ -407,6 +644,7 @@ template <typename TIO, bool FUSE>
 cudaError_t launch_fwd_fuse(const FwdLaunch& L, int mode, cudaStream_t stream) {
     constexpr int TT = FwdCfg<TIO, 4, 1>::TT;
     const bool ckt = L.K == 0 || (L.K % TT == 0 && (mode == kSingle || mode == kCkptOnly || L.Lc % TT == 0));
+    // (kLookback sweeps chunks of L.Lc steps like kPass2)
 #define SSM_FWD_CK(G_, KD_, MODE_, VEC_)                                                   \
     return ckt ? launch_fwd_t<TIO, G_, KD_, VEC_, MODE_, true, FUSE>(L, stream)           \
                : launch_fwd_t<TIO, G_, KD_, VEC_, MODE_, false, FUSE>(L, stream)
@@ -428,6 +666,15 @@ cudaError_t launch_fwd_fuse(const FwdLaunch& L, int mode, cudaStream_t stream) {
             if (L.kd == 2) { SSM_FWD_VEC(4, 2, kPass2); }
             SSM_FWD_VEC(4, 1, kPass2);
         case kCkptOnly: SSM_FWD_VEC(4, 1, kCkptOnly);
+        case kLookback:
+#define SSM_FWD_LB(KD_, VEC_) \
+    return ckt ? launch_fwd_lookback_t<TIO, KD_, VEC_, true, FUSE>(L, stream) \
+               : launch_fwd_lookback_t<TIO, KD_, VEC_, false, FUSE>(L, stream)
+            if (L.kd == 2) {
+                if (L.vec) { SSM_FWD_LB(2, true); } else { SSM_FWD_LB(2, false); }
+            }
+            if (L.vec) { SSM_FWD_LB(1, true); } else { SSM_FWD_LB(1, false); }
+#undef SSM_FWD_LB
         default: return cudaErrorInvalidValue;
     }
 #undef SSM_FWD_VEC

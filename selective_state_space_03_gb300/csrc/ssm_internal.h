@@ -43,6 +43,15 @@ struct FwdLaunch {
     // fused prologue / epilogue (the fused kernel variants only)
     bool softplus;       // delta holds raw values; the scan uses softplus(delta)
     const float* Dskip;  // (D) or null: y += Dskip[d] * x
+    // chunked scan in one launch with decoupled look-back (mode 4)
+    float* lb_S;                    // [B][nchunk][D][16] chunk maps' offsets (end state from a zero start)
+    float* lb_X;                    // [B][nchunk][D][16] inclusive states (state after the chunk)
+    float* lb_Sd;                   // [B][nchunk][D] delta sums of the chunks
+    int* lb_flags;                  // [nchunk][B][nblk]: 0 nothing, 1 map, 2 inclusive state published
+    int* lb_ticket;                 // [B][nblk] next chunk of each chain block, taken in launch order
+    unsigned int* lb_status;        // number of waits that ran out (0 after a good launch)
+    int64_t lb_polls;               // polls of a predecessor's flag (per CTA) before giving up
+    bool lb_test_drop;              // testing aid: chunk 0 publishes nothing, so its successors time out
 };
 
 cudaError_t launch_fwd_f32(const FwdLaunch& L, int mode, cudaStream_t stream);

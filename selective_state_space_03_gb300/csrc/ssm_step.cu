@@ -85,7 +85,7 @@ extern "C" ssm_status ssm_scan_step(const ssm_scan_desc* desc, const void* x, co
     const ssm_scan_desc& d = *desc;
     if (d.B < 0 || d.D < 0 || d.DS < 0 || d.T != 1) return SSM_ERR_INVALID_ARG;
     if (d.io != SSM_IO_F32 && d.io != SSM_IO_BF16) return SSM_ERR_INVALID_ARG;
-    if (d.ckpt_interval < 0 || (d.flags & ~(SSM_SCAN_DETERMINISTIC | SSM_SCAN_DELTA_SOFTPLUS)) != 0 || d.B > 65535) return SSM_ERR_INVALID_ARG;
+    if (d.ckpt_interval < 0 || (d.flags & ~(SSM_SCAN_DETERMINISTIC | SSM_SCAN_DELTA_SOFTPLUS | SSM_SCAN_LOOKBACK)) != 0 || d.B > 65535) return SSM_ERR_INVALID_ARG;
     if (d.DS != kDS || d.D > kMaxD) return SSM_ERR_UNSUPPORTED;
     if (d.B == 0 || d.D == 0) return SSM_OK;
     if (!x || !delta || !A || !b || !c || !h || !y) return SSM_ERR_INVALID_ARG;

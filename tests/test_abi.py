@@ -72,8 +72,9 @@ def bwd(L, d, ckpt=FAKE, ws=None, wsb=0, **kw):
 
 
 def test_status_strings(L):
-    for s in range(6):
+    for s in range(7):
         assert L.ssm_status_str(s)
+    assert b"look-back" in L.ssm_status_str(6)
     assert b"DS" in L.ssm_status_str(2)
 
 
@@ -85,7 +86,7 @@ def test_invalid_descriptors(L):
     assert fwd(L, desc(ckpt_interval=-1)) == 1
     assert fwd(L, desc(B=70000)) == 1
     d = desc()
-    d.flags = 6
+    d.flags = 8
     assert fwd(L, d) == 1
     assert fwd(L, desc(DS=8)) == 2
     assert fwd(L, desc(DS=32)) == 2
@@ -170,8 +171,8 @@ def test_deterministic_flag_workspace(L):
     # without the flag the same shape needs no workspace
     assert L.ssm_scan_bwd_ckpt_workspace_bytes(ctypes.byref(desc(B=2, T=100, D=320, ckpt_interval=100))) == 0
     # unknown flag bits are rejected
-    assert bwd(L, desc(flags=4)) == 1
-    assert step(L, desc(T=1, flags=4)) == 1
+    assert bwd(L, desc(flags=8)) == 1
+    assert step(L, desc(T=1, flags=8)) == 1
 
 
 def test_fused_entry_point_checks(L):
@@ -192,6 +193,29 @@ def test_fused_entry_point_checks(L):
     assert bwdf(gD=None) == 1                            # the skip weights' gradient is required
     assert bwdf(gD=FAKE + 8) == 3
     assert bwdf(dd=desc(flags=8)) == 1
+
+
+def test_lookback_flag_workspace_and_status(L):
+    # a chunked schedule with SSM_SCAN_LOOKBACK keeps every chunk's map and end state
+    d_lb = desc(B=1, T=4096, D=64, chunk_len=256, flags=4)
+    d_2p = desc(B=1, T=4096, D=64, chunk_len=256)
+    need_lb = L.ssm_scan_fwd_workspace_bytes(ctypes.byref(d_lb))
+    need_2p = L.ssm_scan_fwd_workspace_bytes(ctypes.byref(d_2p))
+    nch = 4096 // 256
+    assert need_lb >= 2 * nch * 64 * 16 * 4 + nch * 64 * 4 + nch * (64 // 8) * 4 + 16
+    assert need_lb > need_2p > 0
+    assert fwd(L, d_lb) == 4                                      # workspace required
+    assert fwd(L, d_lb, ws=FAKE, wsb=need_lb - 1) == 4
+    status = L.ssm_scan_fwd_lookback_status
+    assert status(ctypes.byref(d_lb), None, 0, None) == 4
+    assert status(ctypes.byref(d_lb), ctypes.c_void_p(FAKE), 2 * nch * 64 * 16 * 4, None) == 4
+    assert status(ctypes.byref(d_lb), ctypes.c_void_p(FAKE + 8), need_lb, None) == 3
+    # nothing waits in the one-pass schedule, or without the flag: no workspace needed
+    assert status(ctypes.byref(desc(B=1, T=4096, D=64, chunk_len=-1, flags=4)), None, 0, None) == 0
+    assert status(ctypes.byref(d_2p), None, 0, None) == 0
+    assert status(ctypes.byref(desc(flags=16)), None, 0, None) == 1
+    # the one-pass schedule ignores the flag
+    assert L.ssm_scan_fwd_workspace_bytes(ctypes.byref(desc(T=4096, chunk_len=-1, flags=4))) == 0
 
 
 def test_too_many_chunks_is_unsupported(L):

@@ -63,6 +63,7 @@ def draw_case(seed):
     if case["io"] == "bf16" and case["D"] % 8 and r.integers(0, 2):
         case["D"] += 8 - case["D"] % 8           # both aligned and unaligned rows for bf16
     case["chunk_kd"] = r.choice([None, 1, 2])    # channels per lane of the chunked forward
+    case["lookback"] = bool(r.integers(0, 2))    # chunked forward in one launch with look-back
     return case
 
 
@@ -81,7 +82,10 @@ def test_random_case(seed):
     chunk_len = cs["chunk_len"] if cs["fwd"] == "chunked" else (-1 if layout else 0)
     with forced(SSM_SCAN_FORCE_FWD_LAYOUT=layout, SSM_SCAN_FORCE_CHUNK_KD=cs["chunk_kd"]):
         y, hT, ck = ssm.ssm_scan_fwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], ckpt_interval=K,
-                                     chunk_len=chunk_len, D_skip=Ds, delta_softplus=cs["softplus"])
+                                     chunk_len=chunk_len, D_skip=Ds, delta_softplus=cs["softplus"],
+                                     lookback=cs["lookback"])
+        if cs["lookback"]:
+            ssm.lookback_status()
     with forced(SSM_SCAN_FORCE_BWD_KD=cs["kd"], SSM_SCAN_FORCE_BWD_TPAR=cs["tpar"]):
         g = ssm.ssm_scan_bwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], None if cs["rebuild"] else ck,
                              t["dy"], t.get("ghT"), ckpt_interval=K, D_skip=Ds, delta_softplus=cs["softplus"],
