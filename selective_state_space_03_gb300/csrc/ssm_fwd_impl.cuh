@@ -1,4 +1,5 @@
-// Forward scan kernels: one pass over T, and the two passes of the chunked scan.
+// Forward scan kernels: one pass over T, the two passes of the chunked scan, and
+// the chunked scan in one launch with decoupled look-back (fwd_lookback_kernel).
 //
 // Recurrence (page "pssa_kernels.py", module docstring and `scan_reference`):
 //   h_t = exp(delta_t A) h_{t-1} + delta_t b_t x_t,   y_t = <h_t, c_t>.
@@ -20,15 +21,16 @@
 //    are the same for every channel, so each b/c value a lane reads from
 //    shared memory feeds KD channels: broadcast shared loads deliver only 4
 //    bytes per wavefront, which would cap the kernel at 16*KD elements per
-//    clock per SM. KD = 2, G = 2 is used when there are enough (b, d) chains;
-//    KD = 1, G = 4 otherwise. State pairs use packed FP32x2 multiply/FMA.
+//    clock per SM. Layouts (G, KD): (2, 2) when there are enough (b, d) chains,
+//    then (4, 2), then (4, 1) as chains get fewer; the chunk passes use (4, 2)
+//    or (4, 1). State pairs use packed FP32x2 multiply/FMA.
 //  - x, delta, b, c tiles of TT steps are double-buffered in shared memory with
 //    16-byte cp.async, zero-filled past the end (delta = 0 gives decay 1 and no
 //    input, so padded steps leave the state unchanged). bf16 b and c are
 //    widened to float32 once per tile.
 //  - The readout <h_t, c_t> is finished across the G lanes of a channel: with
-//    KD > 1 by a reduce-scatter over the lane's channels, with KD = 1 by a
-//    reduce-scatter over G steps. y goes to a shared-memory tile and leaves in
+//    G = 2 by one exchange that splits the lane pair's channels, with G = 4 by
+//    a reduce-scatter over 4 steps (and the lane's KD channels). y goes to a shared-memory tile and leaves in
 //    16-byte stores once per tile; checkpoints are written at tile starts when
 //    every checkpoint step is one; staging offsets are per-lane constants, so a
 //    full tile costs a few instructions per 16-byte chunk.
