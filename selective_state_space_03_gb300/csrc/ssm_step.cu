@@ -8,9 +8,11 @@
 // It is ssm_scan_fwd with T = 1 and hT written over h0.
 //
 // The step moves 128 bytes of state per chain in and out and does 16 exp per
-// chain, so it is bound by HBM (or by launch latency for small B*D). Layout: 4
-// lanes per chain, 4 states per lane in one 16-byte load and store, the readout
-// finished with two shuffles; 32 chains per 128-thread CTA. Steps are launched
+// chain, so it is bound by HBM (or by launch latency for small B*D). Layout: 2
+// lanes per chain, 8 states per lane in two 16-byte loads and stores, the
+// readout finished with one shuffle; 64 chains per 128-thread CTA (with 4 lanes
+// per chain workload 5's 81920 chains took 2560 CTAs, 1.05 waves at 16 per SM;
+// with 2, 1280 CTAs fit in one). Steps are launched
 // with programmatic stream serialization: a step's loads of its own inputs
 // overlap the end of the previous step, and only the state load waits for it.
 #include "ssm_common.cuh"
@@ -32,43 +34,60 @@ struct StepLaunch {
     bool softplus;       // delta holds raw values
 };
 
+// 8 consecutive I/O values as float32 (16-byte aligned)
+template <typename TIO>
+__device__ __forceinline__ void load8(const TIO* p, float (&v)[8]) {
+    if constexpr (std::is_same<TIO, float>::value) {
+        const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    } else {
+        const uint4 q = *reinterpret_cast<const uint4*>(p);
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            v[2 * i] = __uint_as_float(w[i] << 16);
+            v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    }
+}
+
 template <typename TIO>
 __global__ void __launch_bounds__(128) step_kernel(const StepLaunch p) {
     const int64_t gid = int64_t(blockIdx.x) * 128 + threadIdx.x;
-    const int64_t chain = gid >> 2;
-    const int sg = int(gid & 3), s0 = sg * 4;
-    const bool valid = chain < p.B * p.D;       // whole 4-lane groups are valid or not
+    const int64_t chain = gid >> 1;
+    const int sg = int(gid & 1), s0 = sg * 8;
+    const bool valid = chain < p.B * p.D;       // whole lane pairs are valid or not
     // Consecutive steps on a stream are launched as programmatic dependents: let the next
     // step's CTAs start now; they run up to their wait below while this grid finishes.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     float acc = 0.f;
-    float4 hv = make_float4(0.f, 0.f, 0.f, 0.f);
-    float dl = 0.f, dx = 0.f, bv[4] = {0.f, 0.f, 0.f, 0.f}, cv[4] = {0.f, 0.f, 0.f, 0.f};
-    float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    float hv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float dl = 0.f, dx = 0.f, bv[8], cv[8], av[8];
     if (valid) {      // this step's inputs, which no earlier step writes
         const int64_t bb = chain / p.D, d = chain - bb * p.D;
         dl = to_f32(static_cast<const TIO*>(p.delta)[chain]);
         if (p.softplus) dl = softplus_f32(dl);
         dx = dl * to_f32(static_cast<const TIO*>(p.x)[chain]);
-        load_vals<TIO, 4>(static_cast<const TIO*>(p.b) + bb * kDS + s0, bv);
-        load_vals<TIO, 4>(static_cast<const TIO*>(p.c) + bb * kDS + s0, cv);
-        a4 = *reinterpret_cast<const float4*>(p.A + d * kDS + s0);
+        load8<TIO>(static_cast<const TIO*>(p.b) + bb * kDS + s0, bv);
+        load8<TIO>(static_cast<const TIO*>(p.c) + bb * kDS + s0, cv);
+        load8<float>(p.A + d * kDS + s0, av);
     }
     // the state (and y) belong to the previous step: wait until the grid before this one has
     // completed and its writes are visible (returns at once without such a grid)
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (valid) {
-        hv = *reinterpret_cast<const float4*>(p.h + chain * kDS + s0);
-        hv.x = fmaf(ex2(dl * (a4.x * kLog2e)), hv.x, dx * bv[0]);
-        hv.y = fmaf(ex2(dl * (a4.y * kLog2e)), hv.y, dx * bv[1]);
-        hv.z = fmaf(ex2(dl * (a4.z * kLog2e)), hv.z, dx * bv[2]);
-        hv.w = fmaf(ex2(dl * (a4.w * kLog2e)), hv.w, dx * bv[3]);
-        acc = fmaf(hv.x, cv[0], fmaf(hv.y, cv[1], fmaf(hv.z, cv[2], hv.w * cv[3])));
+        load8<float>(p.h + chain * kDS + s0, hv);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            hv[i] = fmaf(ex2(dl * (av[i] * kLog2e)), hv[i], dx * bv[i]);
+            acc = fmaf(hv[i], cv[i], acc);
+        }
     }
     acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
     if (!valid) return;
-    *reinterpret_cast<float4*>(p.h + chain * kDS + s0) = hv;
+    float4* hd = reinterpret_cast<float4*>(p.h + chain * kDS + s0);
+    hd[0] = make_float4(hv[0], hv[1], hv[2], hv[3]);
+    hd[1] = make_float4(hv[4], hv[5], hv[6], hv[7]);
     if (sg == 0) static_cast<TIO*>(p.y)[chain] = from_f32<TIO>(acc);
 }
 
@@ -92,7 +111,7 @@ extern "C" ssm_status ssm_scan_step(const ssm_scan_desc* desc, const void* x, co
     const void* ptrs[] = {x, delta, A, b, c, h, y};
     for (const void* q : ptrs)
         if (!aligned16(q)) return SSM_ERR_MISALIGNED;
-    const int64_t threads = d.B * d.D * 4;
+    const int64_t threads = d.B * d.D * 2;
     const int64_t blocks = (threads + 127) / 128;
     if (blocks > int64_t(0x7fffffff)) return SSM_ERR_UNSUPPORTED;
     StepLaunch L{x, delta, A, b, c, h, y, d.B, d.D, (d.flags & SSM_SCAN_DELTA_SOFTPLUS) != 0};
