@@ -90,6 +90,8 @@ def test_invalid_descriptors(L):
     assert fwd(L, d) == 1
     assert fwd(L, desc(DS=8)) == 2
     assert fwd(L, desc(DS=32)) == 2
+    assert fwd(L, desc(D=(1 << 27) + 1)) == 2        # past the kernels' 32-bit in-tile offsets
+    assert fwd(L, desc(B=65536)) == 1
     assert bwd(L, desc(DS=8)) == 2
 
 
