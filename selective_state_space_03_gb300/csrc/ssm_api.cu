@@ -129,9 +129,9 @@ cudaError_t run_fwd(const ssm_scan_desc& d, FwdLaunch L, int mode, cudaStream_t 
     return d.io == SSM_IO_BF16 ? launch_fwd_bf16(L, mode, st) : launch_fwd_f32(L, mode, st);
 }
 
-// Backward layout: 2 channels per lane (64 per CTA, 2 CTAs per SM) when that
-// still gives at least two full waves of CTAs; otherwise 1 (32 per CTA, 4 per
-// SM), which keeps more SMs busy on shapes with few (b, d) chains.
+// Backward layout: 2 channels per lane (64 per CTA, 3 CTAs per SM) when that gives
+// at least 4 CTAs per SM; otherwise 1 (32 per CTA, 4 per SM with bf16 I/O), which
+// keeps more SMs busy on shapes with few (b, d) chains.
 int bwd_channels_per_lane(const ssm_scan_desc& d) {
     int kd = d.B * cdiv(d.D, 64) >= int64_t(device_sm_count()) * 4 ? 2 : 1;
     // testing aid: force the layout (1 or 2)

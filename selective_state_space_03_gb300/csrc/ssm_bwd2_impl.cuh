@@ -23,10 +23,10 @@
 // per row, one channel per column; the last sub-chunk of a chunk, which may be
 // short, keeps its start state in registers). The round trip stays in L2. The
 // level-3 window (h_t of both channels, 16 steps, 128 columns) is in tensor
-// memory and b_t comes from shared memory, so shared memory per CTA is ~35 KB
-// and three CTAs (12 warps) are resident per SM, each thread with up to 168
-// registers. As in `bwd_kernel`, the per-state arithmetic is packed f32x2 on
-// pairs of neighbouring states.
+// memory and b_t comes from shared memory, so shared memory per CTA is 41 KB
+// (48 KB with float32 I/O) and three CTAs (12 warps) are resident per SM, each
+// thread with up to 168 registers. As in `bwd_kernel`, the per-state arithmetic
+// is packed f32x2 on pairs of neighbouring states.
 #pragma once
 
 #include "ssm_bwd_impl.cuh"
