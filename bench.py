@@ -157,6 +157,26 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- CPU oracle timing
 
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    import platform
+    import subprocess
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.machine()
+
+
 def oracle_sample(w, budget_s=12.0, seed=0, max_batches=16):
     """Time the float64 oracle (forward with checkpoints + backward) on the first
     B' batches of workload w (all channels), B' grown until one run takes about
@@ -431,7 +451,8 @@ def run_ours(args, rank, world, local_rank):
     }
     if not args.no_cpu:
         v, cores, sample = oracle_sample(w)
-        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
+                                "cpu": cpu_model()}
     print(json.dumps(line), flush=True)
 
 
@@ -625,7 +646,7 @@ def run_reference(args, rank, world):
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded Philox normals, gen.make_inputs)",
             "config": workload_config(w, world),
             "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": f"B={B1} T={w.T} D={w.D} DS={w.DS} per step (fwd+bwd)"},
+                             "sample": f"B={B1} T={w.T} D={w.D} DS={w.DS} per step (fwd+bwd)", "cpu": cpu_model()},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
