@@ -671,6 +671,15 @@ def run_profile_case(args):
 
     t = {k: to_dev(inp.get(k)) for k in ("x", "delta", "A", "b", "c", "h0", "dy")}
     K = w.ckpt_interval
+    if args.decode:
+        # decode steps at the workload's width: the inputs of step 0, the state carried in place
+        h = torch.zeros((w.B, w.D, w.DS), dtype=torch.float32, device=dev)
+        xs, ds, bs, cs = (t[k][:, 0].contiguous() for k in ("x", "delta", "b", "c"))
+        for _ in range(4):
+            ssm.ssm_scan_step(xs, ds, t["A"], bs, cs, h)
+        torch.cuda.synchronize()
+        print("ok")
+        return
     for _ in range(2):
         _, _, ck = ssm.ssm_scan_fwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], ckpt_interval=K)
         if w.bwd:
@@ -694,6 +703,7 @@ def main():
     ap.add_argument("--workload", type=int, default=0, help="with --profile: workload 1-5 instead of 5")
     ap.add_argument("--B", type=int, default=0, help="with --profile: batch size instead of 16")
     ap.add_argument("--T", type=int, default=0, help="with --profile: sequence length instead of 2048")
+    ap.add_argument("--decode", action="store_true", help="with --profile: 4 decode steps instead of fwd+bwd")
     args = ap.parse_args()
     if args.profile:
         run_profile_case(args)
