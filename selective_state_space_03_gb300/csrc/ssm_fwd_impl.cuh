@@ -386,19 +386,37 @@ __global__ void __launch_bounds__(32, FwdCfg<TIO, G, KD>::MINB) fwd_kernel(const
     bool valid[KD];
     float2 A2[KD][KP], h[KD][KP];
     fwd_lane_setup<TIO, G, KD>(p, b, d0, MODE != kPass1, valid, A2, h);
-    if (MODE == kPass2) {
-        // start state of this chunk: fold the carries of the chunks before it
+    if constexpr (MODE == kPass2) {
+        // start state of this chunk: fold the carries of the chunks before it, in order; the
+        // loads of NB chunks are issued together (one round trip to L2 per NB chunks)
+        static_assert(KP == 2, "the chunk passes use 4 lanes per chain (4 states per lane)");
+        constexpr int NB = 4;
+        for (int64_t j0 = 0; j0 < chunk; j0 += NB) {
+            float sd[NB][KD];
+            float4 Sv[NB][KD];
 #pragma unroll
-        for (int k = 0; k < KD; ++k) {
-            if (!valid[k]) continue;
-            for (int64_t j = 0; j < chunk; ++j) {
-                const int64_t row = (b * nprev + j) * D + d0 + c0 + k;
-                const float sd = p.ws_Sd[row];
-                const float* S = p.ws_S + row * kDS + s0;
+            for (int u = 0; u < NB; ++u)
 #pragma unroll
-                for (int q = 0; q < KP; ++q) {
-                    const float2 P = make_float2(ex2(A2[k][q].x * sd), ex2(A2[k][q].y * sd));
-                    h[k][q] = __ffma2_rn(P, h[k][q], make_float2(S[2 * q], S[2 * q + 1]));
+                for (int k = 0; k < KD; ++k) {
+                    sd[u][k] = 0.f;
+                    Sv[u][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (j0 + u < chunk && valid[k]) {
+                        const int64_t row = (b * nprev + j0 + u) * D + d0 + c0 + k;
+                        sd[u][k] = p.ws_Sd[row];
+                        Sv[u][k] = *reinterpret_cast<const float4*>(p.ws_S + row * kDS + s0);
+                    }
+                }
+#pragma unroll
+            for (int u = 0; u < NB; ++u) {
+                if (j0 + u >= chunk) break;
+#pragma unroll
+                for (int k = 0; k < KD; ++k) {
+                    const float2 S2[2] = {make_float2(Sv[u][k].x, Sv[u][k].y), make_float2(Sv[u][k].z, Sv[u][k].w)};
+#pragma unroll
+                    for (int q = 0; q < KP; ++q) {
+                        const float2 P = make_float2(ex2(A2[k][q].x * sd[u][k]), ex2(A2[k][q].y * sd[u][k]));
+                        h[k][q] = __ffma2_rn(P, h[k][q], S2[q]);
+                    }
                 }
             }
         }

@@ -106,25 +106,24 @@ cudaError_t launch_bwd_carry_bf16(const BwdLaunch& L, cudaStream_t stream);
 int device_sm_count();
 
 // Schedule of the chunked forward (both passes use 4 lanes per chain; kd channels per lane).
-// Chosen by the library (chunk_len == 0): two channels per lane with chunks for about 21
-// resident pass-2 warps per SM when those chunks are at least 192 steps long, else one
-// channel per lane with chunks for about 14 (measured on the 2048-chain workloads: 4096
-// steps ran 9 % faster in 22 chunks at two channels than in 8 at one; 1024 steps ran 6 %
-// slower in 16 at two than in 8 at one). Given chunk length: two channels per lane when
-// that still leaves at least 8 pass-2 warps per SM.
+// Two channels per lane whenever that leaves at least 4 pass-2 warps per SM, else one.
+// Chosen by the library (chunk_len == 0): with two channels, chunks for about 21 resident
+// pass-2 warps per SM but at least 128 steps; with one, chunks for about 14 warps per SM, at
+// least 64 steps. Measured on the 2048-chain workloads (after the carry fold's loads were
+// batched): 4096 steps in 22 chunks at two channels 72.3 us, 8 at one 76.4 us (earlier
+// rule); 1024 steps in 8 chunks at two channels 29.4 us, at one 32.4 us.
 struct ChunkSchedule {
     int64_t Lc;
     int kd;
 };
 inline ChunkSchedule chunk_schedule(int64_t T, int64_t chains, int64_t chunk_len, int64_t sms) {
     auto round32 = [](int64_t v) { return (v + 31) / 32 * 32; };
-    if (chunk_len > 0) {
-        const int64_t nch = (T + chunk_len - 1) / chunk_len;
-        return {chunk_len, chains * nch >= 128 * sms ? 2 : 1};
-    }
+    auto kd_for = [&](int64_t Lc) { return chains * ((T + Lc - 1) / Lc) >= 64 * sms ? 2 : 1; };
+    if (chunk_len > 0) return {chunk_len, kd_for(chunk_len)};
     const int64_t n2 = sms * 336 / chains > 2 ? sms * 336 / chains : 2;
-    const int64_t L2 = round32((T + n2 - 1) / n2);
-    if (L2 >= 192) return {L2, 2};
+    int64_t L2 = round32((T + n2 - 1) / n2);
+    if (L2 < 128) L2 = 128;
+    if (kd_for(L2) == 2) return {L2, 2};
     const int64_t n1 = sms * 448 / (chains * 4) > 2 ? sms * 448 / (chains * 4) : 2;
     const int64_t L1 = round32((T + n1 - 1) / n1);
     return {L1 < 64 ? 64 : L1, 1};
