@@ -120,7 +120,8 @@ size_t ssm_scan_ckpt_bytes(const ssm_scan_desc* desc);
 
 /* Bytes of device scratch memory ssm_scan_fwd needs for this desc (0 when the
  * schedule needs none). The workspace holds the chunked scan's per-chunk
- * decay sums and partial states. */
+ * decay sums and partial states; with SSM_SCAN_LOOKBACK, every chunk's map,
+ * end state and publication flag. */
 size_t ssm_scan_fwd_workspace_bytes(const ssm_scan_desc* desc);
 
 /* Bytes of device scratch memory ssm_scan_bwd needs for this desc when it is
