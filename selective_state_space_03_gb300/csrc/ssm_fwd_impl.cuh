@@ -703,7 +703,8 @@ cudaError_t launch_fwd_fuse(const FwdLaunch& L, int mode, cudaStream_t stream) {
 
 template <typename TIO>
 cudaError_t launch_fwd_io(const FwdLaunch& L, int mode, cudaStream_t stream) {
-    const bool fuse = L.softplus || (L.Dskip != nullptr && (mode == kSingle || mode == kPass2));
+    // the skip is applied where y is read out: the one-pass scan, pass 2, the look-back scan
+    const bool fuse = L.softplus || (L.Dskip != nullptr && (mode == kSingle || mode == kPass2 || mode == kLookback));
     return fuse ? launch_fwd_fuse<TIO, true>(L, mode, stream) : launch_fwd_fuse<TIO, false>(L, mode, stream);
 }
 

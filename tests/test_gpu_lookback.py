@@ -96,9 +96,10 @@ def test_lookback_unaligned_channels(io):
 
 
 @pytest.mark.parametrize("io", ["f32", "bf16"])
-def test_lookback_fused_softplus_and_skip(io):
+@pytest.mark.parametrize("softplus,skip", [(True, True), (False, True), (True, False)])
+def test_lookback_fused_softplus_and_skip(io, softplus, skip):
     lookback_case(gen.workload(2, B=2, T=230, D=40, io=io, h0_std=0.1), K=50, chunk_len=50, chunk_kd=2,
-                  softplus=True, skip=True)
+                  softplus=softplus, skip=skip)
 
 
 def test_lookback_automatic_schedule_matches_two_launches():

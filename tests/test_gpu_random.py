@@ -67,7 +67,7 @@ def draw_case(seed):
     return case
 
 
-@pytest.mark.parametrize("seed", range(64))
+@pytest.mark.parametrize("seed", range(160))
 def test_random_case(seed):
     import torch
     import selective_state_space_03_gb300 as ssm
