@@ -252,7 +252,10 @@ ssm_status ssm_scan_fwd_noalloc(const ssm_scan_desc* desc,
  *   b, c          (B, DS)     io dtype
  *   A             (D, DS)     float32
  *   h             (B, D, DS)  float32, read and overwritten (not NULL)
- * No workspace; B == 0 or D == 0 launches nothing. Errors as ssm_scan_fwd.
+ * No workspace; B == 0 or D == 0 launches nothing. Errors as ssm_scan_fwd,
+ * except that x, delta and y need only be aligned to their element size (A,
+ * b, c and h: 16 bytes), so one step's rows of (B, T, D) tensors can be passed
+ * as they are.
  * Steps are launched as programmatic dependents of the preceding kernel on the
  * stream: after an earlier ssm_scan_step, a step may already read its own x,
  * delta, A, b and c while that step finishes (it waits for it before reading h),

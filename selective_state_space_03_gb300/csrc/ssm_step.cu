@@ -108,9 +108,15 @@ extern "C" ssm_status ssm_scan_step(const ssm_scan_desc* desc, const void* x, co
     if (d.DS != kDS || d.D > kMaxD) return SSM_ERR_UNSUPPORTED;
     if (d.B == 0 || d.D == 0) return SSM_OK;
     if (!x || !delta || !A || !b || !c || !h || !y) return SSM_ERR_INVALID_ARG;
-    const void* ptrs[] = {x, delta, A, b, c, h, y};
-    for (const void* q : ptrs)
+    // A, b, c and h are read with 16-byte loads; x, delta and y one element per chain, so a
+    // row of a (B, T, D) tensor (x[:, t] with B = 1) can be passed as it is
+    const void* vec_ptrs[] = {A, b, c, h};
+    for (const void* q : vec_ptrs)
         if (!aligned16(q)) return SSM_ERR_MISALIGNED;
+    const uintptr_t esz = d.io == SSM_IO_BF16 ? 2 : 4;
+    const void* elem_ptrs[] = {x, delta, y};
+    for (const void* q : elem_ptrs)
+        if (reinterpret_cast<uintptr_t>(q) % esz != 0) return SSM_ERR_MISALIGNED;
     const int64_t threads = d.B * d.D * 2;
     const int64_t blocks = (threads + 127) / 128;
     if (blocks > int64_t(0x7fffffff)) return SSM_ERR_UNSUPPORTED;

@@ -146,6 +146,8 @@ def test_step_argument_checks(L):
     assert step(L, desc(T=1), x=None) == 1
     assert step(L, desc(T=1), h=FAKE + 4) == 3
     assert step(L, desc(T=1), y=FAKE + 2) == 3
+    assert step(L, desc(T=1, io=1), x=FAKE + 1) == 3     # bf16 x, y: 2-byte alignment
+    assert step(L, desc(T=1), c=FAKE + 8) == 3           # b, c, A, h: 16-byte loads
     assert step(L, desc(T=1, B=0)) == 0                  # nothing to do, nothing launched
     assert step(L, desc(T=1, D=0)) == 0
 

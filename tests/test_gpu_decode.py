@@ -62,6 +62,26 @@ def test_steps_in_place_follow_the_scan(io):
     assert_close(to_host(h), ref["hT"], io, "fwd", "hT")
 
 
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_steps_on_row_views(io):
+    # with B = 1, x[:, k] is a view into the (1, T, D) tensor whose address is only element
+    # aligned for odd D: the step takes such rows as they are
+    import torch
+    w = gen.workload(2, B=1, T=9, D=37, io=io, h0_std=0.1)
+    inp = gen.make_inputs(w, seed=7)
+    t = dev_inputs(inp)
+    h = t["h0"].clone()
+    ys = []
+    for k in range(w.T):
+        xk, dk = t["x"][:, k], t["delta"][:, k]
+        assert xk.is_contiguous()
+        ys.append(ssm().ssm_scan_step(xk, dk, t["A"], t["b"][:, k].contiguous(), t["c"][:, k].contiguous(), h))
+    torch.cuda.synchronize()
+    ref = oracle.fwd(inp["x"], inp["delta"], inp["A"], inp["b"], inp["c"], inp["h0"])
+    assert_close(np.stack([to_host(v) for v in ys], axis=1), ref["y"], io, "fwd", "y")
+    assert_close(to_host(h), ref["hT"], io, "fwd", "hT")
+
+
 def test_step_writes_only_its_outputs():
     import torch
     B, D = 3, 40
