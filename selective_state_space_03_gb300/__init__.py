@@ -309,10 +309,12 @@ def ssm_scan_step(x, delta, A, b, c, h, *, y=None, delta_softplus=False, stream=
     return y
 
 
-def selective_scan(x, delta, A, b, c, h0=None, ckpt_interval=256):
-    """Differentiable scan: returns (y, hT). Gradients flow to x, delta, A, b, c and h0;
-    hT is differentiated too (its gradient enters the backward as ghT)."""
-    return _ScanFn.apply(x, delta, A, b, c, h0, ckpt_interval)
+def selective_scan(x, delta, A, b, c, h0=None, ckpt_interval=256, D_skip=None, delta_softplus=False):
+    """Differentiable scan: returns (y, hT). Gradients flow to x, delta, A, b, c, h0 and
+    D_skip; hT is differentiated too (its gradient enters the backward as ghT).
+    delta_softplus=True scans with softplus(delta) (delta given raw, its gradient w.r.t. the
+    raw values); D_skip (D,) float32 adds D_skip * x to y."""
+    return _ScanFn.apply(x, delta, A, b, c, h0, D_skip, ckpt_interval, bool(delta_softplus))
 
 
 def _make_autograd():
@@ -320,21 +322,25 @@ def _make_autograd():
 
     class ScanFn(torch.autograd.Function):
         @staticmethod
-        def forward(ctx, x, delta, A, b, c, h0, K):
-            y, hT, ckpt = ssm_scan_fwd(x, delta, A, b, c, h0, ckpt_interval=K)
-            ctx.save_for_backward(x, delta, A, b, c, h0, ckpt)
+        def forward(ctx, x, delta, A, b, c, h0, D_skip, K, softplus):
+            y, hT, ckpt = ssm_scan_fwd(x, delta, A, b, c, h0, ckpt_interval=K, D_skip=D_skip,
+                                       delta_softplus=softplus)
+            ctx.save_for_backward(x, delta, A, b, c, h0, D_skip, ckpt)
             ctx.K = K
+            ctx.softplus = softplus
             ctx.has_h0 = h0 is not None
             return y, hT
 
         @staticmethod
         def backward(ctx, dy, dhT):
-            x, delta, A, b, c, h0, ckpt = ctx.saved_tensors
+            x, delta, A, b, c, h0, D_skip, ckpt = ctx.saved_tensors
             dy = torch.zeros_like(x) if dy is None else dy.to(x.dtype).contiguous()
             ghT = None if dhT is None else dhT.float().contiguous()
-            g = ssm_scan_bwd(x, delta, A, b, c, h0, ckpt, dy, ghT, ckpt_interval=ctx.K)
+            g = ssm_scan_bwd(x, delta, A, b, c, h0, ckpt, dy, ghT, ckpt_interval=ctx.K, D_skip=D_skip,
+                             delta_softplus=ctx.softplus)
             return (g["gx"].to(x.dtype), g["gdelta"].to(delta.dtype), g["gA"], g["gb"].to(b.dtype),
-                    g["gc"].to(c.dtype), g["gh0"] if ctx.has_h0 else None, None)
+                    g["gc"].to(c.dtype), g["gh0"] if ctx.has_h0 else None,
+                    g["gD_skip"] if D_skip is not None else None, None, None)
 
     return ScanFn
 

@@ -148,6 +148,28 @@ def test_decode_step_with_softplus(io):
     assert_close(to_host(h), ref["hT"], io, "fwd", "hT")
 
 
+@pytest.mark.parametrize("softplus,skip", [(True, True), (False, True), (True, False)])
+def test_fused_autograd_wrapper(softplus, skip):
+    """selective_scan with the fused options: torch autograd reaches every input's gradient,
+    D_skip's included, through the fused kernels."""
+    import torch
+    w = gen.workload(2, B=2, T=90, D=24, h0_std=0.1)
+    inp = gen.make_inputs(w, with_grad_inputs=True, with_ghT=True, raw_delta=softplus, with_skip=skip)
+    t = dev_inputs(inp)
+    names = ("x", "delta", "A", "b", "c", "h0")
+    leaves = {k: t[k].clone().requires_grad_(True) for k in names}
+    Ds = to_dev(inp["D_skip"]).requires_grad_(True) if skip else None
+    y, hT = ssm().selective_scan(*(leaves[k] for k in names), ckpt_interval=16, D_skip=Ds,
+                                 delta_softplus=softplus)
+    ((y * t["dy"]).sum() + (hT * t["ghT"]).sum()).backward()
+    gref = oracle.bwd_fused(inp["x"], inp["delta"], inp["A"], inp["b"], inp["c"], inp["h0"], inp["dy"],
+                            inp["ghT"], inp.get("D_skip"), delta_softplus=softplus)
+    for k, gk in zip(names, GRADS):
+        assert_close(to_host(leaves[k].grad), gref[gk], "f32", "grad", gk)
+    if skip:
+        assert_close(to_host(Ds.grad), gref["gD_skip"], "f32", "grad", "gD_skip")
+
+
 def test_fused_and_deterministic_workload5_full_size_sampled():
     """Workload 5 at full size with softplus on delta, the skip and fixed-order sums:
     sampled chains against the oracle, gD_skip and gA on sampled channels over all
