@@ -38,8 +38,10 @@
  * Errors: every argument is checked on the host before anything is enqueued;
  * a failing check returns a status and enqueues nothing. Not checked (the
  * caller's preconditions): A < 0, delta > 0, finite inputs, buffer sizes, and
- * that buffers do not overlap. Numbers outside these preconditions give
- * unspecified (but memory-safe) results.
+ * that buffers do not overlap. Values outside the numeric preconditions give
+ * unspecified but memory-safe results; buffers that are too small or overlap
+ * are undefined behaviour (the backward, for one, uses its gx output as
+ * scratch space before it writes the gradient there).
  *
  * Supported: DS == 16; B, T, D >= 0; B <= 65535; D <= 2^27; at most 65535
  * chunks of a chunked forward, ceil(T / chunk_len) (SSM_ERR_UNSUPPORTED beyond). T == 0 or B == 0 or D == 0
