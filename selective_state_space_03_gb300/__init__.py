@@ -113,10 +113,18 @@ def _check(t, shape, dtype, name, device):
                          f"got {t.dtype} {tuple(t.shape)} on {t.device} (contiguous={t.is_contiguous()})")
 
 
-def _stream(stream):
+def _stream(stream, device):
     torch = _torch()
-    s = torch.cuda.current_stream() if stream is None else stream
+    s = torch.cuda.current_stream(device) if stream is None else stream
     return ctypes.c_void_p(s.cuda_stream)
+
+
+def _call(device, fn, *args):
+    """Call into the library with the tensors' device current (the C ABI works on the
+    current CUDA device)."""
+    torch = _torch()
+    with torch.cuda.device(device):
+        return fn(*args)
 
 
 def _workspace(nbytes, device):
@@ -164,18 +172,18 @@ def ssm_scan_fwd(x, delta, A, b, c, h0=None, *, ckpt_interval=0, chunk_len=0, y=
         ckpt = torch.empty((nslots, B, D, DS), dtype=torch.float32, device=dev)
     _check(y, (B, T, D), x.dtype, "y", dev)
     _check(hT, (B, D, DS), torch.float32, "hT", dev)
-    need = L.ssm_scan_fwd_workspace_bytes(ctypes.byref(desc))
+    need = _call(dev, L.ssm_scan_fwd_workspace_bytes, ctypes.byref(desc))
     if workspace is None:
         workspace, wsb = _workspace(need, dev)
     else:
         wsb = workspace.numel() * workspace.element_size()
     if D_skip is None:
-        st = L.ssm_scan_fwd(ctypes.byref(desc), _ptr(x), _ptr(delta), _ptr(A), _ptr(b), _ptr(c), _ptr(h0),
-                            _ptr(y), _ptr(hT), _ptr(ckpt), _ptr(workspace), wsb, _stream(stream))
+        st = _call(dev, L.ssm_scan_fwd, ctypes.byref(desc), _ptr(x), _ptr(delta), _ptr(A), _ptr(b), _ptr(c), _ptr(h0),
+                            _ptr(y), _ptr(hT), _ptr(ckpt), _ptr(workspace), wsb, _stream(stream, dev))
     else:
-        st = L.ssm_scan_fwd_fused(ctypes.byref(desc), _ptr(x), _ptr(delta), _ptr(A), _ptr(b), _ptr(c),
+        st = _call(dev, L.ssm_scan_fwd_fused, ctypes.byref(desc), _ptr(x), _ptr(delta), _ptr(A), _ptr(b), _ptr(c),
                                   _ptr(D_skip), _ptr(h0), _ptr(y), _ptr(hT), _ptr(ckpt), _ptr(workspace), wsb,
-                                  _stream(stream))
+                                  _stream(stream, dev))
     if st != 0:
         raise SSMError(st, "ssm_scan_fwd")
     if lookback:
@@ -192,7 +200,7 @@ def lookback_status(device=None):
     if dev not in _last_lookback:
         return None
     desc, ws, wsb, stream = _last_lookback[dev]
-    st = lib().ssm_scan_fwd_lookback_status(ctypes.byref(desc), _ptr(ws), wsb, _stream(stream))
+    st = _call(dev, lib().ssm_scan_fwd_lookback_status, ctypes.byref(desc), _ptr(ws), wsb, _stream(stream, dev))
     if st != 0:
         raise SSMError(st, "ssm_scan_fwd_lookback_status")
     return None
@@ -232,21 +240,22 @@ def ssm_scan_bwd(x, delta, A, b, c, h0, ckpt, dy, ghT=None, *, ckpt_interval=0, 
     # when they are further apart than the backward reads directly
     rebuild = ckpt is None or not (0 < ckpt_interval <= MAX_BWD_CKPT_INTERVAL)
     # (with checkpoints, the workspace holds the chunk-parallel carries and deterministic partials)
-    need = (L.ssm_scan_bwd_workspace_bytes if rebuild else L.ssm_scan_bwd_ckpt_workspace_bytes)(ctypes.byref(desc))
+    need = _call(dev, L.ssm_scan_bwd_workspace_bytes if rebuild else L.ssm_scan_bwd_ckpt_workspace_bytes,
+                 ctypes.byref(desc))
     if workspace is None:
         workspace, wsb = _workspace(need, dev)
     else:
         wsb = workspace.numel() * workspace.element_size()
     if D_skip is None:
-        st = L.ssm_scan_bwd(ctypes.byref(desc), _ptr(x), _ptr(delta), _ptr(A), _ptr(b), _ptr(c), _ptr(h0),
+        st = _call(dev, L.ssm_scan_bwd, ctypes.byref(desc), _ptr(x), _ptr(delta), _ptr(A), _ptr(b), _ptr(c), _ptr(h0),
                             _ptr(ckpt), _ptr(dy), _ptr(ghT), _ptr(out["gx"]), _ptr(out["gdelta"]), _ptr(out["gA"]),
                             _ptr(out["gb"]), _ptr(out["gc"]), _ptr(out["gh0"]), _ptr(workspace), wsb,
-                            _stream(stream))
+                            _stream(stream, dev))
     else:
-        st = L.ssm_scan_bwd_fused(ctypes.byref(desc), _ptr(x), _ptr(delta), _ptr(A), _ptr(b), _ptr(c),
+        st = _call(dev, L.ssm_scan_bwd_fused, ctypes.byref(desc), _ptr(x), _ptr(delta), _ptr(A), _ptr(b), _ptr(c),
                                   _ptr(D_skip), _ptr(h0), _ptr(ckpt), _ptr(dy), _ptr(ghT), _ptr(out["gx"]),
                                   _ptr(out["gdelta"]), _ptr(out["gA"]), _ptr(out["gb"]), _ptr(out["gc"]),
-                                  _ptr(out["gh0"]), _ptr(out["gD_skip"]), _ptr(workspace), wsb, _stream(stream))
+                                  _ptr(out["gh0"]), _ptr(out["gD_skip"]), _ptr(workspace), wsb, _stream(stream, dev))
     if st != 0:
         raise SSMError(st, "ssm_scan_bwd")
     return out
@@ -277,8 +286,8 @@ def ssm_scan_fwd_noalloc(x, delta, A, b, c, h0=None, *, ckpt_interval=0, chunk_l
         hT = torch.empty((B, D, DS), dtype=torch.float32, device=dev)
     if ckpt is None and ckpt_interval > 0:
         ckpt = torch.empty((-(-T // ckpt_interval), B, D, DS), dtype=torch.float32, device=dev)
-    st = fn(ctypes.byref(desc), _ptr(x), _ptr(delta), _ptr(A), _ptr(b), _ptr(c), _ptr(h0), _ptr(y), _ptr(hT),
-            _ptr(ckpt), _stream(stream))
+    st = _call(dev, fn, ctypes.byref(desc), _ptr(x), _ptr(delta), _ptr(A), _ptr(b), _ptr(c), _ptr(h0), _ptr(y), _ptr(hT),
+            _ptr(ckpt), _stream(stream, dev))
     if st != 0:
         raise SSMError(st, "ssm_scan_fwd_noalloc")
     return y, hT, ckpt
@@ -303,7 +312,7 @@ def ssm_scan_step(x, delta, A, b, c, h, *, y=None, delta_softplus=False, stream=
     desc = make_desc(B, 1, D, DS, _io_of(x), 0, 0, SSM_SCAN_DELTA_SOFTPLUS if delta_softplus else 0)
     if y is None:
         y = torch.empty((B, D), dtype=x.dtype, device=dev)
-    st = fn(ctypes.byref(desc), _ptr(x), _ptr(delta), _ptr(A), _ptr(b), _ptr(c), _ptr(h), _ptr(y), _stream(stream))
+    st = _call(dev, fn, ctypes.byref(desc), _ptr(x), _ptr(delta), _ptr(A), _ptr(b), _ptr(c), _ptr(h), _ptr(y), _stream(stream, dev))
     if st != 0:
         raise SSMError(st, "ssm_scan_step")
     return y
