@@ -132,6 +132,25 @@ def test_lookback_timeout_is_reported_and_the_context_survives():
     torch.cuda.synchronize()
 
 
+def test_lookback_grid_beyond_resident_ctas():
+    # 256 chunks x 8 batches x 32 channel blocks = 65536 CTAs, far more than are resident at once:
+    # a CTA only waits for CTAs that took an earlier ticket, so the launch still moves
+    import torch
+    from gpu_util import sample_indices, sub_inputs
+    w = gen.workload(2, B=8, T=16384, D=512, h0_std=0.1)
+    inp = gen.make_inputs(w, with_grad_inputs=False)
+    t = dev_inputs(inp)
+    y, hT, _ = ssm().ssm_scan_fwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], chunk_len=64,
+                                  lookback=True)
+    ssm().lookback_status()
+    bsel, dsel = sample_indices(w.B, 3, 1), sample_indices(w.D, 6, 2)
+    sub = sub_inputs(inp, bsel, dsel)
+    ref = oracle.fwd(sub["x"], sub["delta"], sub["A"], sub["b"], sub["c"], sub["h0"])
+    bi, di = torch.as_tensor(bsel), torch.as_tensor(dsel)
+    assert_close(to_host(y[bi][:, :, di]), ref["y"], "f32", "fwd", "y")
+    assert_close(to_host(hT[bi][:, di]), ref["hT"], "f32", "fwd", "hT")
+
+
 def test_lookback_workload4_full_size_chained_sampled():
     import torch
     from gpu_util import sample_indices, sub_inputs
