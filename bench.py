@@ -423,7 +423,7 @@ def run_ours(args, rank, world, local_rank):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded Philox normals, gen.make_inputs)",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded Philox normals, gen.make_inputs)",
         "config": workload_config(w, world),
         "kernels": {"fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "bwd_deterministic_ms": bwd_det_ms,
                     "fused_softplus_skip_fwd_ms": fused_fwd_ms, "fused_softplus_skip_bwd_ms": fused_bwd_ms,
