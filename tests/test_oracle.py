@@ -397,6 +397,60 @@ def test_generator_deterministic_and_rounding():
     assert np.array_equal(A3[0], -np.arange(1, 17, dtype=np.float32))
 
 
+# ---------------------------------------------------------------- bf16 widening of the oracle
+
+def bf16_value(bits):
+    """A bf16 bit pattern's value from the format's definition (1 sign bit, 8 exponent
+    bits with bias 127, 7 fraction bits), in plain Python arithmetic."""
+    sign = -1.0 if bits & 0x8000 else 1.0
+    e, f = (bits >> 7) & 0xFF, bits & 0x7F
+    if e == 0xFF:
+        return sign * math.inf if f == 0 else math.nan
+    if e == 0:
+        return sign * f * 2.0 ** -133          # subnormal: 0.f * 2^-126 = f * 2^-7 * 2^-126
+    return sign * (1.0 + f / 128.0) * 2.0 ** (e - 127)
+
+
+def test_bf16_widening_matches_the_format():
+    # values fixed by the bf16 format itself, independent of any implementation
+    fixed = {0x3F80: 1.0, 0xC020: -2.5, 0x8000: -0.0, 0x0000: 0.0, 0x7F7F: (2 - 2 ** -7) * 2.0 ** 127,
+             0x0001: 2.0 ** -133, 0x0080: 2.0 ** -126, 0x4049: 3.140625, 0xBF00: -0.5, 0x7F80: math.inf,
+             0xFF80: -math.inf}
+    bits = np.array(sorted(fixed), dtype=np.uint16)
+    got = oracle.to_f64(bits)
+    for b, v in zip(bits.tolist(), got.tolist()):
+        assert v == fixed[b], hex(b)
+        assert math.copysign(1.0, v) == math.copysign(1.0, fixed[b]), hex(b)   # -0.0 keeps its sign
+    # every finite pattern against the format's definition
+    every = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    with np.errstate(invalid="ignore"):        # the NaN patterns
+        wide = oracle.to_f64(every)
+    ref = np.array([bf16_value(int(b)) for b in every.tolist()])
+    finite = np.isfinite(ref)
+    assert np.array_equal(wide[finite], ref[finite])
+    assert np.all(np.isnan(wide[np.isnan(ref)]))
+
+
+def test_bf16_inputs_equal_their_float_values():
+    # the oracle fed bf16 bit patterns gives bitwise the results of the same values given as floats
+    w = gen.workload(5, B=2, T=40, D=24)
+    inp = gen.make_inputs(w, seed=3)
+    assert inp["x"].dtype == np.uint16
+    as_float = {}
+    for k in ("x", "delta", "b", "c", "dy"):
+        flat = [bf16_value(int(v)) for v in inp[k].ravel().tolist()]
+        as_float[k] = np.array(flat, dtype=np.float64).reshape(inp[k].shape)
+    f1 = oracle.fwd(inp["x"], inp["delta"], inp["A"], inp["b"], inp["c"], None, ckpt_interval=16)
+    f2 = oracle.fwd(as_float["x"], as_float["delta"], inp["A"], as_float["b"], as_float["c"], None,
+                    ckpt_interval=16)
+    for k in f1:
+        assert np.array_equal(f1[k], f2[k]), k
+    g1 = oracle.bwd(inp["x"], inp["delta"], inp["A"], inp["b"], inp["c"], None, inp["dy"])
+    g2 = oracle.bwd(as_float["x"], as_float["delta"], inp["A"], as_float["b"], as_float["c"], None, as_float["dy"])
+    for k in g1:
+        assert np.array_equal(g1[k], g2[k]), k
+
+
 # ---------------------------------------------------------------- mutation tests
 
 MUTANTS = {
