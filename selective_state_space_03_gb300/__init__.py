@@ -16,12 +16,16 @@ state, hT, checkpoints and gradients are float32.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import threading
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_lib", "libssm_scan.so")
+# The same kernels with schedule overrides read from SSM_SCAN_FORCE_* environment variables,
+# for tests that pin every schedule; selected only inside ``testing_library()``.
+TESTING_LIB_PATH = os.path.join(_PKG, "_lib", "libssm_scan_testing.so")
 
 SSM_IO_F32, SSM_IO_BF16 = 0, 1
 MAX_BWD_CKPT_INTERVAL = 256   # longest checkpoint interval ssm_scan_bwd reads without a rebuild
@@ -45,18 +49,20 @@ class SSMError(RuntimeError):
 
 
 _lock = threading.Lock()
-_lib = None
+_libs = {}
+_testing_depth = 0
 
 
 def lib() -> ctypes.CDLL:
-    """The loaded C library; raises if it has not been built."""
-    global _lib
+    """The loaded C library (the testing build inside ``testing_library()``); raises if it
+    has not been built."""
+    path = TESTING_LIB_PATH if _testing_depth > 0 else LIB_PATH
     with _lock:
-        if _lib is None:
-            if not os.path.exists(LIB_PATH):
-                raise RuntimeError(f"{LIB_PATH} is missing: build it with `python -c \"import __graft_entry__ as g; "
+        if path not in _libs:
+            if not os.path.exists(path):
+                raise RuntimeError(f"{path} is missing: build it with `python -c \"import __graft_entry__ as g; "
                                    f"g.build()\"` (needs nvcc); there is no CPU fallback")
-            L = ctypes.CDLL(LIB_PATH)
+            L = ctypes.CDLL(path)
             vp, sz, dp = ctypes.c_void_p, ctypes.c_size_t, ctypes.POINTER(ssm_scan_desc)
             for name in ("ssm_scan_ckpt_bytes", "ssm_scan_fwd_workspace_bytes", "ssm_scan_bwd_workspace_bytes",
                          "ssm_scan_bwd_ckpt_workspace_bytes"):
@@ -74,8 +80,22 @@ def lib() -> ctypes.CDLL:
             L.ssm_scan_fwd_lookback_status.restype = ctypes.c_int
             L.ssm_status_str.argtypes = [ctypes.c_int]
             L.ssm_status_str.restype = ctypes.c_char_p
-            _lib = L
-    return _lib
+            _libs[path] = L
+    return _libs[path]
+
+
+@contextlib.contextmanager
+def testing_library():
+    """Route the calls made inside the block to libssm_scan_testing.so, whose schedule
+    choices (lane layouts, chunk-parallel backward, look-back polling) follow the
+    SSM_SCAN_FORCE_* / SSM_SCAN_LOOKBACK_POLLS / SSM_SCAN_TEST_LOOKBACK_DROP environment
+    variables. For tests only; the release library ignores those variables."""
+    global _testing_depth
+    _testing_depth += 1
+    try:
+        yield
+    finally:
+        _testing_depth -= 1
 
 
 SSM_SCAN_DETERMINISTIC = 1
@@ -368,4 +388,4 @@ _ScanFn = _Lazy()
 __all__ = ["lib", "ssm_scan_desc", "make_desc", "ssm_scan_fwd", "ssm_scan_bwd", "ssm_scan_step",
            "ssm_scan_fwd_noalloc", "selective_scan", "SSMError", "EXPORTS", "LIB_PATH", "SSM_IO_F32", "SSM_IO_BF16",
            "SSM_SCAN_DETERMINISTIC", "SSM_SCAN_DELTA_SOFTPLUS", "SSM_SCAN_LOOKBACK", "SSM_ERR_TIMEOUT",
-           "lookback_status"]
+           "lookback_status", "testing_library", "TESTING_LIB_PATH"]

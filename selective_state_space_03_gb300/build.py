@@ -2,7 +2,14 @@
 
 Objects are rebuilt when a source or header is newer; translation units compile
 in parallel. The library links the CUDA runtime statically, so it only needs the
-driver at run time. Output: ``_lib/libssm_scan.so`` inside this package.
+driver at run time. Outputs, inside this package:
+
+  _lib/libssm_scan.so          the library;
+  _lib/libssm_scan_testing.so  the same kernels with the C ABI compiled with
+                               SSM_SCAN_TESTING: schedule choices can then be
+                               overridden through SSM_SCAN_FORCE_* variables,
+                               for the tests that cover every schedule. The
+                               release library has no such overrides.
 """
 from __future__ import annotations
 
@@ -19,6 +26,8 @@ INCLUDE = os.path.join(ROOT, "include")
 OBJ_DIR = os.path.join(PKG, "_build")
 LIB_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIB_DIR, "libssm_scan.so")
+TESTING_LIB = os.path.join(LIB_DIR, "libssm_scan_testing.so")
+TESTING_SRC = "ssm_api.cu"          # the only translation unit that differs in the testing build
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
@@ -44,7 +53,7 @@ def _stale(target: str, deps) -> bool:
 
 
 def build(verbose: bool = False, ptxas_info: bool = False) -> str:
-    """Build (if needed) and return the path of libssm_scan.so."""
+    """Build (if needed) both libraries and return the path of libssm_scan.so."""
     os.makedirs(OBJ_DIR, exist_ok=True)
     os.makedirs(LIB_DIR, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
@@ -52,10 +61,12 @@ def build(verbose: bool = False, ptxas_info: bool = False) -> str:
     cc = nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_info else []
 
-    def compile_one(src):
-        obj = os.path.join(OBJ_DIR, os.path.basename(src)[:-3] + ".o")
+    def compile_one(job):
+        src, testing = job
+        obj = os.path.join(OBJ_DIR, os.path.basename(src)[:-3] + ("_testing.o" if testing else ".o"))
         if ptxas_info or _stale(obj, [src] + headers):
-            cmd = [cc] + NVCC_FLAGS + extra + ["-c", src, "-o", obj]
+            defs = ["-DSSM_SCAN_TESTING"] if testing else []
+            cmd = [cc] + NVCC_FLAGS + defs + extra + ["-c", src, "-o", obj]
             r = subprocess.run(cmd, capture_output=True, text=True)
             if r.returncode != 0:
                 raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
@@ -63,15 +74,19 @@ def build(verbose: bool = False, ptxas_info: bool = False) -> str:
                 print(r.stdout + r.stderr)
         return obj
 
+    jobs = [(s, False) for s in srcs] + [(os.path.join(CSRC, TESTING_SRC), True)]
     with ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
-        objs = list(ex.map(compile_one, srcs))
-    if _stale(LIB, objs):
-        tmp = LIB + f".tmp{os.getpid()}"
-        cmd = [cc] + ARCH + ["-shared", "-o", tmp] + objs
-        r = subprocess.run(cmd, capture_output=True, text=True)
-        if r.returncode != 0:
-            raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
+        objs = list(ex.map(compile_one, jobs))
+    release = objs[:len(srcs)]
+    testing = [o for s, o in zip(srcs, release) if os.path.basename(s) != TESTING_SRC] + [objs[-1]]
+    for lib, parts in ((LIB, release), (TESTING_LIB, testing)):
+        if _stale(lib, parts):
+            tmp = lib + f".tmp{os.getpid()}"
+            cmd = [cc] + ARCH + ["-shared", "-o", tmp] + parts
+            r = subprocess.run(cmd, capture_output=True, text=True)
+            if r.returncode != 0:
+                raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+            os.replace(tmp, lib)
     return LIB
 
 

@@ -8,6 +8,16 @@
 #include "ssm_internal.h"
 #include "ssm_scan.h"
 
+// Schedule overrides for tests, read from the environment at each call. They exist only in
+// the testing build of the library (libssm_scan_testing.so, compiled with SSM_SCAN_TESTING);
+// in the release library the macro is a null pointer, so the names are not even compiled in
+// and these variables have no effect.
+#ifdef SSM_SCAN_TESTING
+#define SSM_TEST_ENV(name) std::getenv(name)
+#else
+#define SSM_TEST_ENV(name) (static_cast<const char*>(nullptr))
+#endif
+
 namespace ssm {
 
 int device_sm_count() {
@@ -66,7 +76,7 @@ struct FwdPlan {
 
 // polls of a predecessor's flag before a look-back wait gives up (about a second)
 int64_t lookback_polls() {
-    if (const char* env = std::getenv("SSM_SCAN_LOOKBACK_POLLS")) {     // testing aid
+    if (const char* env = SSM_TEST_ENV("SSM_SCAN_LOOKBACK_POLLS")) {     // testing build only
         const long long v = std::atoll(env);
         if (v > 0) return v;
     }
@@ -87,8 +97,8 @@ FwdPlan plan_fwd(const ssm_scan_desc& d) {
         P.mode = 2;
         P.G = 4;
         P.kd = cs.kd;
-        // testing aid: channels per lane of both chunk passes (1 or 2)
-        if (const char* env = std::getenv("SSM_SCAN_FORCE_CHUNK_KD")) P.kd = std::atoi(env) == 2 ? 2 : 1;
+        // testing build only: channels per lane of both chunk passes (1 or 2)
+        if (const char* env = SSM_TEST_ENV("SSM_SCAN_FORCE_CHUNK_KD")) P.kd = std::atoi(env) == 2 ? 2 : 1;
         P.Lc = cs.Lc;
         P.nchunk = cdiv(d.T, cs.Lc);
         P.ws_S = align_up(size_t(d.B) * size_t(P.nchunk - 1) * size_t(d.D) * kDS * 4);
@@ -110,13 +120,13 @@ FwdPlan plan_fwd(const ssm_scan_desc& d) {
         const int64_t sms = device_sm_count();
         P.G = chains >= sms * 12 * 32 ? 2 : 4;
         P.kd = (P.G == 4 && chains >= sms * 4 * 16) ? 2 : 1;
-        // testing aids: force the layout ("2x2", "4x2", "4x1"; the older SSM_SCAN_FORCE_LANES
+        // testing build only: force the layout ("2x2", "4x2", "4x1"; the older SSM_SCAN_FORCE_LANES
         // takes 2 for 2x2 and 4 for 4x1)
-        if (const char* env = std::getenv("SSM_SCAN_FORCE_LANES")) {
+        if (const char* env = SSM_TEST_ENV("SSM_SCAN_FORCE_LANES")) {
             const int g = std::atoi(env);
             if (g == 2 || g == 4) { P.G = g; P.kd = g == 2 ? 2 : 1; }
         }
-        if (const char* env = std::getenv("SSM_SCAN_FORCE_FWD_LAYOUT")) {
+        if (const char* env = SSM_TEST_ENV("SSM_SCAN_FORCE_FWD_LAYOUT")) {
             if (std::strcmp(env, "2x2") == 0) { P.G = 2; P.kd = 2; }
             if (std::strcmp(env, "4x2") == 0) { P.G = 4; P.kd = 2; }
             if (std::strcmp(env, "4x1") == 0) { P.G = 4; P.kd = 1; }
@@ -134,8 +144,8 @@ cudaError_t run_fwd(const ssm_scan_desc& d, FwdLaunch L, int mode, cudaStream_t 
 // keeps more SMs busy on shapes with few (b, d) chains.
 int bwd_channels_per_lane(const ssm_scan_desc& d) {
     int kd = d.B * cdiv(d.D, 64) >= int64_t(device_sm_count()) * 4 ? 2 : 1;
-    // testing aid: force the layout (1 or 2)
-    if (const char* env = std::getenv("SSM_SCAN_FORCE_BWD_KD")) {
+    // testing build only: force the layout (1 or 2)
+    if (const char* env = SSM_TEST_ENV("SSM_SCAN_FORCE_BWD_KD")) {
         const int k = std::atoi(env);
         if (k == 1 || k == 2) kd = k;
     }
@@ -154,8 +164,8 @@ bool bwd_chunk_parallel(const ssm_scan_desc& d) {
     const int64_t nck = cdiv(d.T, bwd_internal_K(d));
     if (nck < 2 || nck > 65535) return false;
     bool on = bwd_channels_per_lane(d) == 1 && d.B * cdiv(d.D, 32) < int64_t(device_sm_count()) * 4;
-    // testing aid: force the schedule on (1) or off (0)
-    if (const char* env = std::getenv("SSM_SCAN_FORCE_BWD_TPAR")) {
+    // testing build only: force the schedule on (1) or off (0)
+    if (const char* env = SSM_TEST_ENV("SSM_SCAN_FORCE_BWD_TPAR")) {
         const int k = std::atoi(env);
         if (k == 0 || k == 1) on = k == 1;
     }
@@ -298,7 +308,7 @@ ssm_status ssm_scan_fwd_fused(const ssm_scan_desc* desc, const void* x, const vo
         L.lb_flags = reinterpret_cast<int*>(z + 16);
         L.lb_ticket = reinterpret_cast<int*>(z + 16 + size_t(P.nchunk) * size_t(d.B) * nblk * 4);
         L.lb_polls = lookback_polls();
-        L.lb_test_drop = std::getenv("SSM_SCAN_TEST_LOOKBACK_DROP") != nullptr;   // testing aid
+        L.lb_test_drop = SSM_TEST_ENV("SSM_SCAN_TEST_LOOKBACK_DROP") != nullptr;   // testing build only
         e = cudaMemsetAsync(z, 0, P.lb_zero, s);
         if (e == cudaSuccess) e = run_fwd(d, L, 4, s);
     } else {

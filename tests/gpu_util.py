@@ -1,4 +1,8 @@
-"""Helpers shared by the GPU parity tests: device transfer, tolerances, sampling."""
+"""Helpers shared by the GPU parity tests: device transfer, tolerances, sampling,
+schedule overrides."""
+import contextlib
+import os
+
 import numpy as np
 
 TOL = {  # max |got - ref| / (1 + |ref|), elementwise
@@ -67,3 +71,26 @@ def sub_inputs(inp, bsel, dsel):
     for k in ("h0", "ghT"):
         out[k] = None if inp.get(k) is None else inp[k][bsel][:, dsel]
     return out
+
+
+@contextlib.contextmanager
+def forced(**env):
+    """Pin schedule choices for the block: set the SSM_SCAN_* override variables given
+    (None = leave unset) and route the calls to the testing build of the library, the
+    only one that reads them."""
+    import selective_state_space_03_gb300 as ssm
+    old = {k: os.environ.get(k) for k in env}
+    for k, v in env.items():
+        if v is not None:
+            os.environ[k] = str(v)
+    try:
+        with ssm.testing_library():
+            yield
+    finally:
+        for k, v in env.items():
+            if v is None:
+                continue
+            if old[k] is None:
+                del os.environ[k]
+            else:
+                os.environ[k] = old[k]

@@ -242,7 +242,27 @@ def test_product_path_does_not_import_the_oracle(L):
 
 def test_missing_library_raises_instead_of_falling_back(monkeypatch):
     import selective_state_space_03_gb300 as m
-    monkeypatch.setattr(m, "_lib", None)
+    monkeypatch.setattr(m, "_libs", {})
     monkeypatch.setattr(m, "LIB_PATH", os.path.join(ROOT, "no_such_dir", "libssm_scan.so"))
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         m.lib()
+
+
+def test_schedule_overrides_exist_only_in_the_testing_build(L):
+    # the release library compiles none of the SSM_SCAN_FORCE_* / test-only names, so a stray
+    # variable in a user's environment cannot change its schedule or results; the testing build
+    # (used by the GPU tests that pin every schedule) has them all
+    import selective_state_space_03_gb300 as ssm
+    names = [b"SSM_SCAN_FORCE_LANES", b"SSM_SCAN_FORCE_FWD_LAYOUT", b"SSM_SCAN_FORCE_CHUNK_KD",
+             b"SSM_SCAN_FORCE_BWD_KD", b"SSM_SCAN_FORCE_BWD_TPAR", b"SSM_SCAN_LOOKBACK_POLLS",
+             b"SSM_SCAN_TEST_LOOKBACK_DROP"]
+    release = open(ssm.LIB_PATH, "rb").read()
+    testing = open(ssm.TESTING_LIB_PATH, "rb").read()
+    for n in names:
+        assert n not in release, n
+        assert n in testing, n
+    with ssm.testing_library():
+        T = ssm.lib()
+    assert T is not L and ssm.lib() is L
+    for name in declared_functions():
+        assert hasattr(T, name), name

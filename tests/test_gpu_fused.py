@@ -8,15 +8,13 @@ layouts, the chunk-parallel backward, the deterministic sums and the decode
 step. Tolerances as for the plain scan: float32 I/O 1e-4 (y, hT) and 1e-3
 (gradients), bf16 I/O 1e-2, as max |got - ref| / (1 + |ref|).
 """
-import contextlib
-import os
 
 import numpy as np
 import pytest
 
 import gen
 import oracle
-from gpu_util import GRADS, assert_close, dev_inputs, to_dev, to_host
+from gpu_util import GRADS, assert_close, dev_inputs, to_dev, to_host, forced
 
 pytestmark = pytest.mark.gpu
 
@@ -36,23 +34,6 @@ def ssm():
     return m
 
 
-@contextlib.contextmanager
-def forced(**env):
-    """Set layout overrides of the library (read at each call) for the block."""
-    old = {k: os.environ.get(k) for k in env}
-    for k, v in env.items():
-        if v is not None:
-            os.environ[k] = str(v)
-    try:
-        yield
-    finally:
-        for k, v in env.items():
-            if v is None:
-                continue
-            if old[k] is None:
-                del os.environ[k]
-            else:
-                os.environ[k] = old[k]
 
 
 def fused_case(w, K, softplus=True, skip=True, chunk_len=0, lanes=None, kd=None, tpar=None, det=False,

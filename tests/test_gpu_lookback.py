@@ -9,15 +9,13 @@ chunk 0 publish nothing (a testing aid of the library), so the waits of chunk
 1 run out after a short poll budget: the launch must still finish, the status
 query must report SSM_ERR_TIMEOUT, and the next call must work.
 """
-import contextlib
-import os
 
 import numpy as np
 import pytest
 
 import gen
 import oracle
-from gpu_util import assert_close, dev_inputs, to_dev, to_host
+from gpu_util import assert_close, dev_inputs, to_dev, to_host, forced
 
 pytestmark = pytest.mark.gpu
 
@@ -37,22 +35,6 @@ def ssm():
     return m
 
 
-@contextlib.contextmanager
-def forced(**env):
-    old = {k: os.environ.get(k) for k in env}
-    for k, v in env.items():
-        if v is not None:
-            os.environ[k] = str(v)
-    try:
-        yield
-    finally:
-        for k, v in env.items():
-            if v is None:
-                continue
-            if old[k] is None:
-                del os.environ[k]
-            else:
-                os.environ[k] = old[k]
 
 
 def lookback_case(w, K, chunk_len, chunk_kd=None, softplus=False, skip=False, seed=0):
@@ -130,6 +112,26 @@ def test_lookback_timeout_is_reported_and_the_context_survives():
     # the GPU context is still good: the same call without the testing aid is correct
     lookback_case(w, K=0, chunk_len=64)
     torch.cuda.synchronize()
+
+
+def test_release_library_ignores_the_testing_variables():
+    # the same variables outside testing_library(): the release build has no such overrides,
+    # so the look-back call completes normally and matches the oracle
+    import os
+    m = ssm()
+    w = gen.workload(2, B=2, T=256, D=32, h0_std=0.1)
+    inp = gen.make_inputs(w, with_grad_inputs=False)
+    t = dev_inputs(inp)
+    os.environ["SSM_SCAN_TEST_LOOKBACK_DROP"], os.environ["SSM_SCAN_LOOKBACK_POLLS"] = "1", "2000"
+    try:
+        y, hT, _ = m.ssm_scan_fwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], chunk_len=64,
+                                  lookback=True)
+        m.lookback_status()                # raises on a timeout
+    finally:
+        del os.environ["SSM_SCAN_TEST_LOOKBACK_DROP"], os.environ["SSM_SCAN_LOOKBACK_POLLS"]
+    ref = oracle.fwd(inp["x"], inp["delta"], inp["A"], inp["b"], inp["c"], inp["h0"])
+    assert_close(to_host(y), ref["y"], "f32", "fwd", "y")
+    assert_close(to_host(hT), ref["hT"], "f32", "fwd", "hT")
 
 
 def test_lookback_grid_beyond_resident_ctas():

@@ -7,15 +7,13 @@ and check the Euler identities of the loss on the full outputs.
 Tolerances: float32 I/O 1e-4 (y, hT) and 1e-3 (gradients); bf16 I/O 1e-2;
 all as max |got - ref| / (1 + |ref|).
 """
-import contextlib
-import os
 
 import numpy as np
 import pytest
 
 import gen
 import oracle
-from gpu_util import GRADS, assert_close, dev_inputs, sample_indices, sub_inputs, to_dev, to_host
+from gpu_util import GRADS, assert_close, dev_inputs, sample_indices, sub_inputs, to_dev, to_host, forced
 
 pytestmark = pytest.mark.gpu
 
@@ -35,20 +33,6 @@ def ssm():
     return m
 
 
-@contextlib.contextmanager
-def forced(var, value):
-    """Set a layout override of the library (read at each call) for the block."""
-    old = os.environ.get(var)
-    if value is not None:
-        os.environ[var] = str(value)
-    try:
-        yield
-    finally:
-        if value is not None:
-            if old is None:
-                del os.environ[var]
-            else:
-                os.environ[var] = old
 
 
 def run_case(w, K, chunk_len=0, seed=0, ghT=False, bwd=True, lanes=None, ckpt_to_bwd=True, bwd_kd=None,
@@ -56,8 +40,7 @@ def run_case(w, K, chunk_len=0, seed=0, ghT=False, bwd=True, lanes=None, ckpt_to
     import torch
     inp = gen.make_inputs(w, seed=seed, with_grad_inputs=bwd, with_ghT=ghT)
     t = dev_inputs(inp)
-    with forced("SSM_SCAN_FORCE_LANES", lanes), forced("SSM_SCAN_FORCE_FWD_LAYOUT", fwd_layout), \
-            forced("SSM_SCAN_FORCE_CHUNK_KD", chunk_kd):
+    with forced(SSM_SCAN_FORCE_LANES=lanes, SSM_SCAN_FORCE_FWD_LAYOUT=fwd_layout, SSM_SCAN_FORCE_CHUNK_KD=chunk_kd):
         y, hT, ckpt = ssm().ssm_scan_fwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], ckpt_interval=K,
                                          chunk_len=chunk_len)
     torch.cuda.synchronize()
@@ -68,7 +51,7 @@ def run_case(w, K, chunk_len=0, seed=0, ghT=False, bwd=True, lanes=None, ckpt_to
         assert_close(to_host(ckpt), ref["ckpt"], w.io, "fwd", "ckpt")
     if not bwd:
         return
-    with forced("SSM_SCAN_FORCE_BWD_KD", bwd_kd), forced("SSM_SCAN_FORCE_BWD_TPAR", bwd_tpar):
+    with forced(SSM_SCAN_FORCE_BWD_KD=bwd_kd, SSM_SCAN_FORCE_BWD_TPAR=bwd_tpar):
         g = ssm().ssm_scan_bwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"],
                                ckpt if ckpt_to_bwd else None, t["dy"], t["ghT"], ckpt_interval=K,
                                workspace=bwd_workspace, deterministic=deterministic)
@@ -158,7 +141,7 @@ def test_deterministic_backward(layout, io):
     t = dev_inputs(inp)
     _, _, ck = ssm().ssm_scan_fwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], ckpt_interval=64)
     runs = []
-    with forced("SSM_SCAN_FORCE_BWD_KD", env["bwd_kd"]), forced("SSM_SCAN_FORCE_BWD_TPAR", env["bwd_tpar"]):
+    with forced(SSM_SCAN_FORCE_BWD_KD=env["bwd_kd"], SSM_SCAN_FORCE_BWD_TPAR=env["bwd_tpar"]):
         for _ in range(3):
             runs.append(ssm().ssm_scan_bwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], ck, t["dy"],
                                            t["ghT"], ckpt_interval=64, deterministic=True))
@@ -275,7 +258,7 @@ def test_outputs_stay_in_bounds_and_forward_is_deterministic(bwd_kd):
         grads[k] = inner
     shapes = {"gx": (B, T, D), "gdelta": (B, T, D), "gA": (D, 16), "gb": (B, T, 16), "gc": (B, T, 16),
               "gh0": (B, D, 16)}
-    with forced("SSM_SCAN_FORCE_BWD_KD", bwd_kd):
+    with forced(SSM_SCAN_FORCE_BWD_KD=bwd_kd):
         m.ssm_scan_bwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], ck.view(3, B, D, 16), t["dy"],
                        t["ghT"], ckpt_interval=32, grads={k: v.view(shapes[k]) for k, v in grads.items()})
     torch.cuda.synchronize()

@@ -9,15 +9,13 @@ them; it then compares every output with the float64 oracle at the usual
 tolerances. The draws are fixed by the seed, so a failure names a
 reproducible case.
 """
-import contextlib
-import os
 
 import numpy as np
 import pytest
 
 import gen
 import oracle
-from gpu_util import GRADS, assert_close, dev_inputs, to_dev, to_host
+from gpu_util import GRADS, assert_close, dev_inputs, to_dev, to_host, forced
 
 pytestmark = pytest.mark.gpu
 
@@ -32,22 +30,6 @@ def _setup():
     torch.cuda.set_device(0)
 
 
-@contextlib.contextmanager
-def forced(**env):
-    old = {k: os.environ.get(k) for k in env}
-    for k, v in env.items():
-        if v is not None:
-            os.environ[k] = str(v)
-    try:
-        yield
-    finally:
-        for k, v in env.items():
-            if v is None:
-                continue
-            if old[k] is None:
-                del os.environ[k]
-            else:
-                os.environ[k] = old[k]
 
 
 def draw_case(seed):
