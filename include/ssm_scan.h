@@ -231,10 +231,14 @@ ssm_status ssm_scan_bwd_fused(const ssm_scan_desc* desc,
  * B*(nchunk-1)*D*68 bytes (each part rounded up to 256); larger problems are
  * rejected with SSM_ERR_WORKSPACE before anything is enqueued.
  *
- * The first call on each device looks up the array's device address with that
- * device current (later calls reuse it), so make the first call before any
- * stream capture. All calls on a device share the array: calls that overlap on
- * the GPU race on it, so the caller must order them (one stream, or events).
+ * Each call looks up the array's device address in the CUDA context current on
+ * the calling thread (cudaGetSymbolAddress, a host-side lookup that allocates
+ * nothing): every context has its own copy of the array, so calls from another
+ * context of the same device, or after a device reset, use that context's copy.
+ * The first call in a context loads the library's device code there, so make
+ * it before any stream capture. All calls in a context share the array: calls
+ * that overlap on the GPU race on it, so the caller must order them (one
+ * stream, or events).
  * Nothing in the array needs clearing: each call writes every entry it reads.
  * Arguments, layouts, results and other errors are those of ssm_scan_fwd. */
 #define SSM_SCAN_NOALLOC_SCRATCH_BYTES (8u << 20)
@@ -259,10 +263,10 @@ ssm_status ssm_scan_fwd_noalloc(const ssm_scan_desc* desc,
  * b, c and h: 16 bytes), so one step's rows of (B, T, D) tensors can be passed
  * as they are.
  * Steps are launched as programmatic dependents of the preceding kernel on the
- * stream: after an earlier ssm_scan_step, a step may already read its own x,
- * delta, A, b and c while that step finishes (it waits for it before reading h),
- * so these five must not be the h or y written by the preceding step call.
- * After any other kernel or copy the step starts only when that one is done. */
+ * stream: a step's CTAs may be scheduled while that kernel finishes, but every
+ * load waits until it has completed and its writes are visible, so any input
+ * may be the output of the preceding kernel (a projection, or the previous
+ * step's h and y). */
 ssm_status ssm_scan_step(const ssm_scan_desc* desc,
                          const void* x, const void* delta, const float* A,
                          const void* b, const void* c, float* h, void* y, void* stream);

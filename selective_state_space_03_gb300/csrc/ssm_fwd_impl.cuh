@@ -544,6 +544,9 @@ __global__ void __launch_bounds__(32, FwdCfg<TIO, 4, KD>::MINB) fwd_lookback_ker
             const int first = stop ? __ffs(int(stop)) - 1 : 32;
             const bool done = first < 32 && ((incl >> first) & 1u);
             const int n = first + (done ? 1 : 0);          // predecessors to fold now (warp-uniform)
+            // lane i's acquire load saw predecessor j - i published; the barrier orders that
+            // acquire before every lane's loads of the predecessor's payload below
+            __syncwarp();
             for (int i0 = 0; i0 < n; i0 += NB) {
                 float2 v[NB][KD][KP];
                 float sdv[NB][KD];

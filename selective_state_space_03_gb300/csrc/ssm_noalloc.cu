@@ -13,16 +13,18 @@
 // Costs and rules of that choice:
 //  - every GPU that loads the library holds kNoallocScratchBytes of device
 //    memory for this array until the process exits;
-//  - host code cannot use the array's name as a device address, so the first
-//    call on each device looks the address up (cudaGetSymbolAddress, with
-//    that device current) and caches it; that first call should therefore
-//    happen before any stream capture;
+//  - host code cannot use the array's name as a device address, so every call
+//    looks the address up (cudaGetSymbolAddress) in the context current on the
+//    calling thread: each CUDA context (each device's primary context, a
+//    driver-API context of the caller's, the context that replaces one after a
+//    device reset) has its own copy of the array, and a cached address would
+//    outlive its context. The first call in a context loads the library's device
+//    code there, so make it before any stream capture;
 //  - every call on a device shares the one array: calls that overlap on the
 //    GPU (other streams, other host threads) race on it and must be ordered by
 //    the caller. Pass 1 overwrites every entry pass 2 reads, so nothing in the
 //    array needs clearing between calls.
 #include <algorithm>
-#include <mutex>
 
 #include "ssm_internal.h"
 #include "ssm_scan.h"
@@ -36,24 +38,13 @@ static_assert(kNoallocScratchBytes % 256 == 0, "scratch size must keep 256-byte 
 
 static __device__ __align__(256) unsigned char g_scratch[kNoallocScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_setup_mutex;
-void* g_scratch_addr[kMaxDevices] = {};
-
-// Device address of g_scratch on the current device (looked up once per device).
+// Device address of g_scratch in the calling thread's current context (a host-side lookup
+// once the context has loaded the library's device code; it allocates nothing).
 cudaError_t scratch_address(void** out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_scratch);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (g_scratch_addr[dev] == nullptr) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_scratch);
-        if (e != cudaSuccess) return e;
-        g_scratch_addr[dev] = p;
-    }
-    *out = g_scratch_addr[dev];
+    *out = p;
     return cudaSuccess;
 }
 

@@ -12,9 +12,10 @@
 // lanes per chain, 8 states per lane in two 16-byte loads and stores, the
 // readout finished with one shuffle; 64 chains per 128-thread CTA (with 4 lanes
 // per chain workload 5's 81920 chains took 2560 CTAs, 1.05 waves at 16 per SM;
-// with 2, 1280 CTAs fit in one). Steps are launched
-// with programmatic stream serialization: a step's loads of its own inputs
-// overlap the end of the previous step, and only the state load waits for it.
+// with 2, 1280 CTAs fit in one). Steps are launched with programmatic stream
+// serialization: a step's CTAs are scheduled while the previous kernel on the
+// stream finishes, and every load waits (griddepcontrol.wait) until that
+// kernel has completed and its writes are visible, whatever kernel it was.
 #include "ssm_common.cuh"
 #include "ssm_internal.h"
 #include "ssm_scan.h"
@@ -58,12 +59,18 @@ __global__ void __launch_bounds__(128) step_kernel(const StepLaunch p) {
     const int sg = int(gid & 1), s0 = sg * 8;
     const bool valid = chain < p.B * p.D;       // whole lane pairs are valid or not
     // Consecutive steps on a stream are launched as programmatic dependents: let the next
-    // step's CTAs start now; they run up to their wait below while this grid finishes.
+    // step's CTAs be scheduled now; they run up to their wait below while this grid finishes.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // Every input may have been written by the kernel before this one on the stream (the
+    // previous step writes h and y; a projection kernel may write x, delta, b, c, even one
+    // that lets its dependents launch before its own stores): wait until that grid has
+    // completed and its writes are visible before loading anything (returns at once when
+    // there is no such grid).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     float acc = 0.f;
     float hv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     float dl = 0.f, dx = 0.f, bv[8], cv[8], av[8];
-    if (valid) {      // this step's inputs, which no earlier step writes
+    if (valid) {
         const int64_t bb = chain / p.D, d = chain - bb * p.D;
         dl = to_f32(static_cast<const TIO*>(p.delta)[chain]);
         if (p.softplus) dl = softplus_f32(dl);
@@ -71,11 +78,6 @@ __global__ void __launch_bounds__(128) step_kernel(const StepLaunch p) {
         load8<TIO>(static_cast<const TIO*>(p.b) + bb * kDS + s0, bv);
         load8<TIO>(static_cast<const TIO*>(p.c) + bb * kDS + s0, cv);
         load8<float>(p.A + d * kDS + s0, av);
-    }
-    // the state (and y) belong to the previous step: wait until the grid before this one has
-    // completed and its writes are visible (returns at once without such a grid)
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (valid) {
         load8<float>(p.h + chain * kDS + s0, hv);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -126,7 +128,7 @@ extern "C" ssm_status ssm_scan_step(const ssm_scan_desc* desc, const void* x, co
     cfg.blockDim = dim3(128);
     cfg.stream = static_cast<cudaStream_t>(stream);
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // overlap with the previous step
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // scheduled while the previous kernel ends
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;

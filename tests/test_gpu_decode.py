@@ -99,3 +99,31 @@ def test_step_writes_only_its_outputs():
     torch.cuda.synchronize()
     for full in (hb, yb):
         assert torch.all(full[:pad] == canary) and torch.all(full[-pad:] == canary)
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_step_after_a_kernel_that_writes_its_inputs(io):
+    # decode as a model runs it: another kernel (here torch's copy) writes x, delta, b and c into
+    # the same buffers right before every step on the same stream; each step must read the new
+    # values (a step is launched as a programmatic dependent, so it may be scheduled early, but
+    # every load waits for the preceding kernel)
+    import torch
+    w = gen.workload(5, B=4, T=12, D=1024, io=io, h0_std=0.3)
+    inp = gen.make_inputs(w, seed=9, with_grad_inputs=False)
+    t = dev_inputs(inp)
+    h = t["h0"].clone()
+    xs, ds = torch.empty_like(t["x"][:, 0]), torch.empty_like(t["delta"][:, 0])
+    bs, cs = torch.empty_like(t["b"][:, 0]), torch.empty_like(t["c"][:, 0])
+    ys = []
+    for k in range(w.T):
+        xs.copy_(t["x"][:, k])
+        ds.copy_(t["delta"][:, k])
+        bs.copy_(t["b"][:, k])
+        cs.copy_(t["c"][:, k])
+        y = torch.empty_like(xs)
+        ssm().ssm_scan_step(xs, ds, t["A"], bs, cs, h, y=y)
+        ys.append(y)
+    torch.cuda.synchronize()
+    ref = oracle.fwd(inp["x"], inp["delta"], inp["A"], inp["b"], inp["c"], inp["h0"])
+    assert_close(np.stack([to_host(v) for v in ys], 1), ref["y"], io, "fwd", "y")
+    assert_close(to_host(h), ref["hT"], io, "fwd", "h")

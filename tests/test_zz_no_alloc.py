@@ -5,9 +5,11 @@ another runtime that owns all device memory, or services that keep cudaMalloc
 off the hot path because it synchronises the device and can fail under memory
 pressure). For them the library keeps the chunked forward's scratch in a fixed
 device array. These tests call that entry point through the C ABI (ctypes)
-and compare it with ssm_scan_fwd on the same inputs and chunk length, on two
-calls in a row (the second reuses the array the first one wrote). The file is
-named so that pytest collects it last.
+and compare it with the float64 oracle and with ssm_scan_fwd on the same
+inputs and chunk length, on two calls in a row (the second reuses the array
+the first one wrote), including the one-chunk case (no scratch) and a problem
+that fills the array to just under its size. The file is named so that
+pytest collects it last.
 """
 import ctypes
 
@@ -51,20 +53,73 @@ def call_noalloc(L, t, w, K, chunk_len):
     return y, hT, ck
 
 
+def check_against_oracle(inp, K, y, hT, ck, io, bsel=None, dsel=None):
+    import oracle
+    import torch
+    from gpu_util import sub_inputs
+    if bsel is None:
+        sub = inp
+        pick = lambda v, chan_axis: v  # noqa: E731
+    else:
+        sub = sub_inputs(inp, bsel, dsel)
+        bi, di = torch.as_tensor(bsel, device=y.device), torch.as_tensor(dsel, device=y.device)
+        pick = lambda v, chan_axis: v[bi].index_select(chan_axis, di)  # noqa: E731
+    ref = oracle.fwd(sub["x"], sub["delta"], sub["A"], sub["b"], sub["c"], sub["h0"], ckpt_interval=K)
+    assert_close(to_host(pick(y, 2)), ref["y"], io, "fwd", "y")
+    assert_close(to_host(pick(hT, 1)), ref["hT"], io, "fwd", "hT")
+    if bsel is None:
+        assert_close(to_host(ck), ref["ckpt"], io, "fwd", "ckpt")
+    else:
+        bi, di = torch.as_tensor(bsel, device=ck.device), torch.as_tensor(dsel, device=ck.device)
+        assert_close(to_host(ck[:, bi][:, :, di]), ref["ckpt"], io, "fwd", "ckpt")
+
+
 def test_noalloc_matches_workspace_forward_two_calls(L):
+    # each case twice in a row (the second call reuses the array the first one wrote), against
+    # the oracle and against ssm_scan_fwd with the caller's workspace
     import torch
     import selective_state_space_03_gb300 as ssm
     cases = [(gen.workload(2, B=2, T=700, D=96, h0_std=0.1), 128, 100, 0),
-             (gen.workload(5, B=3, T=513, D=64), 64, 96, 1)]
+             (gen.workload(5, B=3, T=513, D=64), 64, 96, 1),
+             # one chunk (chunk_len >= T): the one-pass scan, no scratch
+             (gen.workload(2, B=2, T=200, D=40, h0_std=0.1), 50, 256, 2)]
     for w, K, chunk_len, seed in cases:
-        t = dev_inputs(gen.make_inputs(w, seed=seed, with_grad_inputs=False))
+        inp = gen.make_inputs(w, seed=seed, with_grad_inputs=False)
+        t = dev_inputs(inp)
         y0, h0, c0 = ssm.ssm_scan_fwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], ckpt_interval=K,
                                       chunk_len=chunk_len)
-        y1, h1, c1 = call_noalloc(L, t, w, K, chunk_len)
-        torch.cuda.synchronize()
-        assert_close(to_host(y1), to_host(y0), w.io, "fwd", "y")
-        assert_close(to_host(h1), to_host(h0), w.io, "fwd", "hT")
-        assert_close(to_host(c1), to_host(c0), w.io, "fwd", "ckpt")
+        for _ in range(2):
+            y1, h1, c1 = call_noalloc(L, t, w, K, chunk_len)
+            torch.cuda.synchronize()
+            check_against_oracle(inp, K, y1, h1, c1, w.io)
+            assert_close(to_host(y1), to_host(y0), w.io, "fwd", "y")
+            assert_close(to_host(h1), to_host(h0), w.io, "fwd", "hT")
+            assert_close(to_host(c1), to_host(c0), w.io, "fwd", "ckpt")
+
+
+def test_noalloc_at_its_scratch_limit(L):
+    # B = 1, D = 4096, 31 chunks of 64 steps: 30 carries take 30*4096*64 + 30*4096*4 = 8,355,840
+    # bytes, just under the 8 MiB array; sampled channels against the oracle, all of them
+    # against ssm_scan_fwd
+    import torch
+    import selective_state_space_03_gb300 as ssm
+    from gpu_util import sample_indices
+    w = gen.workload(2, B=1, T=31 * 64, D=4096, h0_std=0.1)
+    assert 30 * 4096 * 68 <= (8 << 20) < 31 * 4096 * 68
+    inp = gen.make_inputs(w, seed=4, with_grad_inputs=False)
+    t = dev_inputs(inp)
+    y0, h0, c0 = ssm.ssm_scan_fwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], ckpt_interval=256,
+                                  chunk_len=64)
+    y1, h1, c1 = call_noalloc(L, t, w, 256, 64)
+    torch.cuda.synchronize()
+    check_against_oracle(inp, 256, y1, h1, c1, w.io, bsel=np.array([0]), dsel=sample_indices(w.D, 24, 5))
+    assert_close(to_host(y1), to_host(y0), w.io, "fwd", "y")
+    assert_close(to_host(h1), to_host(h0), w.io, "fwd", "hT")
+    # one chunk more does not fit
+    desc = ssm.make_desc(1, 32 * 64, 4096, 16, ssm.SSM_IO_F32, 0, 64)
+    fake = ctypes.c_void_p(0x7F0000000000)
+    st = L.ssm_scan_fwd_noalloc(ctypes.byref(desc), fake, fake, fake, fake, fake, None, fake, None, None, None)
+    assert st == 4
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch(L):
