@@ -51,10 +51,9 @@ def load_peaks():
         return 6800.0, "fallback"
 
 
-# DRAM bytes (read + write) of one bwd2_kernel launch at workload 5, from the ncu capture
-# summarised in profiles/bwd2_kernel_B16_T512_D5120.md: 691.4 MB at T = 512, and traffic
-# grows with the number of steps, so 4 x that at T = 2048. Reset to None whenever the
-# kernel changes until it is captured again.
+# DRAM bytes (read + write) of one bwd2_kernel launch at workload 5, from an ncu capture of
+# the same kernel at T = 512 (691.4 MB): traffic grows with the number of steps, so 4 x that
+# at T = 2048. Reset to None whenever the kernel changes until it is captured again.
 BWD2_TRAFFIC = {"bytes_per_launch": 4 * 691.428608e6,
                 "source": "ncu dram__bytes_read+write of bwd2_kernel at T=512 (691.4 MB) x 4 steps ratio"}
 
@@ -76,10 +75,19 @@ def compulsory_bytes(w, direction):
 # state from checkpoints: recompute delta*A, a*h, +delta*x*b (3); adjoint
 # dy*c, g update, a*g, p = (a g) h_{t-1}, gA, gdelta, <g,b>, gb term, gc term (9).
 BWD_OPS_PER_ELEM = 12
-FWD_EX2_PER_ELEM = 1    # one exp per element (MUFU)
-BWD_EX2_PER_ELEM = 3    # exps the backward executes per element: two recompute levels and the reverse sweep
-EX2_PER_SM_CLK = 32     # GB300 MUFU ex2 throughput, measured on the box
-FP32_PER_SM_CLK = 128   # FP32 FMA lanes per SM
+# Exponentials per element the method needs (the roofline's algorithmic count): the forward
+# one; the backward two (the state recomputed once from its checkpoint, the decay once more
+# in the reverse sweep). The kernels execute 1 (forward), 3 (backward: two recompute levels
+# and the reverse sweep) and 2 (chunked forward: pass 1 and pass 2); the fractions below use
+# the algorithmic counts.
+FWD_EX2_PER_ELEM = 1
+BWD_EX2_PER_ELEM = 2
+BWD_EX2_EXECUTED_PER_ELEM = 3
+# Per-SM rates of one GB300 SM, from bench.py --rates (bench_rates.cu: clock64-timed loops of
+# independent chains, 152 SMs): ex2.approx 32.0 per clock, scalar FFMA 125 lanes per clock
+# (128 nominal), packed FFMA2 62 pairs per clock.
+EX2_PER_SM_CLK = 32
+FP32_PER_SM_CLK = 128
 
 
 # ---------------------------------------------------------------- multi-rank aggregation
@@ -420,10 +428,23 @@ def run_ours(args, rank, world, local_rank):
     fwd_ex2 = el * FWD_EX2_PER_ELEM / (fwd_ms / 1e3)
     bwd_ex2 = el * BWD_EX2_PER_ELEM / (bwd_ms / 1e3)
     fwd_bytes, bwd_bytes = compulsory_bytes(w, "fwd"), compulsory_bytes(w, "bwd")
+    # the other workloads' fractions, on the same peaks (algorithmic ex2 count, compulsory bytes)
+    for wk in (gen.workload(2), gen.workload(3), gen.workload(4)):
+        ent = extra.get(wk.name)
+        if not ent:
+            continue
+        elw = gen.elements(wk)
+        for direction, key, n_ex2 in (("fwd", "fwd_ms", FWD_EX2_PER_ELEM), ("bwd", "bwd_ms", BWD_EX2_PER_ELEM)):
+            if key not in ent:
+                continue
+            secs = ent[key] / 1e3
+            ent[direction + "_ex2_frac"] = elw * n_ex2 / secs / ex2_peak
+            ent[direction + "_hbm_frac"] = compulsory_bytes(wk, direction) / secs / 1e9 / hbm_peak
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded Philox normals, gen.make_inputs)",
+        "vs_baseline": None, "dtype": "f32", "io_dtype": w.io,
+        "data": "synthetic (seeded Philox normals, gen.make_inputs)",
         "config": workload_config(w, world),
         "kernels": {"fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "bwd_deterministic_ms": bwd_det_ms,
                     "fused_softplus_skip_fwd_ms": fused_fwd_ms, "fused_softplus_skip_bwd_ms": fused_bwd_ms,
@@ -432,8 +453,10 @@ def run_ours(args, rank, world, local_rank):
                     "fwd_hbm_frac": fwd_bytes / (fwd_ms / 1e3) / 1e9 / hbm_peak,
                     "bwd_hbm_frac": bwd_bytes / (bwd_ms / 1e3) / 1e9 / hbm_peak,
                     "fwd_ex2_frac": fwd_ex2 / ex2_peak, "bwd_ex2_frac": bwd_ex2 / ex2_peak,
-                    "ex2_basis": f"MUFU ex2 executed ({FWD_EX2_PER_ELEM}/element forward, {BWD_EX2_PER_ELEM}/element "
-                                 f"backward) vs {EX2_PER_SM_CLK}/clk/SM x SMs x median SM clock"},
+                    "bwd_ex2_executed_frac": bwd_ex2 * BWD_EX2_EXECUTED_PER_ELEM / BWD_EX2_PER_ELEM / ex2_peak,
+                    "ex2_basis": f"algorithmic MUFU ex2 ({FWD_EX2_PER_ELEM}/element forward, {BWD_EX2_PER_ELEM}/element "
+                                 f"backward; the backward executes {BWD_EX2_EXECUTED_PER_ELEM}) vs {EX2_PER_SM_CLK}"
+                                 f"/clk/SM x SMs x median SM clock"},
         "roofline": {"kernel": "bwd2_kernel (reverse sweep with recompute, two channels per lane)", "bound": "alu",
                      "achieved": bwd_ops / 1e12, "peak": fp32_peak / 1e12, "unit": "TFLOP/s",
                      "frac": bwd_ops / fp32_peak, "traffic": BWD2_TRAFFIC["bytes_per_launch"],
@@ -688,6 +711,21 @@ def run_profile_case(args):
     print("ok")
 
 
+def run_rates():
+    """Build and run bench_rates.cu (per-SM ex2, FFMA, FFMA2, shuffle and shared-load rates,
+    and a 2 GiB device copy) and print its JSON line: the measurements behind the roofline
+    constants above."""
+    import shutil
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    out_dir = os.path.join(ROOT, "_build")
+    os.makedirs(out_dir, exist_ok=True)
+    exe = os.path.join(out_dir, "bench_rates")
+    subprocess.run([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-o", exe,
+                    os.path.join(ROOT, "bench_rates.cu")], check=True)
+    r = subprocess.run([exe], capture_output=True, text=True, check=True)
+    print(r.stdout.strip(), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -704,7 +742,12 @@ def main():
     ap.add_argument("--B", type=int, default=0, help="with --profile: batch size instead of 16")
     ap.add_argument("--T", type=int, default=0, help="with --profile: sequence length instead of 2048")
     ap.add_argument("--decode", action="store_true", help="with --profile: 4 decode steps instead of fwd+bwd")
+    ap.add_argument("--rates", action="store_true",
+                    help="measure the per-SM unit rates the roofline uses (bench_rates.cu) and exit")
     args = ap.parse_args()
+    if args.rates:
+        run_rates()
+        return
     if args.profile:
         run_profile_case(args)
         return
