@@ -156,6 +156,7 @@ def _workspace(nbytes, device):
 
 SSM_SCAN_DELTA_SOFTPLUS = 2
 SSM_SCAN_LOOKBACK = 4
+SSM_SCAN_STEP_INPUTS_READY = 8
 SSM_ERR_TIMEOUT = 6
 
 _last_lookback = {}     # device -> (desc, workspace) of the last forward call with lookback=True
@@ -313,10 +314,11 @@ def ssm_scan_fwd_noalloc(x, delta, A, b, c, h0=None, *, ckpt_interval=0, chunk_l
     return y, hT, ckpt
 
 
-def ssm_scan_step(x, delta, A, b, c, h, *, y=None, delta_softplus=False, stream=None):
+def ssm_scan_step(x, delta, A, b, c, h, *, y=None, delta_softplus=False, inputs_ready=False, stream=None):
     """One decode step through ssm_scan_step: x, delta (B, D), b, c (B, DS) in the I/O
     dtype, A (D, DS) and the state h (B, D, DS) float32, which is updated in place.
-    Returns y (B, D)."""
+    inputs_ready=True sets SSM_SCAN_STEP_INPUTS_READY (the kernel before this one on the
+    stream writes none of x, delta, A, b, c). Returns y (B, D)."""
     torch = _torch()
     L = lib()
     fn = L.ssm_scan_step
@@ -329,7 +331,8 @@ def ssm_scan_step(x, delta, A, b, c, h, *, y=None, delta_softplus=False, stream=
                                 (b, (B, DS), x.dtype, "b"), (c, (B, DS), x.dtype, "c"),
                                 (h, (B, D, DS), torch.float32, "h")):
         _check(t_, shape, dt, name, dev)
-    desc = make_desc(B, 1, D, DS, _io_of(x), 0, 0, SSM_SCAN_DELTA_SOFTPLUS if delta_softplus else 0)
+    flags = (SSM_SCAN_DELTA_SOFTPLUS if delta_softplus else 0) | (SSM_SCAN_STEP_INPUTS_READY if inputs_ready else 0)
+    desc = make_desc(B, 1, D, DS, _io_of(x), 0, 0, flags)
     if y is None:
         y = torch.empty((B, D), dtype=x.dtype, device=dev)
     st = _call(dev, fn, ctypes.byref(desc), _ptr(x), _ptr(delta), _ptr(A), _ptr(b), _ptr(c), _ptr(h), _ptr(y), _stream(stream, dev))
@@ -387,5 +390,6 @@ _ScanFn = _Lazy()
 
 __all__ = ["lib", "ssm_scan_desc", "make_desc", "ssm_scan_fwd", "ssm_scan_bwd", "ssm_scan_step",
            "ssm_scan_fwd_noalloc", "selective_scan", "SSMError", "EXPORTS", "LIB_PATH", "SSM_IO_F32", "SSM_IO_BF16",
-           "SSM_SCAN_DETERMINISTIC", "SSM_SCAN_DELTA_SOFTPLUS", "SSM_SCAN_LOOKBACK", "SSM_ERR_TIMEOUT",
+           "SSM_SCAN_DETERMINISTIC", "SSM_SCAN_DELTA_SOFTPLUS", "SSM_SCAN_LOOKBACK", "SSM_SCAN_STEP_INPUTS_READY",
+           "SSM_ERR_TIMEOUT",
            "lookback_status", "testing_library", "TESTING_LIB_PATH"]

@@ -10,10 +10,18 @@
 // What the second channel buys, per element: the b and c values a lane reads
 // from shared memory serve 8 chains instead of 4; the per-step sums over d of
 // gb and gc first add the lane's two channels in registers, so the lane
-// reduce-scatter (shuffles and selects; two stages here, into per-half-warp
-// slots that the per-tile flush adds) is paid once per 8 elements instead of
-// once per 4; the (delta, delta*x) pair of both channels arrives in one 16-byte
-// shared load. The instruction count per element drops by about a quarter.
+// reduce-scatter (two shuffle stages here, into per-half-warp slots that the
+// per-tile flush adds) is paid once per 8 elements instead of once per 4; the
+// (delta, delta*x) pair of both channels arrives in one 16-byte shared load.
+//
+// The reduce-scatter needs no selects: a lane keeps its 4 states in a
+// lane-dependent order (register slot j holds state s0 + (j ^ m), with
+// m = bits 1-2 of the lane's channel-pair index), chosen so that at each of the
+// two stages every lane keeps the same register slots and sends the others,
+// and its partner's sent slots hold exactly the states it kept. The b and c
+// rows are kept in shared memory in all four orders, so the per-step loads are
+// unchanged; only values loaded or stored once per chunk or per CTA (A, the
+// checkpoints, ghT, gh0, gA) are permuted in registers.
 //
 // Where the extra per-thread state goes: the level-2 sub-checkpoints (the
 // state entering every 16th step of the chunk, 8 floats per thread per
@@ -54,8 +62,11 @@ struct Bwd2Cfg {
     static constexpr size_t RAW_BC = size_t(LS) * kDS * sizeof(TIO);        // one of b, c
     static constexpr size_t CONV1 = size_t(LS) * NP * 16;                   // (d0, d0*x0, d1, d1*x1)
     static constexpr size_t CONV2 = size_t(LS) * NP * 16;                   // (dy0, dy1, x0, x1)
-    static constexpr size_t BCF = size_t(LS) * kDS * 4;                     // one of b, c as float32
-    static constexpr size_t GBC = size_t(2 * NW) * LS * 2 * kDS * 4;        // per-half-warp gb, gc sums of a tile
+    static constexpr size_t BCF = size_t(4) * LS * kDS * 4;                 // one of b, c as float32, 4 state orders
+    // per-half-warp gb, gc sums of a tile, [2 NW][LS][2][16] floats; sets padded by 16 floats so
+    // the two sets a warp writes at once fall on different banks
+    static constexpr int GSET = LS * 2 * kDS + 16;
+    static constexpr size_t GBC = size_t(2 * NW) * GSET * 4;
     static constexpr size_t SMEM = 3 * RAW_X + 2 * RAW_BC + CONV1 + CONV2 + 2 * BCF + GBC + 16;
     // tensor memory columns per lane: h of both channels per step
     static constexpr uint32_t TMEM_H_STEP = KD * KS;                        // 8
@@ -65,6 +76,13 @@ struct Bwd2Cfg {
     static_assert(3 * TMEM_COLS <= 512, "three resident CTAs must fit in tensor memory");
 };
 
+
+// The lane's 4 states of one channel between state order (s0 .. s0 + 3) and its register-slot
+// order (slot j = state s0 + (j ^ m)); the map is its own inverse.
+__device__ __forceinline__ float4 perm4(float4 v, int m) {
+    float4 r = (m & 2) ? make_float4(v.z, v.w, v.x, v.y) : v;
+    return (m & 1) ? make_float4(r.y, r.x, r.w, r.z) : r;
+}
 
 template <typename TIO, bool VEC, bool FUSE>
 __global__ void __launch_bounds__(128, 3) bwd2_kernel(const BwdLaunch p) {
@@ -82,9 +100,9 @@ __global__ void __launch_bounds__(128, 3) bwd2_kernel(const BwdLaunch p) {
     TIO* cr = reinterpret_cast<TIO*>(ptr);  ptr += C::RAW_BC;
     float4* conv1 = reinterpret_cast<float4*>(ptr); ptr += C::CONV1;   // [LS][NP]
     float4* conv2 = reinterpret_cast<float4*>(ptr); ptr += C::CONV2;   // [LS][NP]
-    float* bf = reinterpret_cast<float*>(ptr);      ptr += C::BCF;     // [LS][16]
-    float* cf = reinterpret_cast<float*>(ptr);      ptr += C::BCF;
-    float* gbc = reinterpret_cast<float*>(ptr);     ptr += C::GBC;     // [2 NW][LS][2][16]
+    float* bfp = reinterpret_cast<float*>(ptr);     ptr += C::BCF;     // [4 orders][LS][16]
+    float* cfp = reinterpret_cast<float*>(ptr);     ptr += C::BCF;
+    float* gbc = reinterpret_cast<float*>(ptr);     ptr += C::GBC;     // [2 NW][GSET]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ptr);
 
     const int tid = threadIdx.x;
@@ -93,6 +111,10 @@ __global__ void __launch_bounds__(128, 3) bwd2_kernel(const BwdLaunch p) {
     const int sg = lane & 3;                // state group within the pair
     const int pc = warp * 8 + cw;           // channel pair within the CTA
     const int s0 = sg * KS;
+    const int m = (cw >> 1) & 3;            // register slot j holds state s0 + (j ^ m)
+    // b and c rows in this lane's state order
+    const float* bf = bfp + m * LS * kDS;
+    const float* cf = cfp + m * LS * kDS;
     const int64_t T = p.T, D = p.D, K = p.K;
     const int64_t b = blockIdx.y;
     const int64_t d0 = int64_t(blockIdx.x) * DT;
@@ -120,8 +142,8 @@ __global__ void __launch_bounds__(128, 3) bwd2_kernel(const BwdLaunch p) {
     for (int k = 0; k < 2; ++k) {
         float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f), g4 = a4;
         if (valid[k]) {
-            a4 = *reinterpret_cast<const float4*>(p.A + dch[k] * kDS + s0);
-            if (p.ghT != nullptr) g4 = *reinterpret_cast<const float4*>(p.ghT + (b * D + dch[k]) * kDS + s0);
+            a4 = perm4(*reinterpret_cast<const float4*>(p.A + dch[k] * kDS + s0), m);
+            if (p.ghT != nullptr) g4 = perm4(*reinterpret_cast<const float4*>(p.ghT + (b * D + dch[k]) * kDS + s0), m);
         }
         A2[k][0] = make_float2(a4.x * kLog2e, a4.y * kLog2e);
         A2[k][1] = make_float2(a4.z * kLog2e, a4.w * kLog2e);
@@ -195,20 +217,35 @@ __global__ void __launch_bounds__(128, 3) bwd2_kernel(const BwdLaunch p) {
                 conv2[i] = make_float4(dyv[0], dyv[1], xv[0], xv[1]);
             }
         }
+        // b (threads 0-63) and c (threads 64-127): 4 states of one row each, stored in the four
+        // state orders (order mm holds state s ^ mm at position s)
+        {
+            const int q = tid & 63, r = q >> 2, g = (q & 3) * 4;
+            if (tid < 64 || rev) {
+                const TIO* raw = tid < 64 ? br : cr;
+                float* dst = tid < 64 ? bfp : cfp;
+                float v[4];
+                load_vals<TIO, 4>(raw + r * kDS + g, v);
 #pragma unroll
-        for (int q = 0; q < LS * kDS / NT; ++q) {
-            const int i = tid + NT * q;
-            bf[i] = to_f32(br[i]);
-            if (rev) cf[i] = to_f32(cr[i]);
+                for (int mm = 0; mm < 4; ++mm)
+                    *reinterpret_cast<float4*>(dst + mm * LS * kDS + r * kDS + g) =
+                        make_float4(v[0 ^ mm], v[1 ^ mm], v[2 ^ mm], v[3 ^ mm]);
+            }
         }
     };
     // gb, gc of the tile starting at t0: sum the warps' slots, add to global (rows below t_lim)
     auto flush_gbc = [&](int64_t t0, int64_t t_lim) {
         const int r = tid >> 3, tau = (tid >> 2) & 1, q = tid & 3;
         const int off = r * 2 * kDS + tau * kDS + q * 4;
-        float4 v = *reinterpret_cast<const float4*>(gbc + off);
+        float4 v4 = *reinterpret_cast<const float4*>(gbc + off);
+        float2 lo = make_float2(v4.x, v4.y), hi = make_float2(v4.z, v4.w);
 #pragma unroll
-        for (int w = 1; w < 2 * C::NW; ++w) v = v + *reinterpret_cast<const float4*>(gbc + w * LS * 2 * kDS + off);
+        for (int w = 1; w < 2 * C::NW; ++w) {
+            const float4 u = *reinterpret_cast<const float4*>(gbc + w * C::GSET + off);
+            lo = __fadd2_rn(lo, make_float2(u.x, u.y));
+            hi = __fadd2_rn(hi, make_float2(u.z, u.w));
+        }
+        const float4 v = make_float4(lo.x, lo.y, hi.x, hi.y);
         if (t0 + r < t_lim) {
             if (p.det) {
                 *reinterpret_cast<float4*>(p.part_gbc + ((int64_t(blockIdx.x) * p.B + b) * T + t0 + r) * (2 * kDS) +
@@ -232,7 +269,7 @@ __global__ void __launch_bounds__(128, 3) bwd2_kernel(const BwdLaunch p) {
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
             float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (valid[k]) v = *reinterpret_cast<const float4*>(p.ckpt + ((j * p.B + b) * D + dch[k]) * kDS + s0);
+            if (valid[k]) v = perm4(*reinterpret_cast<const float4*>(p.ckpt + ((j * p.B + b) * D + dch[k]) * kDS + s0), m);
             h[k][0] = v.x; h[k][1] = v.y; h[k][2] = v.z; h[k][3] = v.w;
         }
         float hlast[2 * KS];                 // start state of the chunk's last sub-chunk
@@ -346,8 +383,9 @@ __global__ void __launch_bounds__(128, 3) bwd2_kernel(const BwdLaunch p) {
                 tmem_wait_st();
             }
 
-            // this lane's slot set: sums over the 4 channel pairs {cw, cw^2, cw^4, cw^6} of its warp
-            float* gw = gbc + (warp * 2 + (cw & 1)) * LS * 2 * kDS;
+            // this lane's slot set: sums over the 4 channel pairs {cw, cw^2, cw^4, cw^6} of its warp;
+            // the lane ends with the sums of state s0 + m
+            float* gw = gbc + (warp * 2 + (cw & 1)) * C::GSET + s0 + m;
             // reverse sweep over the sub-chunk, 4 steps per lane reduce-scatter group
 #pragma unroll 2
             for (int rg = LS - 4; rg >= 0; rg -= 4) {
@@ -402,21 +440,31 @@ __global__ void __launch_bounds__(128, 3) bwd2_kernel(const BwdLaunch p) {
                         rr[k][jj] = racc.x + racc.y;
                         qq[k][jj] = qacc.x + qacc.y;
                     }
-                    const float part[8] = {pgb[0].x, pgb[0].y, pgb[1].x, pgb[1].y,
-                                           pgc[0].x, pgc[0].y, pgc[1].x, pgc[1].y};
-                    // sum over the warp's 8 channel pairs; this lane keeps entry (cw >> 2, cw & 3)
-                    {   // sum over 4 of the warp's 8 channel pairs; this lane keeps entries 2 (cw>>1) + {0, 1}
-                        const int e0 = 2 * (cw >> 1);
-                        const float2 v2 = warp_reduce_scatter8_half(part, lane);
-                        *reinterpret_cast<float2*>(gw + r * 2 * kDS + (e0 >> 2) * kDS + s0 + (e0 & 3)) = v2;
+                    // Sum over the channel pairs {cw, cw^4} (lane ^ 16) and then {cw, cw^2} (lane ^ 8):
+                    // every lane keeps slots 0, 1 and sends 2, 3, then keeps slot 0 and sends 1; the
+                    // partner's sent slots hold the states this lane kept (its m differs in bit 1,
+                    // then in bit 0), so no selects are needed.
+                    {
+                        const float2 rb = make_float2(__shfl_xor_sync(0xffffffffu, pgb[1].x, 16),
+                                                      __shfl_xor_sync(0xffffffffu, pgb[1].y, 16));
+                        const float2 rc = make_float2(__shfl_xor_sync(0xffffffffu, pgc[1].x, 16),
+                                                      __shfl_xor_sync(0xffffffffu, pgc[1].y, 16));
+                        const float2 sb = __fadd2_rn(pgb[0], rb);      // slots 0, 1 of gb
+                        const float2 sc = __fadd2_rn(pgc[0], rc);      // slots 0, 1 of gc
+                        const float2 r2 = make_float2(__shfl_xor_sync(0xffffffffu, sb.y, 8),
+                                                      __shfl_xor_sync(0xffffffffu, sc.y, 8));
+                        const float2 v2 = __fadd2_rn(make_float2(sb.x, sc.x), r2);
+                        gw[r * 2 * kDS] = v2.x;                        // gb of state s0 + m
+                        gw[r * 2 * kDS + kDS] = v2.y;                  // gc
                     }
                 }
                 // sums over the pair's 4 lanes: this lane takes step rg + sg of both channels
                 float rs[2], qs[2];
 #pragma unroll
                 for (int k = 0; k < 2; ++k) {
-                    rs[k] = reduce_scatter_steps<4>(rr[k], sg);
-                    qs[k] = reduce_scatter_steps<4>(qq[k], sg);
+                    const float2 rq = reduce_scatter_steps4_pair(rr[k], qq[k], sg);
+                    rs[k] = rq.x;
+                    qs[k] = rq.y;
                 }
                 const int r = rg + sg;
                 const float4 v = conv1[r * NP + pc];
@@ -472,12 +520,12 @@ __global__ void __launch_bounds__(128, 3) bwd2_kernel(const BwdLaunch p) {
     for (int k = 0; k < 2; ++k) {
         if (!valid[k]) continue;
         *reinterpret_cast<float4*>(p.gh0 + (b * D + dch[k]) * kDS + s0) =
-            make_float4(gcar[k][0].x, gcar[k][0].y, gcar[k][1].x, gcar[k][1].y);
+            perm4(make_float4(gcar[k][0].x, gcar[k][0].y, gcar[k][1].x, gcar[k][1].y), m);
+        const float4 ga = perm4(make_float4(gAacc[k][0].x, gAacc[k][0].y, gAacc[k][1].x, gAacc[k][1].y), m);
         if (p.det) {
-            *reinterpret_cast<float4*>(p.part_gA + (b * D + dch[k]) * kDS + s0) =
-                make_float4(gAacc[k][0].x, gAacc[k][0].y, gAacc[k][1].x, gAacc[k][1].y);
+            *reinterpret_cast<float4*>(p.part_gA + (b * D + dch[k]) * kDS + s0) = ga;
         } else {
-            red_add_v4(p.gA + dch[k] * kDS + s0, gAacc[k][0].x, gAacc[k][0].y, gAacc[k][1].x, gAacc[k][1].y);
+            red_add_v4(p.gA + dch[k] * kDS + s0, ga.x, ga.y, ga.z, ga.w);
         }
     }
 }

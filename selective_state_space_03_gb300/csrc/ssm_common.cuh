@@ -220,6 +220,25 @@ __device__ __forceinline__ float reduce_scatter_steps(const float (&v)[G], int g
     }
 }
 
+// reduce_scatter_steps<4> of two arrays at once (lane gl returns the step-gl totals of both as
+// one float2); the additions run as packed f32x2 operations.
+__device__ __forceinline__ float2 reduce_scatter_steps4_pair(const float (&a)[4], const float (&b)[4], int gl) {
+    const bool hi2 = gl & 2;
+    float2 q[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const float sa = hi2 ? a[i] : a[i + 2], sb = hi2 ? b[i] : b[i + 2];
+        const float ka = hi2 ? a[i + 2] : a[i], kb = hi2 ? b[i + 2] : b[i];
+        q[i] = __fadd2_rn(make_float2(ka, kb), make_float2(__shfl_xor_sync(0xffffffffu, sa, 2),
+                                                           __shfl_xor_sync(0xffffffffu, sb, 2)));
+    }
+    const bool hi1 = gl & 1;
+    const float2 send = hi1 ? q[0] : q[1];
+    const float2 keep = hi1 ? q[1] : q[0];
+    return __fadd2_rn(keep, make_float2(__shfl_xor_sync(0xffffffffu, send.x, 1),
+                                        __shfl_xor_sync(0xffffffffu, send.y, 1)));
+}
+
 // Eight values per lane summed over the 4 lanes of a group (gl = lane & 3): lane gl
 // returns the totals of entries 2 gl and 2 gl + 1 (two reduce-scatter stages).
 __device__ __forceinline__ float2 reduce_scatter8_over4(const float (&v)[8], int gl) {

@@ -33,6 +33,7 @@ struct StepLaunch {
     void* y;             // (B, D) io
     int64_t B, D;
     bool softplus;       // delta holds raw values
+    bool inputs_ready;   // the preceding kernel writes none of x, delta, A, b, c
 };
 
 // 8 consecutive I/O values as float32 (16-byte aligned)
@@ -52,6 +53,19 @@ __device__ __forceinline__ void load8(const TIO* p, float (&v)[8]) {
     }
 }
 
+// This step's x, delta (through softplus when asked), b, c and A.
+template <typename TIO>
+__device__ __forceinline__ void load_step_inputs(const StepLaunch& p, int64_t chain, int s0, float& dl, float& dx,
+                                                 float (&bv)[8], float (&cv)[8], float (&av)[8]) {
+    const int64_t bb = chain / p.D, d = chain - bb * p.D;
+    dl = to_f32(static_cast<const TIO*>(p.delta)[chain]);
+    if (p.softplus) dl = softplus_f32(dl);
+    dx = dl * to_f32(static_cast<const TIO*>(p.x)[chain]);
+    load8<TIO>(static_cast<const TIO*>(p.b) + bb * kDS + s0, bv);
+    load8<TIO>(static_cast<const TIO*>(p.c) + bb * kDS + s0, cv);
+    load8<float>(p.A + d * kDS + s0, av);
+}
+
 template <typename TIO>
 __global__ void __launch_bounds__(128) step_kernel(const StepLaunch p) {
     const int64_t gid = int64_t(blockIdx.x) * 128 + threadIdx.x;
@@ -61,23 +75,18 @@ __global__ void __launch_bounds__(128) step_kernel(const StepLaunch p) {
     // Consecutive steps on a stream are launched as programmatic dependents: let the next
     // step's CTAs be scheduled now; they run up to their wait below while this grid finishes.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    // Every input may have been written by the kernel before this one on the stream (the
-    // previous step writes h and y; a projection kernel may write x, delta, b, c, even one
-    // that lets its dependents launch before its own stores): wait until that grid has
-    // completed and its writes are visible before loading anything (returns at once when
-    // there is no such grid).
-    asm volatile("griddepcontrol.wait;" ::: "memory");
     float acc = 0.f;
     float hv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     float dl = 0.f, dx = 0.f, bv[8], cv[8], av[8];
+    // Inputs the caller declared untouched by the preceding kernel load while it finishes.
+    if (p.inputs_ready && valid) load_step_inputs<TIO>(p, chain, s0, dl, dx, bv, cv, av);
+    // Otherwise every input may have been written by the kernel before this one on the stream
+    // (the previous step writes h and y; a projection kernel may write x, delta, b, c, even one
+    // that lets its dependents launch before its own stores): wait until that grid has
+    // completed and its writes are visible (returns at once when there is no such grid).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (valid) {
-        const int64_t bb = chain / p.D, d = chain - bb * p.D;
-        dl = to_f32(static_cast<const TIO*>(p.delta)[chain]);
-        if (p.softplus) dl = softplus_f32(dl);
-        dx = dl * to_f32(static_cast<const TIO*>(p.x)[chain]);
-        load8<TIO>(static_cast<const TIO*>(p.b) + bb * kDS + s0, bv);
-        load8<TIO>(static_cast<const TIO*>(p.c) + bb * kDS + s0, cv);
-        load8<float>(p.A + d * kDS + s0, av);
+        if (!p.inputs_ready) load_step_inputs<TIO>(p, chain, s0, dl, dx, bv, cv, av);
         load8<float>(p.h + chain * kDS + s0, hv);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -106,7 +115,7 @@ extern "C" ssm_status ssm_scan_step(const ssm_scan_desc* desc, const void* x, co
     const ssm_scan_desc& d = *desc;
     if (d.B < 0 || d.D < 0 || d.DS < 0 || d.T != 1) return SSM_ERR_INVALID_ARG;
     if (d.io != SSM_IO_F32 && d.io != SSM_IO_BF16) return SSM_ERR_INVALID_ARG;
-    if (d.ckpt_interval < 0 || (d.flags & ~(SSM_SCAN_DETERMINISTIC | SSM_SCAN_DELTA_SOFTPLUS | SSM_SCAN_LOOKBACK)) != 0 || d.B > 65535) return SSM_ERR_INVALID_ARG;
+    if (d.ckpt_interval < 0 || (d.flags & ~(SSM_SCAN_DETERMINISTIC | SSM_SCAN_DELTA_SOFTPLUS | SSM_SCAN_LOOKBACK | SSM_SCAN_STEP_INPUTS_READY)) != 0 || d.B > 65535) return SSM_ERR_INVALID_ARG;
     if (d.DS != kDS || d.D > kMaxD) return SSM_ERR_UNSUPPORTED;
     if (d.B == 0 || d.D == 0) return SSM_OK;
     if (!x || !delta || !A || !b || !c || !h || !y) return SSM_ERR_INVALID_ARG;
@@ -122,7 +131,8 @@ extern "C" ssm_status ssm_scan_step(const ssm_scan_desc* desc, const void* x, co
     const int64_t threads = d.B * d.D * 2;
     const int64_t blocks = (threads + 127) / 128;
     if (blocks > int64_t(0x7fffffff)) return SSM_ERR_UNSUPPORTED;
-    StepLaunch L{x, delta, A, b, c, h, y, d.B, d.D, (d.flags & SSM_SCAN_DELTA_SOFTPLUS) != 0};
+    StepLaunch L{x, delta, A, b, c, h, y, d.B, d.D, (d.flags & SSM_SCAN_DELTA_SOFTPLUS) != 0,
+                 (d.flags & SSM_SCAN_STEP_INPUTS_READY) != 0};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(blocks));
     cfg.blockDim = dim3(128);

@@ -86,7 +86,7 @@ def test_invalid_descriptors(L):
     assert fwd(L, desc(ckpt_interval=-1)) == 1
     assert fwd(L, desc(B=70000)) == 1
     d = desc()
-    d.flags = 8
+    d.flags = 16            # the first bit no entry point defines
     assert fwd(L, d) == 1
     assert fwd(L, desc(DS=8)) == 2
     assert fwd(L, desc(DS=32)) == 2
@@ -175,8 +175,8 @@ def test_deterministic_flag_workspace(L):
     # without the flag the same shape needs no workspace
     assert L.ssm_scan_bwd_ckpt_workspace_bytes(ctypes.byref(desc(B=2, T=100, D=320, ckpt_interval=100))) == 0
     # unknown flag bits are rejected
-    assert bwd(L, desc(flags=8)) == 1
-    assert step(L, desc(T=1, flags=8)) == 1
+    assert bwd(L, desc(flags=16)) == 1
+    assert step(L, desc(T=1, flags=16)) == 1
 
 
 def test_fused_entry_point_checks(L):
@@ -196,7 +196,7 @@ def test_fused_entry_point_checks(L):
     assert fwdf(y=None) == 1
     assert bwdf(gD=None) == 1                            # the skip weights' gradient is required
     assert bwdf(gD=FAKE + 8) == 3
-    assert bwdf(dd=desc(flags=8)) == 1
+    assert bwdf(dd=desc(flags=16)) == 1
 
 
 def test_lookback_flag_workspace_and_status(L):

@@ -52,8 +52,13 @@ def test_config_names_the_workload_by_its_shape():
     assert "model" not in c
 
 
-def test_work_constants_match_the_schedules():
-    # forward: one exp per element; backward: two recompute levels and the reverse sweep
+def test_work_constants_match_the_method():
+    # algorithmic counts: forward one exp per element; backward one recompute of the state from
+    # its checkpoint and the decay again in the reverse sweep (the kernel executes a third for
+    # its second recompute level, reported separately)
     assert bench.FWD_EX2_PER_ELEM == 1
-    assert bench.BWD_EX2_PER_ELEM == 3
+    assert bench.BWD_EX2_PER_ELEM == 2
+    assert bench.BWD_EX2_EXECUTED_PER_ELEM == 3
     assert bench.BWD_OPS_PER_ELEM == 12
+    # the measured per-SM rates the peaks use (bench.py --rates on a GB300: 31.98 ex2, 125.2 FFMA)
+    assert bench.EX2_PER_SM_CLK == 32 and bench.FP32_PER_SM_CLK == 128

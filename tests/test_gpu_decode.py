@@ -127,3 +127,20 @@ def test_step_after_a_kernel_that_writes_its_inputs(io):
     ref = oracle.fwd(inp["x"], inp["delta"], inp["A"], inp["b"], inp["c"], inp["h0"])
     assert_close(np.stack([to_host(v) for v in ys], 1), ref["y"], io, "fwd", "y")
     assert_close(to_host(h), ref["hT"], io, "fwd", "h")
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_steps_with_inputs_declared_ready(io):
+    # every step's inputs are computed before the first step is launched, so each step may load
+    # them while the step before it finishes (SSM_SCAN_STEP_INPUTS_READY); only h waits
+    import torch
+    w = gen.workload(5, B=3, T=10, D=768, io=io, h0_std=0.3)
+    inp = gen.make_inputs(w, seed=11, with_grad_inputs=False)
+    t = dev_inputs(inp)
+    steps = [tuple(t[k][:, i].contiguous() for k in ("x", "delta", "b", "c")) for i in range(w.T)]
+    h = t["h0"].clone()
+    ys = [ssm().ssm_scan_step(xk, dk, t["A"], bk, ck, h, inputs_ready=True) for xk, dk, bk, ck in steps]
+    torch.cuda.synchronize()
+    ref = oracle.fwd(inp["x"], inp["delta"], inp["A"], inp["b"], inp["c"], inp["h0"])
+    assert_close(np.stack([to_host(v) for v in ys], 1), ref["y"], io, "fwd", "y")
+    assert_close(to_host(h), ref["hT"], io, "fwd", "h")
