@@ -81,7 +81,7 @@ typedef struct {
                                two-pass scan with chunks of this many steps; < 0 = one
                                pass over T. Every schedule computes the same function. */
     int32_t flags;          /* SSM_SCAN_DETERMINISTIC | SSM_SCAN_DELTA_SOFTPLUS |
-                               SSM_SCAN_LOOKBACK or 0;
+                               SSM_SCAN_LOOKBACK | SSM_SCAN_STEP_INPUTS_READY or 0;
                                other bits must be 0 */
 } ssm_scan_desc;
 
@@ -117,18 +117,32 @@ typedef struct {
  * backward, ssm_scan_fwd_noalloc and ssm_scan_step ignore the flag. */
 #define SSM_SCAN_LOOKBACK 4
 
-/* Bytes of the checkpoint buffer: ceil(T/K)*B*D*DS*4, 0 when K == 0. */
+/* ssm_scan_desc.flags, ssm_scan_step only: the caller promises that the kernel
+ * launched before this step on the stream writes none of x, delta, A, b, c
+ * (for example another session's step, all sessions' inputs having been
+ * computed earlier). The step then loads those five while that kernel is still
+ * running and waits for it only before reading h. Without the flag every load
+ * waits. Every other entry point ignores the flag. */
+#define SSM_SCAN_STEP_INPUTS_READY 8
+
+/* Bytes of the checkpoint buffer: ceil(T/K)*B*D*DS*4, 0 when K == 0.
+ * Defined by: the chunk-boundary retention of the ruDNN page ("src/kda/chunk.rs",
+ * `chunk_kda` with retained boundaries): one state per chunk of K steps, slot j
+ * the state entering step j*K. */
 size_t ssm_scan_ckpt_bytes(const ssm_scan_desc* desc);
 
 /* Bytes of device scratch memory ssm_scan_fwd needs for this desc (0 when the
  * schedule needs none). The workspace holds the chunked scan's per-chunk
  * decay sums and partial states; with SSM_SCAN_LOOKBACK, every chunk's map,
- * end state and publication flag. */
+ * end state and publication flag. Defined by: the state carried across chunks
+ * of the sequence (pssa page, "pssa_kernels.py", module docstring: h0 in, hT
+ * out; ruDNN `chunk_kda`, the state carried from chunk to chunk). */
 size_t ssm_scan_fwd_workspace_bytes(const ssm_scan_desc* desc);
 
 /* Bytes of device scratch memory ssm_scan_bwd needs for this desc when it is
  * called with ckpt == NULL: what ssm_scan_bwd_ckpt_workspace_bytes counts plus
- * the checkpoints it rebuilds. */
+ * the checkpoints it rebuilds (the ruDNN page's `chunk_kda_backward` needs the
+ * retained chunk boundaries; without them they are recomputed first). */
 size_t ssm_scan_bwd_workspace_bytes(const ssm_scan_desc* desc);
 
 /* Bytes of device scratch memory for a backward call with the forward's
@@ -148,6 +162,10 @@ size_t ssm_scan_bwd_workspace_bytes(const ssm_scan_desc* desc);
 size_t ssm_scan_bwd_ckpt_workspace_bytes(const ssm_scan_desc* desc);
 
 /* Forward scan: y, hT and (if K > 0 and ckpt != NULL) the checkpoints.
+ * Defined by: the pssa page ("pssa_kernels.py"), `scan_reference` (the plain
+ * loop: decay, injection, readout of the updated state) and `scan_fwd` (the
+ * same recurrence with y and the final state stored); checkpoints as in
+ * ssm_scan_ckpt_bytes.
  *   h0    may be NULL (zero initial state)
  *   hT    may be NULL (not written)
  *   ckpt  may be NULL (not written); ignored when K == 0
@@ -161,7 +179,10 @@ ssm_status ssm_scan_fwd(const ssm_scan_desc* desc,
                         void* y, float* hT, float* ckpt,
                         void* workspace, size_t workspace_bytes, void* stream);
 
-/* After a forward call with SSM_SCAN_LOOKBACK whose schedule was chunked:
+/* After a forward call with SSM_SCAN_LOOKBACK whose schedule was chunked
+ * (the single-pass prefix scan with decoupled look-back of Merrill and Garland,
+ * 2016, applied to the chunk maps; the pages have no counterpart of the status
+ * query):
  * waits for `stream` (cudaStreamSynchronize) and reads the count of look-back
  * waits that ran out from `workspace` (the same workspace and desc as that
  * call). SSM_OK when none ran out, or when desc's schedule is not the
@@ -174,6 +195,12 @@ ssm_status ssm_scan_fwd_lookback_status(const ssm_scan_desc* desc, const void* w
 
 /* Backward scan: gx, gdelta, gA, gb, gc, gh0 (all float32) for
  * L = sum dy*y + sum ghT*hT.
+ * Defined by: the pssa page, `scan_bwd` (the reverse sweep: adjoint carried
+ * with the next step's decay, the per-step gradient terms, gb/gc/gA summed over
+ * chains, gh0 = a_0 g_0) and `ScanFn` (inputs and outputs of the autograd
+ * function; hT not differentiated there, ghT = NULL here); the states are
+ * rematerialised from the checkpoints as the ruDNN page's `chunk_kda_backward`
+ * rematerialises each chunk from its retained boundary state.
  *   ckpt  the checkpoints the forward wrote with the same desc (K > 0), or
  *         NULL: the backward then rebuilds them from h0 in the workspace
  *   h0    may be NULL (zero initial state); used only when ckpt is NULL
@@ -192,7 +219,9 @@ ssm_status ssm_scan_bwd(const ssm_scan_desc* desc,
                         float* gh0,
                         void* workspace, size_t workspace_bytes, void* stream);
 
-/* The forward with the trace page's skip connection fused into its readout:
+/* Defined by: the POPCORNBENCH trace page ("FW-GLM-5-1__l2_p30"), its model's
+ * forward() op list and kernel (softplus on delta, y + x * D after the scan).
+ * The forward with the trace page's skip connection fused into its readout:
  * y[b,t,d] = <h_t, c_t> + D_skip[d] * x[b,t,d] (its forward() op list, and the
  * skip its kernel adds before storing y). D_skip is (D) float32 or NULL (no
  * skip: then this is ssm_scan_fwd). Everything else as ssm_scan_fwd, including
@@ -203,7 +232,9 @@ ssm_status ssm_scan_fwd_fused(const ssm_scan_desc* desc,
                               void* y, float* hT, float* ckpt,
                               void* workspace, size_t workspace_bytes, void* stream);
 
-/* The backward of ssm_scan_fwd_fused with the same D_skip: gx gets
+/* Defined by: the chain rule through the trace page's skip and softplus (see
+ * ssm_scan_fwd_fused) around the pssa page's `scan_bwd`.
+ * The backward of ssm_scan_fwd_fused with the same D_skip: gx gets
  * + dy * D_skip[d] and gD_skip[d] = sum_{b,t} dy[b,t,d] * x[b,t,d] ((D)
  * float32, required when D_skip is not NULL; accumulated with atomic adds, or
  * in a fixed order under SSM_SCAN_DETERMINISTIC). Everything else as
@@ -247,7 +278,10 @@ ssm_status ssm_scan_fwd_noalloc(const ssm_scan_desc* desc,
                                 const void* b, const void* c, const float* h0,
                                 void* y, float* hT, float* ckpt, void* stream);
 
-/* One step of the scan for every (b, d) chain, the state updated in place:
+/* Defined by: the pssa page's `scan_reference` over one step (T = 1) with the
+ * state carried between calls, as the ruDNN page's fused recurrent decode
+ * (`chunk_kda` with one token) advances its state one token per call.
+ * One step of the scan for every (b, d) chain, the state updated in place:
  * the decode form of the recurrence (one token per call, the state carried
  * between calls, as the ruDNN page's fused recurrent decode does for KDA).
  *     h[b,d,s] <- exp(delta[b,d] A[d,s]) h[b,d,s] + delta[b,d] b[b,s] x[b,d]
@@ -266,12 +300,14 @@ ssm_status ssm_scan_fwd_noalloc(const ssm_scan_desc* desc,
  * stream: a step's CTAs may be scheduled while that kernel finishes, but every
  * load waits until it has completed and its writes are visible, so any input
  * may be the output of the preceding kernel (a projection, or the previous
- * step's h and y). */
+ * step's h and y). With SSM_SCAN_STEP_INPUTS_READY in desc->flags only the load
+ * of h waits (see there). */
 ssm_status ssm_scan_step(const ssm_scan_desc* desc,
                          const void* x, const void* delta, const float* A,
                          const void* b, const void* c, float* h, void* y, void* stream);
 
-/* Static description of a status code. */
+/* Static description of a status code (the error results of the ruDNN page's
+ * `validate` / `KdaError`, as C status codes). */
 const char* ssm_status_str(ssm_status status);
 
 #ifdef __cplusplus
