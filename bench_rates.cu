@@ -8,8 +8,12 @@
 //   ffma2    packed f32x2 fused multiply-add (one instruction, two lanes' worth);
 //   mix      one ex2 and four FFMA per element (the forward's arithmetic);
 //   shfl     warp shuffles (the lane reductions);
-//   lds128   16-byte shared-memory loads that four lanes of eight share (the
-//            b/c broadcast loads of the kernels), counted as loads per clock;
+//   lds      shared-memory loads in the patterns the kernels use, counted as
+//            warp-instructions per clock: 16-byte loads where groups of four
+//            neighbouring lanes share an address (lane >> 2: the per-channel-pair
+//            records), 16-byte loads where the four lanes of a group read four
+//            different addresses (lane & 3: the b/c rows), 8-byte loads shared by
+//            groups of four, and a shuffle interleaved with a 16-byte load;
 //   copy     a device-memory copy of 2 GiB (read + write bytes), for HBM.
 // Each compute probe runs one CTA of 1024 threads per SM with 8 independent
 // chains per thread, times its loop with clock64 and reports operations per
@@ -35,14 +39,19 @@ __device__ __forceinline__ float mufu_ex2(float v) {
     return r;
 }
 
-enum Probe { kEx2 = 0, kFfma, kFfma2, kMix, kShfl, kLds128, kNumProbes };
+enum Probe { kEx2 = 0, kFfma, kFfma2, kMix, kShfl, kLds128, kLds128Quad, kLds128Spread, kLds64Quad, kShflLds,
+             kNumProbes };
 
 // ops counted per inner iteration per thread: 8 chains x (1 op), except the mix (8 elements)
-// and lds128 (8 loads)
+// and the shared loads (8 loads; shfl + load: 8 pairs)
 template <int P>
 __global__ void __launch_bounds__(1024, 1) probe(float* sink, long long* cycles, int iters, float a, float b) {
     __shared__ float4 tile[64];
     if (threadIdx.x < 64) tile[threadIdx.x] = make_float4(threadIdx.x, 1.f, 2.f, 3.f);
+    const int lane = threadIdx.x & 31;
+    // 16-byte column of the shared-load probes: groups of 4 lanes share one (quad) or the
+    // 4 lanes of a group read 4 different ones (spread)
+    const int qcol = (P == kLds128Spread) ? (lane & 3) : (lane >> 2);
     float v[8];
     float2 w[8];
 #pragma unroll
@@ -68,6 +77,16 @@ __global__ void __launch_bounds__(1024, 1) probe(float* sink, long long* cycles,
                 const float4 q = tile[(row + i + it) & 63];
                 w[i] = __fadd2_rn(w[i], make_float2(q.x, q.y));
                 w[i] = __fadd2_rn(w[i], make_float2(q.z, q.w));
+            }
+            if (P == kLds128Quad || P == kLds128Spread || P == kShflLds) {
+                const float4 q = tile[(qcol + 8 * i + it) & 63];
+                w[i] = __fadd2_rn(w[i], make_float2(q.x, q.y));
+                w[i] = __fadd2_rn(w[i], make_float2(q.z, q.w));
+                if (P == kShflLds) v[i] = __shfl_xor_sync(0xffffffffu, v[i], 1 + (i & 7)) + b;
+            }
+            if (P == kLds64Quad) {
+                const float2 q = reinterpret_cast<const float2*>(tile)[(qcol + 8 * i + it) & 127];
+                w[i] = __fadd2_rn(w[i], q);
             }
         }
     }
@@ -127,7 +146,9 @@ int main() {
     CHECK(cudaMalloc(&sink, sizeof(float) * 1024 * sms));
     CHECK(cudaMalloc(&cycles, sizeof(long long) * sms));
     long long* host = new long long[sms];
-    const char* names[kNumProbes] = {"ex2", "ffma", "ffma2_pairs", "ex2_plus_4_fp32", "shfl", "lds128_loads"};
+    const char* names[kNumProbes] = {"ex2", "ffma", "ffma2_pairs", "ex2_plus_4_fp32", "shfl", "lds128_loads",
+                                     "lds128_quad_shared_loads", "lds128_quad_spread_loads",
+                                     "lds64_quad_shared_loads", "shfl_plus_lds128_pairs"};
     double rate[kNumProbes] = {}, mhz[kNumProbes] = {};
     if (run_probe<kEx2>(sms, sink, cycles, host, &rate[kEx2], &mhz[kEx2])) return 1;
     if (run_probe<kFfma>(sms, sink, cycles, host, &rate[kFfma], &mhz[kFfma])) return 1;
@@ -135,6 +156,10 @@ int main() {
     if (run_probe<kMix>(sms, sink, cycles, host, &rate[kMix], &mhz[kMix])) return 1;
     if (run_probe<kShfl>(sms, sink, cycles, host, &rate[kShfl], &mhz[kShfl])) return 1;
     if (run_probe<kLds128>(sms, sink, cycles, host, &rate[kLds128], &mhz[kLds128])) return 1;
+    if (run_probe<kLds128Quad>(sms, sink, cycles, host, &rate[kLds128Quad], &mhz[kLds128Quad])) return 1;
+    if (run_probe<kLds128Spread>(sms, sink, cycles, host, &rate[kLds128Spread], &mhz[kLds128Spread])) return 1;
+    if (run_probe<kLds64Quad>(sms, sink, cycles, host, &rate[kLds64Quad], &mhz[kLds64Quad])) return 1;
+    if (run_probe<kShflLds>(sms, sink, cycles, host, &rate[kShflLds], &mhz[kShflLds])) return 1;
 
     // HBM: copy 2 GiB, best of 10
     const size_t bytes = size_t(2) << 30, n4 = bytes / 16;

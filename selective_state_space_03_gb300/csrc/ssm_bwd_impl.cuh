@@ -68,7 +68,10 @@ struct BwdCfg {
     // shared memory (bytes)
     static constexpr size_t RAW_X = size_t(LS) * DT * sizeof(TIO);          // one of x, delta, dy
     static constexpr size_t RAW_BC = size_t(LS) * kDS * sizeof(TIO);        // one of b, c
-    static constexpr size_t CONV = size_t(LS) * DT * 16;                    // float4 per (step, channel)
+    // float4 per (step, channel); rows padded by one float4 so that the 4 lanes of a channel,
+    // which read 4 different steps at once in the per-step sums, hit different banks
+    static constexpr int CROW = DT + 1;
+    static constexpr size_t CONV = size_t(LS) * CROW * 16;
     static constexpr size_t BCF = size_t(LS) * kDS * 4;                     // one of b, c as float32
     static constexpr size_t SUB = size_t(NSUB) * NT * 16;                   // float4 sub-checkpoints
     static constexpr size_t GBC = size_t(NW) * LS * 2 * kDS * 4;            // per-warp sums of gb, gc for a tile
@@ -150,7 +153,7 @@ __global__ void __launch_bounds__(128, 4) bwd_kernel(const BwdLaunch p) {
     TIO* yr = reinterpret_cast<TIO*>(ptr);  ptr += C::RAW_X;
     TIO* br = reinterpret_cast<TIO*>(ptr);  ptr += C::RAW_BC;
     TIO* cr = reinterpret_cast<TIO*>(ptr);  ptr += C::RAW_BC;
-    float4* conv = reinterpret_cast<float4*>(ptr); ptr += C::CONV;     // [LS][DT]
+    float4* conv = reinterpret_cast<float4*>(ptr); ptr += C::CONV;     // [LS][CROW]
     float* bf = reinterpret_cast<float*>(ptr);     ptr += C::BCF;      // [LS][16]
     float* cf = reinterpret_cast<float*>(ptr);     ptr += C::BCF;
     float4* sub = reinterpret_cast<float4*>(ptr);  ptr += C::SUB;      // [NSUB][NT]
@@ -237,7 +240,7 @@ __global__ void __launch_bounds__(128, 4) bwd_kernel(const BwdLaunch p) {
             float dl = to_f32(dr[i]);
             if (FUSE && p.softplus) dl = (i / DT < rows_valid) ? softplus_f32(dl) : 0.f;
             const float xv = to_f32(xr[i]);
-            conv[i] = make_float4(dl, dl * xv, xv, rev ? to_f32(yr[i]) : 0.f);
+            conv[(i / DT) * C::CROW + i % DT] = make_float4(dl, dl * xv, xv, rev ? to_f32(yr[i]) : 0.f);
         }
 #pragma unroll
         for (int k = 0; k < LS * kDS / NT; ++k) {
@@ -303,7 +306,7 @@ __global__ void __launch_bounds__(128, 4) bwd_kernel(const BwdLaunch p) {
             float2 h2[2] = {make_float2(h[0], h[1]), make_float2(h[2], h[3])};
 #pragma unroll 4
             for (int r = 0; r < LS; ++r) {
-                const float2 v = *reinterpret_cast<const float2*>(conv + r * DT + c);   // delta, delta*x
+                const float2 v = *reinterpret_cast<const float2*>(conv + r * C::CROW + c);   // delta, delta*x
                 const float4 b4 = *reinterpret_cast<const float4*>(bf + r * kDS + s0);
                 const float2 bp[2] = {make_float2(b4.x, b4.y), make_float2(b4.z, b4.w)};
                 const float2 dl2 = make_float2(v.x, v.x), dx2 = make_float2(v.y, v.y);
@@ -340,7 +343,7 @@ __global__ void __launch_bounds__(128, 4) bwd_kernel(const BwdLaunch p) {
                 float2 hc[2] = {make_float2(hs[0], hs[1]), make_float2(hs[2], hs[3])};
 #pragma unroll
                 for (int r = 0; r < LS; ++r) {
-                    const float2 v = *reinterpret_cast<const float2*>(conv + r * DT + c);
+                    const float2 v = *reinterpret_cast<const float2*>(conv + r * C::CROW + c);
                     const float4 b4 = *reinterpret_cast<const float4*>(bf + r * kDS + s0);
                     const float2 bp[2] = {make_float2(b4.x, b4.y), make_float2(b4.z, b4.w)};
                     const float2 dl2 = make_float2(v.x, v.x), dx2 = make_float2(v.y, v.y);
@@ -374,8 +377,8 @@ __global__ void __launch_bounds__(128, 4) bwd_kernel(const BwdLaunch p) {
                 for (int jj = 3; jj >= 0; --jj) {
                     const int r = rg + jj;
                     // delta, delta*x and dy of this step (x is read once per 4 steps, below)
-                    const float2 v2 = *reinterpret_cast<const float2*>(conv + r * DT + c);
-                    const float dyv = reinterpret_cast<const float*>(conv + r * DT + c)[3];
+                    const float2 v2 = *reinterpret_cast<const float2*>(conv + r * C::CROW + c);
+                    const float dyv = reinterpret_cast<const float*>(conv + r * C::CROW + c)[3];
                     const float4 v = make_float4(v2.x, v2.y, 0.f, dyv);
                     const float4 c4 = *reinterpret_cast<const float4*>(cf + r * kDS + s0);
                     const float2 cp[2] = {make_float2(c4.x, c4.y), make_float2(c4.z, c4.w)};
@@ -407,7 +410,7 @@ __global__ void __launch_bounds__(128, 4) bwd_kernel(const BwdLaunch p) {
                 const float rs = reduce_scatter_steps<4>(rr, sg);
                 const float qs = reduce_scatter_steps<4>(qq, sg);
                 const int r = rg + sg;
-                const float* vr = reinterpret_cast<const float*>(conv + r * DT + c);
+                const float* vr = reinterpret_cast<const float*>(conv + r * C::CROW + c);
                 const float dl = vr[0], xv = vr[2];
                 const int64_t t = t0 + r;
                 if (valid && t < ce) {

@@ -76,14 +76,16 @@ struct FwdCfg {
     static_assert(X_CPR >= 1 && DT % EPC == 0, "tile rows must be whole 16-byte chunks");
 };
 
-// The lane's KD x KS states into a (.., D, 16) array (rows of chains b * D + d).
+// The lane's KD x KS states into a (.., D, 16) array (rows of chains b * D + d); channel slot k
+// of the lane holds channel dfirst + (k ^ perm).
 template <int G, int KD>
 __device__ __forceinline__ void store_lane_states(float* base, int64_t b, int64_t D, int64_t dfirst, int s0,
-                                                  const bool (&valid)[KD], const float2 (&h)[KD][kDS / G / 2]) {
+                                                  const bool (&valid)[KD], const float2 (&h)[KD][kDS / G / 2],
+                                                  int perm = 0) {
 #pragma unroll
     for (int k = 0; k < KD; ++k) {
         if (!valid[k]) continue;
-        float4* dst = reinterpret_cast<float4*>(base + (b * D + dfirst + k) * kDS + s0);
+        float4* dst = reinterpret_cast<float4*>(base + (b * D + dfirst + (k ^ perm)) * kDS + s0);
 #pragma unroll
         for (int q = 0; q < kDS / G / 2; q += 2)
             dst[q / 2] = make_float4(h[k][q].x, h[k][q].y, h[k][q + 1].x, h[k][q + 1].y);
@@ -118,6 +120,13 @@ __device__ __forceinline__ void fwd_sweep(const FwdLaunch& p, int64_t b, int64_t
     const int s0 = gl * KS;
     const int64_t T = p.T, D = p.D;
     const bool full_d = d0 + DT <= D;
+    // Two lanes per channel pair with bf16 I/O: lane gl holds its channels in the order
+    // (c0 + gl, c0 + (gl ^ 1)), so that the readout exchange keeps slot 0 and sends slot 1 on
+    // every lane (no selects); the bf16 pairs are unpacked into that order by byte permutes
+    // whose selectors are per-lane constants.
+    constexpr bool PERM = (G == 2 && C::BF);
+    const int perm = PERM ? gl : 0;
+    const uint32_t sel0 = gl ? 0x3244u : 0x1044u, sel1 = gl ? 0x1044u : 0x3244u;
 
     const TIO* xg = static_cast<const TIO*>(p.x) + b * T * D;
     const TIO* dg = static_cast<const TIO*>(p.delta) + b * T * D;
@@ -180,7 +189,7 @@ __device__ __forceinline__ void fwd_sweep(const FwdLaunch& p, int64_t b, int64_t
             if (READ) stage_tile<TIO, TT, kDS, NT, true>(csr + buf * TT * kDS, cgl, kDS, t0, t_end, 0);
         }
     };
-    auto store_state = [&](float* base) { store_lane_states<G, KD>(base, b, D, d0 + c0, s0, valid, h); };
+    auto store_state = [&](float* base) { store_lane_states<G, KD>(base, b, D, d0 + c0, s0, valid, h, perm); };
 
     if (ntiles > 0) {
         stage(0, 0);
@@ -245,9 +254,23 @@ __device__ __forceinline__ void fwd_sweep(const FwdLaunch& p, int64_t b, int64_t
                     next_ck += K;
                 }
                 float dl[KD], xv[KD];
-                if constexpr (FUSE) load_vals<float, KD>(dsf + r * DT + c0, dl);
-                else load_vals<TIO, KD>(dt + r * DT + c0, dl);
-                load_vals<TIO, KD>(xt + r * DT + c0, xv);
+                if constexpr (PERM) {
+                    if constexpr (FUSE) {
+                        dl[0] = dsf[r * DT + c0 + gl];
+                        dl[1] = dsf[r * DT + c0 + (gl ^ 1)];
+                    } else {
+                        const uint32_t w = *reinterpret_cast<const uint32_t*>(dt + r * DT + c0);
+                        dl[0] = __uint_as_float(__byte_perm(w, 0u, sel0));
+                        dl[1] = __uint_as_float(__byte_perm(w, 0u, sel1));
+                    }
+                    const uint32_t wx = *reinterpret_cast<const uint32_t*>(xt + r * DT + c0);
+                    xv[0] = __uint_as_float(__byte_perm(wx, 0u, sel0));
+                    xv[1] = __uint_as_float(__byte_perm(wx, 0u, sel1));
+                } else {
+                    if constexpr (FUSE) load_vals<float, KD>(dsf + r * DT + c0, dl);
+                    else load_vals<TIO, KD>(dt + r * DT + c0, dl);
+                    load_vals<TIO, KD>(xt + r * DT + c0, xv);
+                }
                 float2 bb[KP], cc[KP];
 #pragma unroll
                 for (int q = 0; q < KP; q += 2) {
@@ -266,8 +289,9 @@ __device__ __forceinline__ void fwd_sweep(const FwdLaunch& p, int64_t b, int64_t
                     const float dx = dl[k] * xv[k];
                     // Packed (f32x2) multiplies for the exponent arguments and the input
                     // term, packed FMA for the state update, scalar readout: on sm_103a this
-                    // mix issues the fewest instructions per element (measured; a packed
-                    // readout was slower).
+                    // mix issues the fewest instructions per element for the time it takes
+                    // (measured; a packed readout, with one or two accumulators, was 2-4 %
+                    // slower).
                     float acc0 = 0.f, acc1 = 0.f;
                     const float2 dl2 = make_float2(dl[k], dl[k]), dx2 = make_float2(dx, dx);
 #pragma unroll
@@ -311,8 +335,9 @@ __device__ __forceinline__ void fwd_sweep(const FwdLaunch& p, int64_t b, int64_t
                     float out[H];
 #pragma unroll
                     for (int i = 0; i < H; ++i) {
-                        const float send = gl ? part[0][i] : part[0][H + i];
-                        const float keep = gl ? part[0][H + i] : part[0][i];
+                        // (with PERM, slot 0 is already this lane's own channel)
+                        const float send = PERM ? part[0][1] : (gl ? part[0][i] : part[0][H + i]);
+                        const float keep = PERM ? part[0][0] : (gl ? part[0][H + i] : part[0][i]);
                         out[i] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
                         if constexpr (FUSE)                                                // skip
                             out[i] = fmaf(Dkeep[i], to_f32(xt[tt * DT + c0 + gl * H + i]), out[i]);
@@ -344,16 +369,17 @@ __device__ __forceinline__ void fwd_sweep(const FwdLaunch& p, int64_t b, int64_t
 }
 
 // Lane layout, A * log2(e) and the start state of the lane's chains (channels d0 + c0 + k).
+// Channel slot k of the lane is channel d0 + c0 + (k ^ perm).
 template <typename TIO, int G, int KD>
 __device__ __forceinline__ void fwd_lane_setup(const FwdLaunch& p, int64_t b, int64_t d0, bool with_h0,
                                                bool (&valid)[KD], float2 (&A2)[KD][FwdCfg<TIO, G, KD>::KP],
-                                               float2 (&h)[KD][FwdCfg<TIO, G, KD>::KP]) {
+                                               float2 (&h)[KD][FwdCfg<TIO, G, KD>::KP], int perm = 0) {
     constexpr int KP = FwdCfg<TIO, G, KD>::KP, KS = FwdCfg<TIO, G, KD>::KS;
     const int lane = threadIdx.x;
     const int c0 = (lane / G) * KD, s0 = (lane % G) * KS;
 #pragma unroll
     for (int k = 0; k < KD; ++k) {
-        const int64_t d = d0 + c0 + k;
+        const int64_t d = d0 + c0 + (k ^ perm);
         valid[k] = d < p.D;
 #pragma unroll
         for (int q = 0; q < KP; ++q) {
@@ -383,15 +409,30 @@ __global__ void __launch_bounds__(32, FwdCfg<TIO, G, KD>::MINB) fwd_kernel(const
     const int64_t t_begin = chunk * p.Lc;
     const int64_t t_end = (MODE == kPass1 || MODE == kPass2) ? min(p.T, t_begin + p.Lc) : p.T;
 
+    constexpr bool PERM = (G == 2 && C::BF);        // the channel order fwd_sweep uses
+    const int perm = PERM ? gl : 0;
     bool valid[KD];
     float2 A2[KD][KP], h[KD][KP];
-    fwd_lane_setup<TIO, G, KD>(p, b, d0, MODE != kPass1, valid, A2, h);
+    fwd_lane_setup<TIO, G, KD>(p, b, d0, MODE != kPass1, valid, A2, h, perm);
     if constexpr (MODE == kPass2) {
-        // start state of this chunk: fold the carries of the chunks before it, in order; the
-        // loads of NB chunks are issued together (one round trip to L2 per NB chunks)
         static_assert(KP == 2, "the chunk passes use 4 lanes per chain (4 states per lane)");
+        if (p.carry_scanned) {
+            // the middle pass left this chunk's start state in the carry of the chunk before it
+            if (chunk > 0) {
+#pragma unroll
+                for (int k = 0; k < KD; ++k) {
+                    if (!valid[k]) continue;
+                    const int64_t row = (b * nprev + chunk - 1) * D + d0 + c0 + k;
+                    const float4 v = *reinterpret_cast<const float4*>(p.ws_S + row * kDS + s0);
+                    h[k][0] = make_float2(v.x, v.y);
+                    h[k][1] = make_float2(v.z, v.w);
+                }
+            }
+        }
+        // otherwise: start state of this chunk: fold the carries of the chunks before it, in
+        // order; the loads of NB chunks are issued together (one round trip to L2 per NB chunks)
         constexpr int NB = 4;
-        for (int64_t j0 = 0; j0 < chunk; j0 += NB) {
+        for (int64_t j0 = 0; j0 < (p.carry_scanned ? 0 : chunk); j0 += NB) {
             float sd[NB][KD];
             float4 Sv[NB][KD];
 #pragma unroll
@@ -440,7 +481,7 @@ __global__ void __launch_bounds__(32, FwdCfg<TIO, G, KD>::MINB) fwd_kernel(const
         return;
     }
     const bool last = (MODE != kPass2) || (chunk == p.nchunk - 1);
-    if (last && p.hT != nullptr) store_lane_states<G, KD>(p.hT, b, D, d0 + c0, s0, valid, h);
+    if (last && p.hT != nullptr) store_lane_states<G, KD>(p.hT, b, D, d0 + c0, s0, valid, h, perm);
 }
 
 __device__ __forceinline__ int ld_acquire_gpu(const int* ptr) {

@@ -31,6 +31,7 @@ struct FwdLaunch {
     float* ckpt;    // may be null
     float* ws_S;    // [B][nchunk-1][D][16]   (chunked modes)
     float* ws_Sd;   // [B][nchunk-1][D]       (chunked modes)
+    bool carry_scanned;  // mode 2: ws_S holds the start states of chunks 1.. (launch_fwd_carry_scan)
     int64_t B, T, D;
     int64_t K;      // checkpoint interval, 0 = none
     int64_t Lc;     // chunk length (chunked modes; T in mode 0)
@@ -56,6 +57,12 @@ struct FwdLaunch {
 
 cudaError_t launch_fwd_f32(const FwdLaunch& L, int mode, cudaStream_t stream);
 cudaError_t launch_fwd_bf16(const FwdLaunch& L, int mode, cudaStream_t stream);
+// Between the chunked passes: overwrite each chunk's carry S_j in ws_S with the start state of
+// chunk j + 1 (one sweep per chain), for pass 2 with carry_scanned set.
+cudaError_t launch_fwd_carry_scan(const FwdLaunch& L, cudaStream_t stream);
+// Chunked forwards with more carries than this fold them in the middle pass above (linear in
+// the chunk count) instead of in every pass-2 CTA (quadratic).
+constexpr int64_t kCarryScanMinCarries = 48;
 
 struct BwdLaunch {
     const void* x;
@@ -77,6 +84,7 @@ struct BwdLaunch {
     IO io;
     bool vec;
     int kd;              // channels per lane: 1 (32 channels per CTA) or 2 (64 per CTA)
+    bool split;          // kd == 2: producer and consumer warpgroups (bwd3_kernel; not the fused variant)
     // chunk-parallel schedule (kd == 1 only): one CTA per (channel block, batch, chunk); the
     // adjoint entering each chunk comes from the carries of all later chunks
     bool tpar;

@@ -64,7 +64,7 @@ extern "C" ssm_status ssm_scan_fwd_noalloc(const ssm_scan_desc* desc, const void
     const ssm_scan_desc& d = *desc;
     if (d.B < 0 || d.T < 0 || d.D < 0 || d.DS < 0) return SSM_ERR_INVALID_ARG;
     if (d.io != SSM_IO_F32 && d.io != SSM_IO_BF16) return SSM_ERR_INVALID_ARG;
-    if (d.ckpt_interval < 0 || (d.flags & ~(SSM_SCAN_DETERMINISTIC | SSM_SCAN_DELTA_SOFTPLUS | SSM_SCAN_LOOKBACK)) != 0 || d.B > 65535) return SSM_ERR_INVALID_ARG;
+    if (d.ckpt_interval < 0 || (d.flags & ~(SSM_SCAN_DETERMINISTIC | SSM_SCAN_DELTA_SOFTPLUS | SSM_SCAN_LOOKBACK | SSM_SCAN_STEP_INPUTS_READY)) != 0 || d.B > 65535) return SSM_ERR_INVALID_ARG;
     if (d.DS != kDS) return SSM_ERR_UNSUPPORTED;
     if (d.D > kMaxD) return SSM_ERR_UNSUPPORTED;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -119,6 +119,10 @@ extern "C" ssm_status ssm_scan_fwd_noalloc(const ssm_scan_desc* desc, const void
     L.ws_S = static_cast<float*>(base);
     L.ws_Sd = reinterpret_cast<float*>(static_cast<unsigned char*>(base) + bytes_S);
     cudaError_t e = run(1);
+    if (e == cudaSuccess && nchunk - 1 > kCarryScanMinCarries) {    // start states folded in place
+        L.carry_scanned = true;
+        e = launch_fwd_carry_scan(L, s);
+    }
     if (e == cudaSuccess) e = run(2);
     return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }

@@ -184,6 +184,17 @@ def test_chunked_two_channels_per_lane_unaligned(io):
     run_case(gen.workload(2, B=3, T=300, D=D, io=io, h0_std=0.1), K=32, chunk_len=64, bwd=False, chunk_kd=2)
 
 
+@pytest.mark.parametrize("T,chunk_len,scan", [(230, 64, 1), (700, 16, None), (700, 16, 0), (1000, 16, 1),
+                                              (16 * 40 + 5, 16, None)])
+@pytest.mark.parametrize("chunk_kd", [1, 2])
+def test_chunked_carry_scan(T, chunk_len, scan, chunk_kd):
+    # the middle pass that folds the chunk carries once per chain (on by default above 32
+    # carries; forced on or off here) against the oracle: y, hT and checkpoints, ragged last chunk
+    w = gen.workload(2, B=2, T=T, D=40, h0_std=0.1)
+    with forced(SSM_SCAN_FORCE_CARRY_SCAN=scan):
+        run_case(w, K=32, chunk_len=chunk_len, bwd=False, chunk_kd=chunk_kd)
+
+
 def test_backward_rebuilds_checkpoints():
     # no checkpoints passed: the backward rebuilds them in its workspace
     run_case(gen.workload(2, B=2, T=300, D=40, h0_std=0.1), K=64, ghT=True, ckpt_to_bwd=False)
