@@ -49,7 +49,7 @@ ssm_status check_desc(const ssm_scan_desc* d) {
     if (d == nullptr) return SSM_ERR_INVALID_ARG;
     if (d->B < 0 || d->T < 0 || d->D < 0 || d->DS < 0) return SSM_ERR_INVALID_ARG;
     if (d->io != SSM_IO_F32 && d->io != SSM_IO_BF16) return SSM_ERR_INVALID_ARG;
-    constexpr int32_t kFlags = SSM_SCAN_DETERMINISTIC | SSM_SCAN_DELTA_SOFTPLUS | SSM_SCAN_LOOKBACK;
+    constexpr int32_t kFlags = SSM_SCAN_DETERMINISTIC | SSM_SCAN_DELTA_SOFTPLUS | SSM_SCAN_LOOKBACK | SSM_SCAN_STEP_INPUTS_READY;
     if (d->ckpt_interval < 0 || (d->flags & ~kFlags) != 0) return SSM_ERR_INVALID_ARG;
     if (d->B > 65535) return SSM_ERR_INVALID_ARG;
     if (d->DS != kDS) return SSM_ERR_UNSUPPORTED;
@@ -294,6 +294,13 @@ ssm_status ssm_scan_fwd_fused(const ssm_scan_desc* desc, const void* x, const vo
         L.ws_S = static_cast<float*>(workspace);
         L.ws_Sd = reinterpret_cast<float*>(static_cast<char*>(workspace) + P.ws_S);
         e = run_fwd(d, L, 1, s);
+        bool scan = P.nchunk - 1 > kCarryScanMinCarries;
+        // testing build only: force the middle pass on (1) or off (0)
+        if (const char* env = SSM_TEST_ENV("SSM_SCAN_FORCE_CARRY_SCAN")) scan = std::atoi(env) == 1;
+        if (e == cudaSuccess && scan) {
+            L.carry_scanned = true;
+            e = launch_fwd_carry_scan(L, s);
+        }
         if (e == cudaSuccess) e = run_fwd(d, L, 2, s);
     } else if (P.mode == 4) {
         char* w = static_cast<char*>(workspace);

@@ -60,8 +60,11 @@ struct Bwd2Cfg {
     // shared memory (bytes)
     static constexpr size_t RAW_X = size_t(LS) * DT * sizeof(TIO);          // one of x, delta, dy
     static constexpr size_t RAW_BC = size_t(LS) * kDS * sizeof(TIO);        // one of b, c
-    static constexpr size_t CONV1 = size_t(LS) * NP * 16;                   // (d0, d0*x0, d1, d1*x1)
-    static constexpr size_t CONV2 = size_t(LS) * NP * 16;                   // (dy0, dy1, x0, x1)
+    // converted records, one float4 per (step, pair); rows padded by one float4 so that the 4 lanes
+    // of a pair, which read 4 different steps at once in the per-step sums, hit different banks
+    static constexpr int CROW = NP + 1;
+    static constexpr size_t CONV1 = size_t(LS) * CROW * 16;                 // (d0, d0*x0, d1, d1*x1)
+    static constexpr size_t CONV2 = size_t(LS) * CROW * 16;                 // (dy0, dy1, x0, x1)
     static constexpr size_t BCF = size_t(4) * LS * kDS * 4;                 // one of b, c as float32, 4 state orders
     // per-half-warp gb, gc sums of a tile, [2 NW][LS][2][16] floats; sets padded by 16 floats so
     // the two sets a warp writes at once fall on different banks
@@ -98,8 +101,8 @@ __global__ void __launch_bounds__(128, 3) bwd2_kernel(const BwdLaunch p) {
     TIO* yr = reinterpret_cast<TIO*>(ptr);  ptr += C::RAW_X;
     TIO* br = reinterpret_cast<TIO*>(ptr);  ptr += C::RAW_BC;
     TIO* cr = reinterpret_cast<TIO*>(ptr);  ptr += C::RAW_BC;
-    float4* conv1 = reinterpret_cast<float4*>(ptr); ptr += C::CONV1;   // [LS][NP]
-    float4* conv2 = reinterpret_cast<float4*>(ptr); ptr += C::CONV2;   // [LS][NP]
+    float4* conv1 = reinterpret_cast<float4*>(ptr); ptr += C::CONV1;   // [LS][CROW]
+    float4* conv2 = reinterpret_cast<float4*>(ptr); ptr += C::CONV2;   // [LS][CROW]
     float* bfp = reinterpret_cast<float*>(ptr);     ptr += C::BCF;     // [4 orders][LS][16]
     float* cfp = reinterpret_cast<float*>(ptr);     ptr += C::BCF;
     float* gbc = reinterpret_cast<float*>(ptr);     ptr += C::GBC;     // [2 NW][GSET]
@@ -210,11 +213,11 @@ __global__ void __launch_bounds__(128, 3) bwd2_kernel(const BwdLaunch p) {
                 dl[1] = r < rows_valid ? sp.y : 0.f;
             }
             load_vals<TIO, 2>(xr + r * DT + 2 * pp, xv);
-            conv1[i] = make_float4(dl[0], dl[0] * xv[0], dl[1], dl[1] * xv[1]);
+            conv1[r * C::CROW + pp] = make_float4(dl[0], dl[0] * xv[0], dl[1], dl[1] * xv[1]);
             if (rev) {
                 float dyv[2];
                 load_vals<TIO, 2>(yr + r * DT + 2 * pp, dyv);
-                conv2[i] = make_float4(dyv[0], dyv[1], xv[0], xv[1]);
+                conv2[r * C::CROW + pp] = make_float4(dyv[0], dyv[1], xv[0], xv[1]);
             }
         }
         // b (threads 0-63) and c (threads 64-127): 4 states of one row each, stored in the four
@@ -303,7 +306,7 @@ __global__ void __launch_bounds__(128, 3) bwd2_kernel(const BwdLaunch p) {
                 for (int q = 0; q < KP; ++q) hp2[k][q] = make_float2(h[k][2 * q], h[k][2 * q + 1]);
 #pragma unroll 8
             for (int r = 0; r < LS; ++r) {
-                const float4 v = conv1[r * NP + pc];                                   // d0, d0 x0, d1, d1 x1
+                const float4 v = conv1[r * C::CROW + pc];                                   // d0, d0 x0, d1, d1 x1
                 const float4 b4 = *reinterpret_cast<const float4*>(bf + r * kDS + s0);
                 const float2 bp[KP] = {make_float2(b4.x, b4.y), make_float2(b4.z, b4.w)};
                 const float2 dl2[2] = {make_float2(v.x, v.x), make_float2(v.z, v.z)};
@@ -364,7 +367,7 @@ __global__ void __launch_bounds__(128, 3) bwd2_kernel(const BwdLaunch p) {
                     for (int q = 0; q < KP; ++q) hc[k][q] = make_float2(hs[k * KS + 2 * q], hs[k * KS + 2 * q + 1]);
 #pragma unroll
                 for (int r = 0; r < LS; ++r) {
-                    const float4 v = conv1[r * NP + pc];
+                    const float4 v = conv1[r * C::CROW + pc];
                     const float4 b4 = *reinterpret_cast<const float4*>(bf + r * kDS + s0);
                     const float2 bp[KP] = {make_float2(b4.x, b4.y), make_float2(b4.z, b4.w)};
                     const float2 dl2[2] = {make_float2(v.x, v.x), make_float2(v.z, v.z)};
@@ -402,8 +405,8 @@ __global__ void __launch_bounds__(128, 3) bwd2_kernel(const BwdLaunch p) {
 #pragma unroll
                 for (int jj = 3; jj >= 0; --jj) {
                     const int r = rg + jj;
-                    const float4 v = conv1[r * NP + pc];                                           // d0, d0 x0, d1, d1 x1
-                    const float2 dyv = *reinterpret_cast<const float2*>(conv2 + r * NP + pc);      // dy0, dy1
+                    const float4 v = conv1[r * C::CROW + pc];                                           // d0, d0 x0, d1, d1 x1
+                    const float2 dyv = *reinterpret_cast<const float2*>(conv2 + r * C::CROW + pc);      // dy0, dy1
                     const float4 c4 = *reinterpret_cast<const float4*>(cf + r * kDS + s0);
                     const float4 b4 = *reinterpret_cast<const float4*>(bf + r * kDS + s0);
                     const float2 cp[KP] = {make_float2(c4.x, c4.y), make_float2(c4.z, c4.w)};
@@ -467,8 +470,8 @@ __global__ void __launch_bounds__(128, 3) bwd2_kernel(const BwdLaunch p) {
                     qs[k] = rq.y;
                 }
                 const int r = rg + sg;
-                const float4 v = conv1[r * NP + pc];
-                const float4 w = conv2[r * NP + pc];
+                const float4 v = conv1[r * C::CROW + pc];
+                const float4 w = conv2[r * C::CROW + pc];
                 const int64_t t = t0 + r;
                 if (t < ce) {
                     float gx0 = v.x * qs[0], gx1 = v.z * qs[1];

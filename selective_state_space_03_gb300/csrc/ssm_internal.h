@@ -84,7 +84,6 @@ struct BwdLaunch {
     IO io;
     bool vec;
     int kd;              // channels per lane: 1 (32 channels per CTA) or 2 (64 per CTA)
-    bool split;          // kd == 2: producer and consumer warpgroups (bwd3_kernel; not the fused variant)
     // chunk-parallel schedule (kd == 1 only): one CTA per (channel block, batch, chunk); the
     // adjoint entering each chunk comes from the carries of all later chunks
     bool tpar;
