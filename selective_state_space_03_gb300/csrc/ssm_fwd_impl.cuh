@@ -62,8 +62,11 @@ struct FwdCfg {
     static constexpr int BC_PL = (BC_CH + NT - 1) / NT;
     static constexpr int Y_CH = TT * X_CPR;                      // y chunks per tile
     static constexpr int Y_PL = (Y_CH + NT - 1) / NT;
-    static constexpr size_t X_BYTES = size_t(2) * TT * DT * sizeof(TIO);     // one tensor, 2 buffers
-    static constexpr size_t BC_RAW = size_t(2) * TT * kDS * sizeof(TIO);    // one tensor, 2 buffers
+    // staging buffers per tensor: tiles are loaded NBUF - 1 tiles ahead (3 or 4 buffers for the
+    // low-occupancy layouts measured no faster than 2)
+    static constexpr int NBUF = 2;
+    static constexpr size_t X_BYTES = size_t(NBUF) * TT * DT * sizeof(TIO);     // one tensor
+    static constexpr size_t BC_RAW = size_t(NBUF) * TT * kDS * sizeof(TIO);    // one tensor
     static constexpr size_t BC_F32 = BF ? size_t(TT) * kDS * 4 : 0;          // widened copy (bf16)
     static constexpr size_t Y_BYTES = size_t(TT) * DT * sizeof(TIO);
     static constexpr size_t SMEM = 2 * X_BYTES + 2 * BC_RAW + 2 * BC_F32 + Y_BYTES;
@@ -191,19 +194,17 @@ __device__ __forceinline__ void fwd_sweep(const FwdLaunch& p, int64_t b, int64_t
     };
     auto store_state = [&](float* base) { store_lane_states<G, KD>(base, b, D, d0 + c0, s0, valid, h, perm); };
 
-    if (ntiles > 0) {
-        stage(0, 0);
+    // one cp.async group per tile (empty past the end), so every wait has the same depth
+#pragma unroll
+    for (int u = 0; u < C::NBUF - 1; ++u) {
+        if (u < ntiles) stage(u, u);
         cp_async_commit();
     }
     for (int64_t tile = 0; tile < ntiles; ++tile) {
-        const int buf = int(tile & 1);
-        if (tile + 1 < ntiles) {
-            stage(tile + 1, buf ^ 1);
-            cp_async_commit();
-            cp_async_wait<1>();
-        } else {
-            cp_async_wait<0>();
-        }
+        const int buf = int(tile % C::NBUF);
+        if (tile + C::NBUF - 1 < ntiles) stage(tile + C::NBUF - 1, int((tile + C::NBUF - 1) % C::NBUF));
+        cp_async_commit();
+        cp_async_wait<C::NBUF - 1>();
         __syncwarp();
         const float* bt;
         const float* ct;
