@@ -255,12 +255,13 @@ ssm_status ssm_scan_bwd_fused(const ssm_scan_desc* desc,
  * and can fail under memory pressure.
  *
  * It always uses the chunked two-pass schedule (chunk length desc->chunk_len
- * when > 0, else chosen by the library; one chunk falls back to the one-pass
- * scan, which needs no scratch) and keeps the chunk carries in a fixed device
- * array inside the library of SSM_SCAN_NOALLOC_SCRATCH_BYTES bytes, which
- * every GPU that loads the library holds until the process exits. Carries take
- * B*(nchunk-1)*D*68 bytes (each part rounded up to 256); larger problems are
- * rejected with SSM_ERR_WORKSPACE before anything is enqueued.
+ * when > 0, else chosen by the library and doubled until the carries fit; one
+ * chunk falls back to the one-pass scan, which needs no scratch) and keeps the
+ * chunk carries in a fixed device array inside the library of
+ * SSM_SCAN_NOALLOC_SCRATCH_BYTES bytes, which every GPU that loads the library
+ * holds until the process exits. Carries take B*(nchunk-1)*D*68 bytes (each
+ * part rounded up to 256); a caller's chunk length that needs more is rejected
+ * with SSM_ERR_WORKSPACE before anything is enqueued.
  *
  * Each call looks up the array's device address in the CUDA context current on
  * the calling thread (cudaGetSymbolAddress, a host-side lookup that allocates

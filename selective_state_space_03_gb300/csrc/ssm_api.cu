@@ -87,24 +87,41 @@ FwdPlan plan_fwd(const ssm_scan_desc& d) {
     FwdPlan P{0, 4, 1, d.T, 1, 0, 0, 0, 0, 0, 0};
     const int64_t chains = d.B * d.D;
     const int64_t want = int64_t(device_sm_count()) * 512;   // ~16 resident warps per SM
+    // Chosen by the library: chunked when one pass would leave fewer than about 16 warps per SM
+    // (4 lanes per chain), and for long sequences up to about 84 chains per SM, where the one-pass
+    // grid leaves one or two warps per SMSP and the second sweep over T costs less than the
+    // latency it hides (4096 steps, bf16: 8192 chains 251 -> 228 us, 10240 chains 341 -> 285 us,
+    // 12288 chains 343 -> 334 us; 16384 chains one pass 347 us, chunked 427 us).
+    const bool few_chains = chains * 4 * 2 < want ||
+                            (chains < int64_t(device_sm_count()) * 84 && d.T >= 2048);
     bool chunked = false;
     ChunkSchedule cs{0, 1};
-    if (d.chunk_len > 0 || (d.chunk_len == 0 && chains * 4 * 2 < want && d.T >= 256)) {
+    if (d.chunk_len > 0 || (d.chunk_len == 0 && few_chains && d.T >= 256)) {
         cs = chunk_schedule(d.T, chains, d.chunk_len, device_sm_count());
         chunked = cdiv(d.T, cs.Lc) >= 2;
     }
     if (chunked) {
         P.mode = 2;
-        P.G = 4;
+        P.G = cs.G;
         P.kd = cs.kd;
-        // testing build only: channels per lane of both chunk passes (1 or 2)
-        if (const char* env = SSM_TEST_ENV("SSM_SCAN_FORCE_CHUNK_KD")) P.kd = std::atoi(env) == 2 ? 2 : 1;
+        // testing build only: channels per lane of both chunk passes with 4 lanes per chain (1 or
+        // 2), or their layout ("2x2", "4x2", "4x1")
+        if (const char* env = SSM_TEST_ENV("SSM_SCAN_FORCE_CHUNK_KD")) {
+            P.G = 4;
+            P.kd = std::atoi(env) == 2 ? 2 : 1;
+        }
+        if (const char* env = SSM_TEST_ENV("SSM_SCAN_FORCE_CHUNK_LAYOUT")) {
+            if (std::strcmp(env, "2x2") == 0) { P.G = 2; P.kd = 2; }
+            if (std::strcmp(env, "4x2") == 0) { P.G = 4; P.kd = 2; }
+            if (std::strcmp(env, "4x1") == 0) { P.G = 4; P.kd = 1; }
+        }
         P.Lc = cs.Lc;
         P.nchunk = cdiv(d.T, cs.Lc);
         P.ws_S = align_up(size_t(d.B) * size_t(P.nchunk - 1) * size_t(d.D) * kDS * 4);
         P.ws_Sd = align_up(size_t(d.B) * size_t(P.nchunk - 1) * size_t(d.D) * 4);
         if (d.flags & SSM_SCAN_LOOKBACK) {
             P.mode = 4;
+            P.G = 4;                  // the look-back kernel runs 4 lanes per chain
             const size_t rows = size_t(d.B) * size_t(P.nchunk) * size_t(d.D);
             const size_t nblk = size_t(cdiv(d.D, 8 * P.kd));
             P.lb_S = align_up(rows * kDS * 4);

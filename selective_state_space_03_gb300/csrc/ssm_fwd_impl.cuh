@@ -416,36 +416,44 @@ __global__ void __launch_bounds__(32, FwdCfg<TIO, G, KD>::MINB) fwd_kernel(const
     float2 A2[KD][KP], h[KD][KP];
     fwd_lane_setup<TIO, G, KD>(p, b, d0, MODE != kPass1, valid, A2, h, perm);
     if constexpr (MODE == kPass2) {
-        static_assert(KP == 2, "the chunk passes use 4 lanes per chain (4 states per lane)");
+        // (channel slot k of the lane is channel d0 + c0 + (k ^ perm); a carry row holds a chain's
+        // 16 states, of which the lane's KS start at s0)
         if (p.carry_scanned) {
             // the middle pass left this chunk's start state in the carry of the chunk before it
             if (chunk > 0) {
 #pragma unroll
                 for (int k = 0; k < KD; ++k) {
                     if (!valid[k]) continue;
-                    const int64_t row = (b * nprev + chunk - 1) * D + d0 + c0 + k;
-                    const float4 v = *reinterpret_cast<const float4*>(p.ws_S + row * kDS + s0);
-                    h[k][0] = make_float2(v.x, v.y);
-                    h[k][1] = make_float2(v.z, v.w);
+                    const int64_t row = (b * nprev + chunk - 1) * D + d0 + c0 + (k ^ perm);
+                    const float4* src = reinterpret_cast<const float4*>(p.ws_S + row * kDS + s0);
+#pragma unroll
+                    for (int q = 0; q < KP; q += 2) {
+                        const float4 v = src[q / 2];
+                        h[k][q] = make_float2(v.x, v.y);
+                        h[k][q + 1] = make_float2(v.z, v.w);
+                    }
                 }
             }
         }
         // otherwise: start state of this chunk: fold the carries of the chunks before it, in
         // order; the loads of NB chunks are issued together (one round trip to L2 per NB chunks)
-        constexpr int NB = 4;
+        constexpr int NB = KP == 2 ? 4 : 2;
         for (int64_t j0 = 0; j0 < (p.carry_scanned ? 0 : chunk); j0 += NB) {
             float sd[NB][KD];
-            float4 Sv[NB][KD];
+            float4 Sv[NB][KD][KP / 2];
 #pragma unroll
             for (int u = 0; u < NB; ++u)
 #pragma unroll
                 for (int k = 0; k < KD; ++k) {
                     sd[u][k] = 0.f;
-                    Sv[u][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int q = 0; q < KP / 2; ++q) Sv[u][k][q] = make_float4(0.f, 0.f, 0.f, 0.f);
                     if (j0 + u < chunk && valid[k]) {
-                        const int64_t row = (b * nprev + j0 + u) * D + d0 + c0 + k;
+                        const int64_t row = (b * nprev + j0 + u) * D + d0 + c0 + (k ^ perm);
                         sd[u][k] = p.ws_Sd[row];
-                        Sv[u][k] = *reinterpret_cast<const float4*>(p.ws_S + row * kDS + s0);
+#pragma unroll
+                        for (int q = 0; q < KP / 2; ++q)
+                            Sv[u][k][q] = reinterpret_cast<const float4*>(p.ws_S + row * kDS + s0)[q];
                     }
                 }
 #pragma unroll
@@ -453,11 +461,12 @@ __global__ void __launch_bounds__(32, FwdCfg<TIO, G, KD>::MINB) fwd_kernel(const
                 if (j0 + u >= chunk) break;
 #pragma unroll
                 for (int k = 0; k < KD; ++k) {
-                    const float2 S2[2] = {make_float2(Sv[u][k].x, Sv[u][k].y), make_float2(Sv[u][k].z, Sv[u][k].w)};
 #pragma unroll
                     for (int q = 0; q < KP; ++q) {
+                        const float4 v = Sv[u][k][q / 2];
+                        const float2 S2 = (q & 1) ? make_float2(v.z, v.w) : make_float2(v.x, v.y);
                         const float2 P = make_float2(ex2(A2[k][q].x * sd[u][k]), ex2(A2[k][q].y * sd[u][k]));
-                        h[k][q] = __ffma2_rn(P, h[k][q], S2[q]);
+                        h[k][q] = __ffma2_rn(P, h[k][q], S2);
                     }
                 }
             }
@@ -473,7 +482,7 @@ __global__ void __launch_bounds__(32, FwdCfg<TIO, G, KD>::MINB) fwd_kernel(const
 #pragma unroll
         for (int k = 0; k < KD; ++k) {
             if (!valid[k]) continue;
-            const int64_t row = (b * nprev + chunk) * D + d0 + c0 + k;
+            const int64_t row = (b * nprev + chunk) * D + d0 + c0 + (k ^ perm);
             float4* S = reinterpret_cast<float4*>(p.ws_S + row * kDS + s0);
 #pragma unroll
             for (int q = 0; q < KP; q += 2) S[q / 2] = make_float4(h[k][q].x, h[k][q].y, h[k][q + 1].x, h[k][q + 1].y);
@@ -721,6 +730,10 @@ cudaError_t launch_fwd_fuse(const FwdLaunch& L, int mode, cudaStream_t stream) {
             if (L.kd == 2) { SSM_FWD_VEC(4, 2, kSingle); }
             SSM_FWD_VEC(4, 1, kSingle);
         case kPass1:
+            if (L.G == 2) {
+                if (L.vec) return launch_fwd_t<TIO, 2, 2, true, kPass1, true, FUSE>(L, stream);
+                return launch_fwd_t<TIO, 2, 2, false, kPass1, true, FUSE>(L, stream);
+            }
             if (L.kd == 2) {
                 if (L.vec) return launch_fwd_t<TIO, 4, 2, true, kPass1, true, FUSE>(L, stream);
                 return launch_fwd_t<TIO, 4, 2, false, kPass1, true, FUSE>(L, stream);
@@ -728,6 +741,7 @@ cudaError_t launch_fwd_fuse(const FwdLaunch& L, int mode, cudaStream_t stream) {
             if (L.vec) return launch_fwd_t<TIO, 4, 1, true, kPass1, true, FUSE>(L, stream);
             return launch_fwd_t<TIO, 4, 1, false, kPass1, true, FUSE>(L, stream);
         case kPass2:
+            if (L.G == 2) { SSM_FWD_VEC(2, 2, kPass2); }
             if (L.kd == 2) { SSM_FWD_VEC(4, 2, kPass2); }
             SSM_FWD_VEC(4, 1, kPass2);
         case kCkptOnly: SSM_FWD_VEC(4, 1, kCkptOnly);

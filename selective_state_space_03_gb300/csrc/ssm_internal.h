@@ -112,28 +112,44 @@ cudaError_t launch_bwd_carry_bf16(const BwdLaunch& L, cudaStream_t stream);
 
 int device_sm_count();
 
-// Schedule of the chunked forward (both passes use 4 lanes per chain; kd channels per lane).
+// Schedule of the chunked forward (both passes use G lanes per chain; kd channels per lane).
 // Two channels per lane whenever that leaves at least 4 pass-2 warps per SM, else one.
 // Chosen by the library (chunk_len == 0): with two channels, chunks for about 21 resident
 // pass-2 warps per SM but at least 128 steps; with one, chunks for about 14 warps per SM, at
-// least 64 steps. Measured on the 2048-chain workloads (after the carry fold's loads were
-// batched): 4096 steps in 22 chunks at two channels 72.3 us, 8 at one 76.4 us (earlier
-// rule); 1024 steps in 8 chunks at two channels 29.4 us, at one 32.4 us.
+// least 64 steps; two-channel chunks are at most 512 steps (with 8192 chains and 4096 steps, 6
+// chunks of 704 steps took 254 us, 8 of 512 228 us). Measured on the 2048-chain workloads (after
+// the carry fold's loads were batched): 4096 steps in 22 chunks at two channels 72.3 us, 8 at one
+// 76.4 us (earlier rule); 1024 steps in 8 chunks at two channels 29.4 us, at one 32.4 us.
+// Lanes per chain G: 2 lanes (8 states each, two channels per lane) from about 40 chains per SM
+// as below, or with a given chunk length when the chunk passes still have about 12 warps per SM
+// that way (the one-pass layout rule); else 4.
 struct ChunkSchedule {
     int64_t Lc;
     int kd;
+    int G;
 };
 inline ChunkSchedule chunk_schedule(int64_t T, int64_t chains, int64_t chunk_len, int64_t sms) {
     auto round32 = [](int64_t v) { return (v + 31) / 32 * 32; };
     auto kd_for = [&](int64_t Lc) { return chains * ((T + Lc - 1) / Lc) >= 64 * sms ? 2 : 1; };
-    if (chunk_len > 0) return {chunk_len, kd_for(chunk_len)};
+    auto with_lanes = [&](int64_t Lc, int kd) {
+        const bool two = kd == 2 && chains * ((T + Lc - 1) / Lc) >= 12 * 32 * sms;
+        return ChunkSchedule{Lc, kd, two ? 2 : 4};
+    };
+    if (chunk_len > 0) return with_lanes(chunk_len, kd_for(chunk_len));
     const int64_t n2 = sms * 336 / chains > 2 ? sms * 336 / chains : 2;
     int64_t L2 = round32((T + n2 - 1) / n2);
     if (L2 < 128) L2 = 128;
-    if (kd_for(L2) == 2) return {L2, 2};
+    if (L2 > 512) L2 = 512;
+    if (kd_for(L2) == 2) {
+        // from about 40 chains per SM: 2 lanes per chain in chunks of 256 steps (4096 steps, bf16,
+        // against 4 lanes in chunks of 512: 8192 chains 228 -> 216 us, 10240 285 -> 259 us, 12288
+        // 335 -> 312 us; at 4096 chains 4 lanes stay ahead, 133 against 130-140 us)
+        if (chains >= 40 * sms && T >= 512) return {256, 2, 2};
+        return with_lanes(L2, 2);
+    }
     const int64_t n1 = sms * 448 / (chains * 4) > 2 ? sms * 448 / (chains * 4) : 2;
     const int64_t L1 = round32((T + n1 - 1) / n1);
-    return {L1 < 64 ? 64 : L1, 1};
+    return {L1 < 64 ? 64 : L1, 1, 4};
 }
 
 }  // namespace ssm

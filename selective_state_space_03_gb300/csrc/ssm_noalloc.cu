@@ -84,8 +84,16 @@ extern "C" ssm_status ssm_scan_fwd_noalloc(const ssm_scan_desc* desc, const void
     }
 
     // chunk length and lanes: the schedule ssm_scan_fwd uses for its chunked scan (with the
-    // caller's chunk length when given)
-    const ChunkSchedule cs = chunk_schedule(d.T, d.B * d.D, d.chunk_len > 0 ? d.chunk_len : 0, device_sm_count());
+    // caller's chunk length when given); a chunk length the library chose is doubled until the
+    // carries fit the scratch array
+    auto carry_bytes = [&](int64_t n) {
+        return up256(size_t(d.B) * size_t(n - 1) * size_t(d.D) * kDS * 4) + up256(size_t(d.B) * size_t(n - 1) * size_t(d.D) * 4);
+    };
+    ChunkSchedule cs = chunk_schedule(d.T, d.B * d.D, d.chunk_len > 0 ? d.chunk_len : 0, device_sm_count());
+    if (d.chunk_len <= 0) {
+        while (cdiv64(d.T, cs.Lc) >= 2 && carry_bytes(cdiv64(d.T, cs.Lc)) > kNoallocScratchBytes)
+            cs = chunk_schedule(d.T, d.B * d.D, cs.Lc * 2, device_sm_count());
+    }
     const int64_t Lc = cs.Lc;
     const int64_t nchunk = cdiv64(d.T, Lc);
     if (nchunk > kMaxChunks) return SSM_ERR_UNSUPPORTED;      // one grid dimension per chunk
@@ -97,7 +105,7 @@ extern "C" ssm_status ssm_scan_fwd_noalloc(const ssm_scan_desc* desc, const void
     L.io = d.io == SSM_IO_BF16 ? IO::BF16 : IO::F32;
     L.vec = (d.D * (d.io == SSM_IO_BF16 ? 2 : 4)) % 16 == 0;
     L.ckpt_only = false;
-    L.G = 4;
+    L.G = cs.G;
     L.kd = cs.kd;
     L.softplus = (d.flags & SSM_SCAN_DELTA_SOFTPLUS) != 0;
     auto run = [&](int mode) {
@@ -109,8 +117,7 @@ extern "C" ssm_status ssm_scan_fwd_noalloc(const ssm_scan_desc* desc, const void
         return run(0) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
     }
     const size_t bytes_S = up256(size_t(d.B) * size_t(nchunk - 1) * size_t(d.D) * kDS * 4);
-    const size_t bytes_Sd = up256(size_t(d.B) * size_t(nchunk - 1) * size_t(d.D) * 4);
-    if (bytes_S + bytes_Sd > kNoallocScratchBytes) return SSM_ERR_WORKSPACE;
+    if (carry_bytes(nchunk) > kNoallocScratchBytes) return SSM_ERR_WORKSPACE;
 
     void* base = nullptr;
     if (scratch_address(&base) != cudaSuccess) return SSM_ERR_CUDA;

@@ -254,6 +254,7 @@ def test_schedule_overrides_exist_only_in_the_testing_build(L):
     # (used by the GPU tests that pin every schedule) has them all
     import selective_state_space_03_gb300 as ssm
     names = [b"SSM_SCAN_FORCE_LANES", b"SSM_SCAN_FORCE_FWD_LAYOUT", b"SSM_SCAN_FORCE_CHUNK_KD",
+             b"SSM_SCAN_FORCE_CHUNK_LAYOUT", b"SSM_SCAN_FORCE_CARRY_SCAN",
              b"SSM_SCAN_FORCE_BWD_KD", b"SSM_SCAN_FORCE_BWD_TPAR", b"SSM_SCAN_LOOKBACK_POLLS",
              b"SSM_SCAN_TEST_LOOKBACK_DROP"]
     release = open(ssm.LIB_PATH, "rb").read()

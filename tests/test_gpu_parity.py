@@ -36,11 +36,13 @@ def ssm():
 
 
 def run_case(w, K, chunk_len=0, seed=0, ghT=False, bwd=True, lanes=None, ckpt_to_bwd=True, bwd_kd=None,
-             bwd_tpar=None, bwd_workspace=None, deterministic=False, fwd_layout=None, chunk_kd=None):
+             bwd_tpar=None, bwd_workspace=None, deterministic=False, fwd_layout=None, chunk_kd=None,
+             chunk_layout=None):
     import torch
     inp = gen.make_inputs(w, seed=seed, with_grad_inputs=bwd, with_ghT=ghT)
     t = dev_inputs(inp)
-    with forced(SSM_SCAN_FORCE_LANES=lanes, SSM_SCAN_FORCE_FWD_LAYOUT=fwd_layout, SSM_SCAN_FORCE_CHUNK_KD=chunk_kd):
+    with forced(SSM_SCAN_FORCE_LANES=lanes, SSM_SCAN_FORCE_FWD_LAYOUT=fwd_layout, SSM_SCAN_FORCE_CHUNK_KD=chunk_kd,
+                SSM_SCAN_FORCE_CHUNK_LAYOUT=chunk_layout):
         y, hT, ckpt = ssm().ssm_scan_fwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], ckpt_interval=K,
                                          chunk_len=chunk_len)
     torch.cuda.synchronize()
@@ -170,29 +172,58 @@ def test_ragged_lengths_and_intervals(T, K, bwd_kd):
     run_case(gen.workload(2, B=2, T=T, D=40, h0_std=0.1), K=K, ghT=True, bwd_kd=bwd_kd)
 
 
-@pytest.mark.parametrize("chunk_kd", [1, 2])
-@pytest.mark.parametrize("chunk_len", [32, 50, 129])
-def test_chunked_ragged_chunks(chunk_len, chunk_kd):
-    run_case(gen.workload(2, B=2, T=230, D=48, h0_std=0.1), K=64, chunk_len=chunk_len, bwd=False, chunk_kd=chunk_kd)
+CHUNK_LAYOUTS = ["4x1", "4x2", "2x2"]      # lanes per chain x channels per lane of the chunk passes
 
 
 @pytest.mark.parametrize("io", ["f32", "bf16"])
-def test_chunked_two_channels_per_lane_unaligned(io):
+@pytest.mark.parametrize("chunk_layout", CHUNK_LAYOUTS)
+@pytest.mark.parametrize("chunk_len", [32, 50, 129])
+def test_chunked_ragged_chunks(chunk_len, chunk_layout, io):
+    run_case(gen.workload(2, B=2, T=230, D=48, io=io, h0_std=0.1), K=64, chunk_len=chunk_len, bwd=False,
+             chunk_layout=chunk_layout)
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("chunk_layout", ["4x2", "2x2"])
+def test_chunked_two_channels_per_lane_unaligned(io, chunk_layout):
     # an odd channel count leaves the last lane's second channel empty; bf16 rows of 20
     # channels are not whole 16-byte chunks
     D = 37 if io == "f32" else 20
-    run_case(gen.workload(2, B=3, T=300, D=D, io=io, h0_std=0.1), K=32, chunk_len=64, bwd=False, chunk_kd=2)
+    run_case(gen.workload(2, B=3, T=300, D=D, io=io, h0_std=0.1), K=32, chunk_len=64, bwd=False,
+             chunk_layout=chunk_layout)
 
 
 @pytest.mark.parametrize("T,chunk_len,scan", [(230, 64, 1), (700, 16, None), (700, 16, 0), (1000, 16, 1),
                                               (16 * 40 + 5, 16, None)])
-@pytest.mark.parametrize("chunk_kd", [1, 2])
-def test_chunked_carry_scan(T, chunk_len, scan, chunk_kd):
-    # the middle pass that folds the chunk carries once per chain (on by default above 32
+@pytest.mark.parametrize("chunk_layout", CHUNK_LAYOUTS)
+def test_chunked_carry_scan(T, chunk_len, scan, chunk_layout):
+    # the middle pass that folds the chunk carries once per chain (on by default above 48
     # carries; forced on or off here) against the oracle: y, hT and checkpoints, ragged last chunk
-    w = gen.workload(2, B=2, T=T, D=40, h0_std=0.1)
+    w = gen.workload(2, B=2, T=T, D=40, h0_std=0.1, io="bf16" if chunk_layout == "2x2" else "f32")
     with forced(SSM_SCAN_FORCE_CARRY_SCAN=scan):
-        run_case(w, K=32, chunk_len=chunk_len, bwd=False, chunk_kd=chunk_kd)
+        run_case(w, K=32, chunk_len=chunk_len, bwd=False, chunk_layout=chunk_layout)
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_chunked_layout_chosen_by_the_library(io):
+    # 12288 chains over 4096 steps: the library picks 8 chunks of 512 steps with 2 lanes per chain
+    # (the workload-3 shape); sampled chains against the oracle, all of them against the one-pass
+    # scan
+    import torch
+    w = gen.workload(3, io=io)
+    inp = gen.make_inputs(w, seed=3, with_grad_inputs=False)
+    t = dev_inputs(inp)
+    y, hT, _ = ssm().ssm_scan_fwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"])
+    y1, hT1, _ = ssm().ssm_scan_fwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], chunk_len=-1)
+    torch.cuda.synchronize()
+    bsel, dsel = np.array([0, 7]), sample_indices(w.D, 12, 9)
+    sub = sub_inputs(inp, bsel, dsel)
+    ref = oracle.fwd(sub["x"], sub["delta"], sub["A"], sub["b"], sub["c"], sub["h0"])
+    bi, di = torch.as_tensor(bsel, device=y.device), torch.as_tensor(dsel, device=y.device)
+    assert_close(to_host(y[bi][:, :, di]), ref["y"], w.io, "fwd", "y")
+    assert_close(to_host(hT[bi][:, di]), ref["hT"], w.io, "fwd", "hT")
+    assert_close(to_host(y), to_host(y1), w.io, "fwd", "y")
+    assert_close(to_host(hT), to_host(hT1), w.io, "fwd", "hT")
 
 
 def test_backward_rebuilds_checkpoints():

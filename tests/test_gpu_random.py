@@ -46,6 +46,7 @@ def draw_case(seed):
         case["D"] += 8 - case["D"] % 8           # both aligned and unaligned rows for bf16
     case["chunk_kd"] = r.choice([None, 1, 2])    # channels per lane of the chunked forward
     case["lookback"] = bool(r.integers(0, 2))    # chunked forward in one launch with look-back
+    case["chunk_layout"] = r.choice([None, "2x2"])   # 2 lanes x 2 channels in the chunk passes
     return case
 
 
@@ -62,7 +63,8 @@ def test_random_case(seed):
     K = cs["K"]
     layout = cs["fwd"] if cs["fwd"] in ("2x2", "4x2", "4x1") else None
     chunk_len = cs["chunk_len"] if cs["fwd"] == "chunked" else (-1 if layout else 0)
-    with forced(SSM_SCAN_FORCE_FWD_LAYOUT=layout, SSM_SCAN_FORCE_CHUNK_KD=cs["chunk_kd"]):
+    with forced(SSM_SCAN_FORCE_FWD_LAYOUT=layout, SSM_SCAN_FORCE_CHUNK_KD=cs["chunk_kd"],
+                SSM_SCAN_FORCE_CHUNK_LAYOUT=cs["chunk_layout"]):
         y, hT, ck = ssm.ssm_scan_fwd(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"], ckpt_interval=K,
                                      chunk_len=chunk_len, D_skip=Ds, delta_softplus=cs["softplus"],
                                      lookback=cs["lookback"])

@@ -67,6 +67,8 @@ def check_against_oracle(inp, K, y, hT, ck, io, bsel=None, dsel=None):
     ref = oracle.fwd(sub["x"], sub["delta"], sub["A"], sub["b"], sub["c"], sub["h0"], ckpt_interval=K)
     assert_close(to_host(pick(y, 2)), ref["y"], io, "fwd", "y")
     assert_close(to_host(pick(hT, 1)), ref["hT"], io, "fwd", "hT")
+    if ck is None:
+        return
     if bsel is None:
         assert_close(to_host(ck), ref["ckpt"], io, "fwd", "ckpt")
     else:
@@ -120,6 +122,22 @@ def test_noalloc_at_its_scratch_limit(L):
     fake = ctypes.c_void_p(0x7F0000000000)
     st = L.ssm_scan_fwd_noalloc(ctypes.byref(desc), fake, fake, fake, fake, fake, None, fake, None, None, None)
     assert st == 4
+
+
+def test_noalloc_library_chunks_grow_to_fit_its_scratch(L):
+    # B = 2, D = 4096, T = 16384 with the chunk length left to the library: its 512-step chunks
+    # would need 31 carries of 8192 chains (17.3 MB), so it takes 16 chunks of 1024 (8,355,840
+    # bytes); sampled channels against the oracle
+    import torch
+    import selective_state_space_03_gb300 as ssm
+    from gpu_util import sample_indices
+    w = gen.workload(5, B=2, T=16384, D=4096)
+    assert 31 * 8192 * 68 > (8 << 20) >= 15 * 8192 * 68
+    inp = gen.make_inputs(w, seed=7, with_grad_inputs=False)
+    t = dev_inputs(inp)
+    y, hT, _ = ssm.ssm_scan_fwd_noalloc(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"])
+    torch.cuda.synchronize()
+    check_against_oracle(inp, 0, y, hT, None, w.io, bsel=np.array([0, 1]), dsel=sample_indices(w.D, 16, 8))
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch(L):
