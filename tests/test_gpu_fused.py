@@ -88,8 +88,10 @@ def test_fused_chunked_forward_chunk_parallel_backward(io):
 
 
 @pytest.mark.parametrize("io", ["f32", "bf16"])
-def test_fused_chunked_forward_two_channels_per_lane(io):
-    with forced(SSM_SCAN_FORCE_CHUNK_KD=2):
+@pytest.mark.parametrize("chunk_layout", ["4x2", "2x2"])
+def test_fused_chunked_forward_two_channels_per_lane(io, chunk_layout):
+    # softplus prologue and skip epilogue in both chunk passes, with 4 or 2 lanes per chain
+    with forced(SSM_SCAN_FORCE_CHUNK_LAYOUT=chunk_layout):
         fused_case(gen.workload(2, B=2, T=230, D=40, io=io, h0_std=0.1), K=50, chunk_len=50, kd=2, tpar=0)
 
 
