@@ -125,14 +125,14 @@ def test_noalloc_at_its_scratch_limit(L):
 
 
 def test_noalloc_library_chunks_grow_to_fit_its_scratch(L):
-    # B = 2, D = 4096, T = 16384 with the chunk length left to the library: its 512-step chunks
-    # would need 31 carries of 8192 chains (17.3 MB), so it takes 16 chunks of 1024 (8,355,840
-    # bytes); sampled channels against the oracle
+    # B = 2, D = 4096, T = 16384 with the chunk length left to the library: its 256-step chunks
+    # would need 63 carries of 8192 chains (35 MB) and 512-step ones 31 (17.3 MB), so it takes 16
+    # chunks of 1024 (8,355,840 bytes); sampled channels against the oracle
     import torch
     import selective_state_space_03_gb300 as ssm
     from gpu_util import sample_indices
     w = gen.workload(5, B=2, T=16384, D=4096)
-    assert 31 * 8192 * 68 > (8 << 20) >= 15 * 8192 * 68
+    assert 63 * 8192 * 68 > 31 * 8192 * 68 > (8 << 20) >= 15 * 8192 * 68
     inp = gen.make_inputs(w, seed=7, with_grad_inputs=False)
     t = dev_inputs(inp)
     y, hT, _ = ssm.ssm_scan_fwd_noalloc(t["x"], t["delta"], t["A"], t["b"], t["c"], t["h0"])
