@@ -194,7 +194,9 @@ def test_chunked_two_channels_per_lane_unaligned(io, chunk_layout):
 
 
 @pytest.mark.parametrize("T,chunk_len,scan", [(230, 64, 1), (700, 16, None), (700, 16, 0), (1000, 16, 1),
-                                              (16 * 40 + 5, 16, None)])
+                                              (16 * 40 + 5, 16, None),
+                                              # 32 and 64 carries: one and two per lane of the scan
+                                              (33 * 16, 16, 1), (65 * 16, 16, 1)])
 @pytest.mark.parametrize("chunk_layout", CHUNK_LAYOUTS)
 def test_chunked_carry_scan(T, chunk_len, scan, chunk_layout):
     # the middle pass that folds the chunk carries once per chain (on by default above 48
