@@ -90,12 +90,13 @@ FwdPlan plan_fwd(const ssm_scan_desc& d) {
     // Chosen by the library: chunked when one pass would leave fewer than about 16 warps per SM
     // (4 lanes per chain), and for long sequences up to about 84 chains per SM, where the one-pass
     // grid leaves one or two warps per SMSP and the second sweep over T costs less than the
-    // latency it hides (4096 steps, bf16: 8192 chains 251 -> 228 us, 10240 chains 341 -> 285 us,
-    // 12288 chains 343 -> 334 us; 16384 chains one pass 347 us, chunked 427 us).
+    // latency it hides (4096 steps, bf16, one pass -> chunked: 8192 chains 298 -> 216 us, 10240
+    // chains 341 -> 259 us, 12288 chains 343 -> 310 us; 16384 chains one pass 349 us, chunked
+    // 382-431 us).
     const bool few_chains = chains * 4 * 2 < want ||
                             (chains < int64_t(device_sm_count()) * 84 && d.T >= 2048);
     bool chunked = false;
-    ChunkSchedule cs{0, 1};
+    ChunkSchedule cs{0, 1, 4};
     if (d.chunk_len > 0 || (d.chunk_len == 0 && few_chains && d.T >= 256)) {
         cs = chunk_schedule(d.T, chains, d.chunk_len, device_sm_count());
         chunked = cdiv(d.T, cs.Lc) >= 2;
