@@ -20,7 +20,15 @@
 
 namespace ssm {
 
+#ifdef SSM_SCAN_TESTING
+// testing build only: the SM count the schedule queries assume (0 = the device's)
+thread_local int g_test_sms = 0;
+#endif
+
 int device_sm_count() {
+#ifdef SSM_SCAN_TESTING
+    if (g_test_sms > 0) return g_test_sms;
+#endif
     static std::atomic<int> cache[64];      // per device, filled on first use (0 = not yet)
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) {
@@ -137,7 +145,7 @@ FwdPlan plan_fwd(const ssm_scan_desc& d) {
         // channels (16 per warp) from about 4 warps per SM, else 4 lanes x 1 channel (8).
         const int64_t sms = device_sm_count();
         P.G = chains >= sms * 12 * 32 ? 2 : 4;
-        P.kd = (P.G == 4 && chains >= sms * 4 * 16) ? 2 : 1;
+        P.kd = (P.G == 2 || chains >= sms * 4 * 16) ? 2 : 1;
         // testing build only: force the layout ("2x2", "4x2", "4x1"; the older SSM_SCAN_FORCE_LANES
         // takes 2 for 2x2 and 4 for 4x1)
         if (const char* env = SSM_TEST_ENV("SSM_SCAN_FORCE_LANES")) {
@@ -480,3 +488,26 @@ ssm_status ssm_scan_bwd(const ssm_scan_desc* desc, const void* x, const void* de
 }
 
 }  // extern "C"
+
+#ifdef SSM_SCAN_TESTING
+// Testing build only: the schedule the library would choose for desc on a GPU with `sms` SMs,
+// computed on the host without touching a device. out[0..4]: forward mode (0 one pass,
+// 2 chunked, 4 chunked with look-back), lanes per chain, channels per lane, chunk length,
+// chunks; out[5..7]: backward channels per lane, chunk-parallel (0/1), its chunk length.
+extern "C" int ssm_testing_schedule(const ssm_scan_desc* desc, int sms, int64_t* out) {
+    if (desc == nullptr || out == nullptr || sms <= 0) return SSM_ERR_INVALID_ARG;
+    ssm::g_test_sms = sms;
+    const ssm::FwdPlan P = ssm::plan_fwd(*desc);
+    out[0] = P.mode;
+    out[1] = P.G;
+    out[2] = P.kd;
+    out[3] = P.Lc;
+    out[4] = P.nchunk;
+    const bool tpar = ssm::bwd_chunk_parallel(*desc);
+    out[5] = tpar ? 1 : ssm::bwd_channels_per_lane(*desc);
+    out[6] = tpar ? 1 : 0;
+    out[7] = ssm::bwd_internal_K(*desc);
+    ssm::g_test_sms = 0;
+    return SSM_OK;
+}
+#endif

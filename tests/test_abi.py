@@ -267,3 +267,37 @@ def test_schedule_overrides_exist_only_in_the_testing_build(L):
     assert T is not L and ssm.lib() is L
     for name in declared_functions():
         assert hasattr(T, name), name
+
+
+# The schedule the library chooses, computed on the host by the testing build for a GB300's 152
+# SMs (no device needed): each workload's forward (mode 0 one pass / 2 chunked / 4 chunked in one
+# launch, lanes per chain, channels per lane, chunk length, chunks) and backward (channels per
+# lane, chunk-parallel, its chunk length), as measured and documented for each shape.
+SCHEDULES = [
+    # (B, T, D, io, K, chunk_len, flags) -> forward, backward
+    ((16, 2048, 5120, 1, 256, 0, 0), (0, 2, 2, 2048, 1), (2, 0, 256)),   # workload 5
+    ((8, 4096, 1536, 1, 0, 0, 0), (2, 2, 2, 256, 16), (1, 1, 256)),      # workload 3
+    ((1, 4096, 2048, 0, 0, 0, 0), (2, 4, 2, 192, 22), (1, 1, 256)),      # one call of workload 4
+    ((8, 1024, 256, 0, 256, 0, 0), (2, 4, 2, 128, 8), (1, 1, 256)),      # workload 2
+    ((2, 64, 32, 0, 16, 0, 0), (0, 4, 1, 64, 1), (1, 1, 16)),            # workload 1
+    ((8, 4096, 2048, 1, 0, 0, 0), (0, 4, 2, 4096, 1), (1, 1, 256)),      # 16384 chains: one pass
+    ((8, 4096, 1536, 1, 0, -1, 0), (0, 4, 2, 4096, 1), (1, 1, 256)),     # one pass asked for
+    ((8, 4096, 1536, 1, 0, 100, 0), (2, 2, 2, 100, 41), (1, 1, 256)),    # chunk length given
+    ((1, 4096, 2048, 0, 0, 0, 4), (4, 4, 2, 192, 22), (1, 1, 256)),      # look-back flag
+]
+
+
+@pytest.mark.parametrize("case,fwd_plan,bwd_plan", SCHEDULES)
+def test_schedule_choices(L, case, fwd_plan, bwd_plan):
+    import selective_state_space_03_gb300 as ssm
+    B, T, D, io, K, chunk_len, flags = case
+    d = ssm.make_desc(B, T, D, 16, io, K, chunk_len, flags)
+    out = (ctypes.c_int64 * 8)()
+    with ssm.testing_library():
+        T_lib = ssm.lib()
+        T_lib.ssm_testing_schedule.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]
+        T_lib.ssm_testing_schedule.restype = ctypes.c_int
+        assert T_lib.ssm_testing_schedule(ctypes.byref(d), 152, out) == 0
+    assert tuple(out[:5]) == fwd_plan, tuple(out[:5])
+    assert tuple(out[5:]) == bwd_plan, tuple(out[5:])
+
