@@ -304,8 +304,7 @@ __global__ void __launch_bounds__(128, 3) bwd2_kernel(const BwdLaunch p) {
             for (int k = 0; k < 2; ++k)
 #pragma unroll
                 for (int q = 0; q < KP; ++q) hp2[k][q] = make_float2(h[k][2 * q], h[k][2 * q + 1]);
-#pragma unroll 8
-            for (int r = 0; r < LS; ++r) {
+            auto level2_step = [&](int r) {
                 const float4 v = conv1[r * C::CROW + pc];                                   // d0, d0 x0, d1, d1 x1
                 const float4 b4 = *reinterpret_cast<const float4*>(bf + r * kDS + s0);
                 const float2 bp[KP] = {make_float2(b4.x, b4.y), make_float2(b4.z, b4.w)};
@@ -318,6 +317,21 @@ __global__ void __launch_bounds__(128, 3) bwd2_kernel(const BwdLaunch p) {
                         const float2 e = __fmul2_rn(dl2[k], A2[k][q]);
                         hp2[k][q] = __ffma2_rn(make_float2(ex2(e.x), ex2(e.y)), hp2[k][q], __fmul2_rn(dx2[k], bp[q]));
                     }
+            };
+            if (i + 1 < nsub) {
+#pragma unroll 8
+                for (int r = 0; r < LS; ++r) level2_step(r);
+            } else {
+                // the chunk's last sub-chunk, which the reverse takes first: its states go straight
+                // into the window, so the reverse skips level 3 for it
+#pragma unroll 8
+                for (int r = 0; r < LS; ++r) {
+                    level2_step(r);
+                    const float hv[8] = {hp2[0][0].x, hp2[0][0].y, hp2[0][1].x, hp2[0][1].y,
+                                         hp2[1][0].x, hp2[1][0].y, hp2[1][1].x, hp2[1][1].y};
+                    tmem_st8(tw + uint32_t(r * HS), hv);
+                }
+                tmem_wait_st();
             }
 #pragma unroll
             for (int k = 0; k < 2; ++k)
@@ -358,8 +372,9 @@ __global__ void __launch_bounds__(128, 3) bwd2_kernel(const BwdLaunch p) {
             pend_t0 = t0;
             pend_lim = ce;
 
-            // level 3: states of this sub-chunk into the window (8 columns per step)
-            {
+            // level 3: states of this sub-chunk into the window (8 columns per step); the first
+            // sub-chunk of the reverse (the chunk's last) was written by level 2
+            if (ii > 0) {
                 float2 hc[2][KP];
 #pragma unroll
                 for (int k = 0; k < 2; ++k)
