@@ -52,10 +52,10 @@ def load_peaks():
 
 
 # DRAM bytes (read + write) of one bwd2_kernel launch at workload 5, from an ncu capture of
-# the same kernel at T = 512 (691.4 MB): traffic grows with the number of steps, so 4 x that
-# at T = 2048. Reset to None whenever the kernel changes until it is captured again.
-BWD2_TRAFFIC = {"bytes_per_launch": 4 * 692.50176e6,
-                "source": "ncu dram__bytes_read+write of bwd2_kernel at T=512 (692.5 MB) x 4 steps ratio"}
+# the same kernel at T = 512 (344.0 + 344.7 MB): traffic grows with the number of steps, so
+# 4 x that at T = 2048. Reset to None whenever the kernel changes until it is captured again.
+BWD2_TRAFFIC = {"bytes_per_launch": 4 * 688.759808e6,
+                "source": "ncu dram__bytes_read+write of bwd2_kernel at T=512 (688.8 MB) x 4 steps ratio"}
 
 # ---------------------------------------------------------------- algorithmic work per element
 
