@@ -304,8 +304,8 @@ __global__ void __launch_bounds__(128, 4) bwd_kernel(const BwdLaunch p) {
             if (i + 1 < nsub) stage(cs + int64_t(i + 1) * LS, ce, false);
             sub[i * NT + tid] = make_float4(h[0], h[1], h[2], h[3]);
             float2 h2[2] = {make_float2(h[0], h[1]), make_float2(h[2], h[3])};
-#pragma unroll 4
-            for (int r = 0; r < LS; ++r) {
+            // one step; with `window`, the step's state and b also go into the TMEM window
+            auto level2_step = [&](int r, bool window) {
                 const float2 v = *reinterpret_cast<const float2*>(conv + r * C::CROW + c);   // delta, delta*x
                 const float4 b4 = *reinterpret_cast<const float4*>(bf + r * kDS + s0);
                 const float2 bp[2] = {make_float2(b4.x, b4.y), make_float2(b4.z, b4.w)};
@@ -315,6 +315,20 @@ __global__ void __launch_bounds__(128, 4) bwd_kernel(const BwdLaunch p) {
                     const float2 e = __fmul2_rn(dl2, A2[q]);
                     h2[q] = __ffma2_rn(make_float2(ex2(e.x), ex2(e.y)), h2[q], __fmul2_rn(dx2, bp[q]));
                 }
+                if (window) {
+                    tmem_st4(tw + uint32_t(r * KS), h2[0].x, h2[0].y, h2[1].x, h2[1].y);
+                    tmem_st4(tw + C::TMEM_B + uint32_t(r * KS), b4.x, b4.y, b4.z, b4.w);
+                }
+            };
+            if (i + 1 < nsub) {
+#pragma unroll 4
+                for (int r = 0; r < LS; ++r) level2_step(r, false);
+            } else {
+                // the chunk's last sub-chunk, which the reverse takes first: its window is written
+                // here, so the reverse skips level 3 for it
+#pragma unroll 4
+                for (int r = 0; r < LS; ++r) level2_step(r, true);
+                tmem_wait_st();
             }
             h[0] = h2[0].x; h[1] = h2[0].y; h[2] = h2[1].x; h[3] = h2[1].y;
         }
@@ -339,7 +353,7 @@ __global__ void __launch_bounds__(128, 4) bwd_kernel(const BwdLaunch p) {
                 const float4 v = sub[i * NT + tid];
                 hs[0] = v.x; hs[1] = v.y; hs[2] = v.z; hs[3] = v.w;
             }
-            {
+            if (ii > 0) {       // (the chunk's last sub-chunk: written by level 2)
                 float2 hc[2] = {make_float2(hs[0], hs[1]), make_float2(hs[2], hs[3])};
 #pragma unroll
                 for (int r = 0; r < LS; ++r) {
